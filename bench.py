@@ -1,0 +1,511 @@
+"""Benchmark: the per-tensor-scaled E4M3 GEMM path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input,
+the 8192 x 8192 x 8192 E4M3 workload with E4M3 output:
+    amax(A), amax(B) -> scale = amax/448 -> quantise(A), quantise(B)
+    -> tensor-core GEMM, D = E4M3(sA*sB*(A_q @ B_q^T) / sD)
+with FP32 A and B resident in HBM (2 x 268 MB, larger than the 129 MB L2).
+`value` is whole-step throughput in TFLOPS (2*M*N*K per step); `roofline`
+rates the dominant kernel (the GEMM) on its own CUDA-event launch time;
+`e2e` repeats the step through the public API with the FP32 inputs copied
+from pinned host memory and D copied back inside the timed region; `extra`
+lists kernel-level numbers for the other workloads (decode QKV GEMV GB/s,
+4096^3 FP8 and FP16 TFLOPS, amax/quantise GB/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl own|reference]
+
+`--impl reference` times the CPU oracle (the only reference this method has)
+on the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M = N = K = 8192
+FLOP_PER_STEP = 2.0 * M * N * K
+WORKLOAD = "fp8_8192_e4m3out"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+GEMM_SOURCES = [os.path.join(ROOT, "fp16_tensor_core_gb300", "csrc", f)
+                for f in ("k_gemm_tc.cu", "dg_ptx.cuh")]
+
+
+# ---------------------------------------------------------------- plumbing
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["own", "reference"], default="own")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload kernel numbers")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in GEMM_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256_16") != gemm_source_hash() or rec.get("workload") != WORKLOAD:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                             "hw": parts[5], "hwth": parts[6], "swth": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        pmax = max(r["power"] for r in rows)
+        load = [r for r in rows if r["power"] >= 0.5 * pmax] or rows
+        reasons = set()
+        for r in load:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwth"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swth"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": pmax}
+
+
+# ------------------------------------------------------------ own workload
+
+class Workload:
+    """Device buffers for one step of the 8192^3 E4M3-output path."""
+
+    def __init__(self, torch, dg, A32, B32, sd: float):
+        self.torch, self.dg = torch, dg
+        dev = "cuda"
+        self.A = torch.from_numpy(A32).to(dev)
+        self.B = torch.from_numpy(B32).to(dev)
+        f = lambda: torch.zeros(4, dtype=torch.float32, device=dev)  # noqa: E731
+        self.amax_a, self.amax_b, self.sa, self.sb, self.sd = f(), f(), f(), f(), f()
+        self.sd[0] = sd
+        self.qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        self.qb = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        self.D = torch.empty((M, N), dtype=torch.uint8, device=dev)
+
+    def step(self, stream, ev=None):
+        dg = self.dg
+        dg.dg_amax(self.A, self.amax_a, self.sa, stream=stream)
+        dg.dg_amax(self.B, self.amax_b, self.sb, stream=stream)
+        dg.dg_quantize_e4m3(self.A, self.sa, self.qa, stream=stream)
+        dg.dg_quantize_e4m3(self.B, self.sb, self.qb, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        dg.dg_fp8_gemm(self.qa, self.qb, self.D, self.sa, self.sb, self.sd, dg.DG_E4M3,
+                       stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    KERNELS_PER_STEP = 7  # 2 x (amax + scale), 2 x quantise, 1 GEMM
+
+
+def time_kernel(torch, stream, fn, iters: int, warmup: int = 3) -> float:
+    """Mean milliseconds per call of fn(i) measured with CUDA events."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for i in range(iters):
+        fn(i)
+    e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def extras(torch, dg, synth, stream, peaks) -> dict:
+    """Kernel-level numbers for the other workloads (L2 defeated by rotating
+    several copies of every operand that would otherwise stay resident)."""
+    out = {}
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    dev = "cuda"
+
+    def codes(shape, seed):
+        # any E4M3 code pattern works for timing; NaN codes are avoided
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        t = torch.randint(0, 256, shape, dtype=torch.uint8, device=dev, generator=g)
+        return torch.where((t & 0x7F) == 0x7F, torch.zeros_like(t), t)
+
+    one = torch.ones(4, dtype=torch.float32, device=dev)
+    sd = torch.ones(4, dtype=torch.float32, device=dev)
+
+    # decode QKV projection: A [1,4096], B [12288,4096], BF16 out
+    Mq, Nq, Kq = 1, 12288, 4096
+    nb = int(3 * l2 // (Nq * Kq)) + 1
+    As = [codes((Mq, Kq), 10 + i) for i in range(nb)]
+    Bs = [codes((Nq, Kq), 20 + i) for i in range(nb)]
+    Dq = torch.empty((Mq, Nq), dtype=torch.bfloat16, device=dev)
+    ms = time_kernel(torch, stream, lambda i: dg.dg_fp8_gemm(As[i % nb], Bs[i % nb], Dq, one, one,
+                                                             None, dg.DG_BF16, stream=stream), 200)
+    qkv_bytes = Nq * Kq + Mq * Kq + Mq * Nq * 2
+    out["qkv_gemv_1x12288x4096"] = {"us": ms * 1e3, "GB/s": qkv_bytes / (ms * 1e-3) / 1e9,
+                                    "frac_hbm": qkv_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                    "bytes": qkv_bytes, "l2": f"{nb} rotating copies"}
+    del As, Bs
+
+    # 4096^3 FP8 (BF16 out) and FP16 (FP16 out)
+    S = 4096
+    flop = 2.0 * S ** 3
+    As = [codes((S, S), 30 + i) for i in range(4)]
+    Bs = [codes((S, S), 40 + i) for i in range(4)]
+    D = torch.empty((S, S), dtype=torch.bfloat16, device=dev)
+    ms = time_kernel(torch, stream, lambda i: dg.dg_fp8_gemm(As[i % 4], Bs[i % 4], D, one, one, None,
+                                                             dg.DG_BF16, stream=stream), 50)
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    out["fp8_gemm_4096"] = {"us": ms * 1e3, "TFLOPS": flop / (ms * 1e-3) / 1e12,
+                            "frac_fp8_peak": flop / (ms * 1e-3) / 1e12 / fp8_peak}
+    del As, Bs
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    Hs = [(torch.rand((S, S), device=dev, generator=g) * 2 - 1).half() for _ in range(4)]
+    Hb = [(torch.rand((S, S), device=dev, generator=g) * 2 - 1).half() for _ in range(4)]
+    Dh = torch.empty((S, S), dtype=torch.float16, device=dev)
+    ms = time_kernel(torch, stream, lambda i: dg.dg_hgemm(Hs[i % 4], Hb[i % 4], Dh, dg.DG_FP16,
+                                                          stream=stream), 30)
+    out["fp16_hgemm_4096"] = {"us": ms * 1e3, "TFLOPS": flop / (ms * 1e-3) / 1e12,
+                              "frac_fp16_peak": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+    del Hs, Hb, Dh, D
+
+    # amax and quantise on an 8192^2 FP32 tensor (268 MB, > L2)
+    x = torch.randn((8192, 8192), device=dev)
+    am = torch.zeros(4, dtype=torch.float32, device=dev)
+    sc = torch.zeros(4, dtype=torch.float32, device=dev)
+    q = torch.empty((8192, 8192), dtype=torch.uint8, device=dev)
+    n = x.numel()
+    ms = time_kernel(torch, stream, lambda i: dg.dg_amax(x, am, sc, stream=stream), 50)
+    out["amax_8192sq"] = {"us": ms * 1e3, "GB/s": 4 * n / (ms * 1e-3) / 1e9,
+                          "frac_hbm": 4 * n / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    ms = time_kernel(torch, stream, lambda i: dg.dg_quantize_e4m3(x, sc, q, stream=stream), 50)
+    out["quantise_8192sq"] = {"us": ms * 1e3, "GB/s": 5 * n / (ms * 1e-3) / 1e9,
+                              "frac_hbm": 5 * n / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    return out
+
+
+def cpu_baseline_sample(A32, B32, sd: float, rows: int) -> dict:
+    """The oracle, as it stands, on `rows` rows of A against all of B: full
+    amax/scale of A and B, quantise of the sampled rows and all of B, the
+    FP64 contraction and the E4M3 epilogue."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    sa = oracle.scale_from_amax(oracle.amax(A32))
+    sb = oracle.scale_from_amax(oracle.amax(B32))
+    qa = oracle.quantize_e4m3(A32[:rows], sa)
+    qb = oracle.quantize_e4m3(B32, sb)
+    R = oracle.gemm_e4m3(qa, qb, with_abs=False)
+    oracle.epilogue_e4m3(R, sa, sb, np.float32(sd))
+    dt = time.perf_counter() - t0
+    cores = os.cpu_count() or 1
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        pass
+    return {"seconds": dt, "flop": 2.0 * rows * N * K, "cores": cores}
+
+
+def run_own(args):
+    import numpy as np
+    import torch
+
+    import fp16_tensor_core_gb300 as dg
+    import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dg.dg_init()
+    peaks = load_peaks()
+    sd = json.load(open(os.path.join(ROOT, "tests", "golden", "sd_8192.json")))["scale_d"]
+
+    A32, B32 = synth.make_inputs(WORKLOAD)
+    wl = Workload(torch, dg, A32, B32, sd)
+    stream = torch.cuda.current_stream()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    # keep the GPU busy for ~1.5 s before the timed region so that the clock
+    # sampler (100 ms period) sees the step under sustained load
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        wl.step(stream)
+        torch.cuda.synchronize()
+    st = dg.dg_sync_status()
+    assert st == dg.DG_OK, dg.dg_status_string(st)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_s, t_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_s.record(stream)
+    for i in range(args.steps):
+        wl.step(stream, evs[i])
+    t_e.record(stream)
+    t_e.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_local = t_s.elapsed_time(t_e)
+    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    st = dg.dg_sync_status()
+    assert st == dg.DG_OK, dg.dg_status_string(st)
+    ms_total = reduce_max(ms_local, world, device=f"cuda:{local}")
+    ms_step = ms_total / args.steps
+    value = world * FLOP_PER_STEP / (ms_step * 1e-3) / 1e12
+
+    # end to end: pinned host FP32 inputs in, E4M3 D out, every step
+    hA = torch.from_numpy(A32).pin_memory()
+    hB = torch.from_numpy(B32).pin_memory()
+    hD = torch.empty((M, N), dtype=torch.uint8).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        wl.A.copy_(hA, non_blocking=True)
+        wl.B.copy_(hB, non_blocking=True)
+        wl.step(stream)
+        hD.copy_(wl.D, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e_e.record(stream)
+    e_e.synchronize()
+    e2e_ms = reduce_max(e_s.elapsed_time(e_e), world, device=f"cuda:{local}") / e2e_steps
+    st = dg.dg_sync_status()
+    assert st == dg.DG_OK, dg.dg_status_string(st)
+
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    achieved = FLOP_PER_STEP / (gemm_ms * 1e-3) / 1e12
+    traffic = recorded_traffic()
+    line = {
+        "metric": "FP8 GEMM TFLOPS (and GB/s at M=1) on 1 GB300, % of roofline",
+        "value": value,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {
+            "workload": "FP8 E4M3 GEMM 8192x8192x8192, E4M3 output, per-tensor scales",
+            "M": M, "N": N, "K": K,
+            "step": "amax(A), amax(B) -> scale -> quantise(A), quantise(B) -> GEMM (E4M3 out)",
+            "inputs": "FP32 A, B ~ N(0,1) seed 0, resident in HBM; sD from tests/golden/sd_8192.json",
+            "l2": "inputs larger than L2 (2 x 268 MB FP32 per step), no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "gemm_tc_kernel (tcgen05 E4M3, 128x256 tiles)",
+            "achieved": achieved,
+            "peak": fp8_peak,
+            "unit": "TFLOP/s",
+            "frac": achieved / fp8_peak,
+            "peak_source": f"{peaks['source']}: bf16 burst {peaks['bf16_tflops']} x 2 (FP8/BF16 dense ratio)",
+            "launch_ms": gemm_ms,
+            "traffic": traffic,
+        },
+        "e2e": {"value": world * FLOP_PER_STEP / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": A32.nbytes + B32.nbytes,
+                "d2h_bytes_per_step": M * N},
+        "gpu_launches": Workload.KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    del hA, hB, hD
+    if rank == 0 and not args.no_extra:
+        line["extra"] = extras(torch, dg, synth, stream, peaks)
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_baseline_sample(A32, B32, sd, rows=768)
+        line["cpu_baseline"] = {
+            "value": cb["flop"] / cb["seconds"] / 1e12, "unit": "TFLOPS", "cores": cb["cores"],
+            "kind": "oracle", "seconds": cb["seconds"],
+            "sample": "rows 0-767 of A against all 8192 rows of B (768x8192x8192): full-tensor "
+                      "amax/scale of A and B, quantise of the sampled rows and all of B, FP64 "
+                      "contraction, E4M3 epilogue"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The oracle on the host cores, on bounded samples of the same workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+
+    import synth
+    sd = json.load(open(os.path.join(ROOT, "tests", "golden", "sd_8192.json")))["scale_d"]
+    A32, B32 = synth.make_inputs(WORKLOAD)
+    rows = 64
+    for _ in range(args.warmup):
+        cpu_baseline_sample(A32, B32, sd, rows)
+    times, cores = [], 1
+    for _ in range(args.steps):
+        r = cpu_baseline_sample(A32, B32, sd, rows)
+        times.append(r["seconds"])
+        cores = r["cores"]
+    sec = statistics.mean(times)
+    value = 2.0 * rows * N * K / sec / 1e12
+    sample = (f"each step: rows 0-{rows - 1} of A against all 8192 rows of B ({rows}x8192x8192): "
+              "full-tensor amax/scale, quantise, FP64 contraction, E4M3 epilogue")
+    line = {
+        "metric": "FP8 GEMM TFLOPS (and GB/s at M=1) on 1 GB300, % of roofline",
+        "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": "FP8 E4M3 GEMM 8192x8192x8192, E4M3 output, per-tensor scales",
+                   "M": M, "N": N, "K": K, "sampled_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_own(args)
+
+
+if __name__ == "__main__":
+    main()

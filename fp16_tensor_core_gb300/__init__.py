@@ -1,0 +1,175 @@
+"""Python binding of libdg (include/dg.h): argument marshalling only.
+
+Every function below has the name of the C entry point it calls and does no
+arithmetic of its own: it turns torch tensors (device memory) into pointers
+and sizes, calls the library, and raises DgError on a non-zero status.
+PyTorch is used only for device memory and streams.  There is no fallback:
+if ``_build/libdg.so`` has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "DG_OK", "DG_ERR_INVALID_VALUE", "DG_ERR_MISALIGNED", "DG_ERR_UNSUPPORTED",
+    "DG_ERR_CUDA", "DG_ERR_TIMEOUT", "DG_BF16", "DG_E4M3", "DG_FP16", "DgError",
+    "lib", "library_path", "dg_amax", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_hgemm",
+    "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
+    "dg_debug_skip_first_load", "dg_status_string", "dg_version", "EXPORTED_SYMBOLS",
+]
+
+DG_OK, DG_ERR_INVALID_VALUE, DG_ERR_MISALIGNED, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_TIMEOUT = range(6)
+DG_BF16, DG_E4M3, DG_FP16 = 0, 1, 2
+
+#: Every function include/dg.h declares.
+EXPORTED_SYMBOLS = (
+    "dg_amax", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_hgemm", "dg_gemm_plan",
+    "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
+    "dg_status_string", "dg_version",
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libdg.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+class DgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {dg_status_string(status)} ({status})")
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("path", "block_m", "block_n", "block_k", "stages", "grid", "tiles", "smem_bytes")]
+
+
+def lib():
+    """The loaded libdg (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"libdg.so not found at {_LIB_PATH}; build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(_LIB_PATH)
+            vp, i64, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            L.dg_amax.argtypes = [vp, i64, vp, vp, vp]
+            L.dg_quantize_e4m3.argtypes = [vp, i64, vp, vp, vp]
+            L.dg_fp8_gemm.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, ctypes.c_int, vp]
+            L.dg_hgemm.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]
+            L.dg_gemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(_Plan)]
+            L.dg_init.argtypes = []
+            L.dg_sync_status.argtypes = [vp]
+            L.dg_set_wait_timeout_us.argtypes = [ctypes.c_uint64]
+            L.dg_set_wait_timeout_us.restype = None
+            L.dg_debug_skip_first_load.argtypes = [ctypes.c_int]
+            L.dg_debug_skip_first_load.restype = None
+            L.dg_status_string.argtypes = [ctypes.c_int]
+            L.dg_status_string.restype = ctypes.c_char_p
+            L.dg_version.argtypes = []
+            for name in ("dg_amax", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_hgemm",
+                         "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_version"):
+                getattr(L, name).restype = st
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != DG_OK:
+        raise DgError(rc, where)
+
+
+def dg_status_string(status: int) -> str:
+    return lib().dg_status_string(int(status)).decode()
+
+
+def dg_version() -> int:
+    return lib().dg_version()
+
+
+def dg_init() -> None:
+    _check(lib().dg_init(), "dg_init")
+
+
+def dg_amax(x, amax_out, scale_out=None, stream=None) -> None:
+    """amax_out[0] = max |x|; scale_out[0] = amax / 448 (1 if amax == 0)."""
+    _check(lib().dg_amax(_ptr(x), x.numel(), _ptr(amax_out), _ptr(scale_out), _stream(stream)),
+           "dg_amax")
+
+
+def dg_quantize_e4m3(x, scale, q, stream=None) -> None:
+    """q = E4M3(x / scale[0]) elementwise (uint8 codes)."""
+    if q.numel() != x.numel():
+        raise ValueError("q must have as many elements as x")
+    _check(lib().dg_quantize_e4m3(_ptr(x), x.numel(), _ptr(scale), _ptr(q), _stream(stream)),
+           "dg_quantize_e4m3")
+
+
+def dg_fp8_gemm(A, B, D, scale_a, scale_b, scale_d=None, out=DG_BF16, stream=None,
+                M=None, N=None, K=None) -> None:
+    """D (M x N) = out(scale_a * scale_b * A (M x K, E4M3) @ B (N x K, E4M3)^T)."""
+    if M is None:
+        M, K = A.shape
+        N = B.shape[0]
+    _check(lib().dg_fp8_gemm(_ptr(A), _ptr(B), _ptr(D), M, N, K, _ptr(scale_a), _ptr(scale_b),
+                             _ptr(scale_d), int(out), _stream(stream)), "dg_fp8_gemm")
+
+
+def dg_hgemm(A, B, D, out=DG_FP16, stream=None, M=None, N=None, K=None) -> None:
+    """D (M x N) = out(A (M x K, FP16) @ B (N x K, FP16)^T), FP32 accumulation."""
+    if M is None:
+        M, K = A.shape
+        N = B.shape[0]
+    _check(lib().dg_hgemm(_ptr(A), _ptr(B), _ptr(D), M, N, K, int(out), _stream(stream)),
+           "dg_hgemm")
+
+
+def dg_gemm_plan(M, N, K, in_dtype=DG_E4M3, out_dtype=DG_BF16, sm_count=0) -> dict:
+    """The path and tile the library picks for this shape (host only)."""
+    p = _Plan()
+    _check(lib().dg_gemm_plan(M, N, K, int(in_dtype), int(out_dtype), int(sm_count),
+                              ctypes.byref(p)), "dg_gemm_plan")
+    return {f: getattr(p, f) for f, _ in _Plan._fields_}
+
+
+def dg_sync_status(stream=None) -> int:
+    """Synchronise the stream; return (without raising) the status code."""
+    return lib().dg_sync_status(_stream(stream))
+
+
+def dg_set_wait_timeout_us(us: int) -> None:
+    lib().dg_set_wait_timeout_us(int(us))
+
+
+def dg_debug_skip_first_load(enable: bool = True) -> None:
+    lib().dg_debug_skip_first_load(1 if enable else 0)

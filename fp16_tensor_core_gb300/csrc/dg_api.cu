@@ -1,0 +1,262 @@
+// dg_api.cu -- the C ABI declared in include/dg.h: argument validation,
+// per-device state, path/tile selection and launch.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "dg.h"
+#include "dg_internal.h"
+#include "dg_ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceState g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_skip_first_load{0};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline dg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
+
+}  // namespace
+
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+bool take_skip_first_load() { return g_skip_first_load.exchange(0) != 0; }
+
+dg_status current_device_state(DeviceState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
+        return DG_ERR_UNSUPPORTED;
+    }
+    if (dev >= kMaxDevices) return DG_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ready[dev]) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return DG_ERR_CUDA;
+        if (prop.major != 10 || prop.minor != 3) return DG_ERR_UNSUPPORTED;
+        DeviceState st;
+        st.device = dev;
+        st.sm_count = prop.multiProcessorCount;
+        void* p = nullptr;
+        if (cudaMalloc(&p, 16) != cudaSuccess) return DG_ERR_CUDA;
+        if (cudaMemset(p, 0, 16) != cudaSuccess) {
+            cudaFree(p);
+            return DG_ERR_CUDA;
+        }
+        st.status = static_cast<uint32_t*>(p);
+        g_dev[dev] = st;
+        g_dev_ready[dev] = true;
+    }
+    *out = &g_dev[dev];
+    return DG_OK;
+}
+
+namespace {
+
+// Shared path selection for dg_gemm_plan and the GEMM entry points.
+dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p) {
+    *p = dg_plan{};
+    if (M == 0 || N == 0) {
+        p->path = 0;
+        return DG_OK;
+    }
+    if (K == 0) {
+        p->path = 1;
+        return DG_OK;
+    }
+    if (M <= 16) {
+        p->path = 2;
+        p->grid = static_cast<int>((N + 7) / 8);
+        p->block_m = static_cast<int>(M);
+        p->block_n = 8;
+        p->block_k = fp16_in ? 8 * 32 : 16 * 32;
+        p->stages = 1;
+        return DG_OK;
+    }
+    const int64_t tiles = ((M + 127) / 128) * ((N + 63) / 64);
+    if (tiles > INT_MAX) return DG_ERR_UNSUPPORTED;
+    p->path = 3;
+    plan_tc(M, N, K, fp16_in, sm_count, p);
+    return DG_OK;
+}
+
+dg_status check_sizes(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return DG_ERR_INVALID_VALUE;
+    if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return DG_ERR_INVALID_VALUE;
+    return DG_OK;
+}
+
+dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                   bool fp16_in, const float* sa, const float* sb, const float* sd,
+                   dg_dtype out, cudaStream_t s) {
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    dg_plan plan;
+    rc = make_plan(M, N, K, fp16_in, st->sm_count, &plan);
+    if (rc != DG_OK) return rc;
+    const int ok = out_kind_of(out);
+    switch (plan.path) {
+        case 0:
+            return DG_OK;
+        case 1:
+            return from_cuda(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * elem_bytes(out)), s));
+        case 2:
+            return from_cuda(launch_gemv(A, B, D, static_cast<int>(M), static_cast<int>(N),
+                                         static_cast<int>(K), fp16_in, sa, sb, sd, ok, s));
+        default: {
+            TcLaunch L;
+            L.A = A;
+            L.B = B;
+            L.D = D;
+            L.M = static_cast<int>(M);
+            L.N = static_cast<int>(N);
+            L.K = static_cast<int>(K);
+            L.fp16_in = fp16_in;
+            L.sa = sa;
+            L.sb = sb;
+            L.sd = sd;
+            L.out_kind = ok;
+            L.out_elem = elem_bytes(out);
+            L.plan = &plan;
+            L.status = st->status;
+            return from_cuda(launch_gemm_tc(L, s));
+        }
+    }
+}
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+dg_status dg_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
+                  dg_stream_t stream) {
+    if (n < 0 || amax_out == nullptr || (n > 0 && x == nullptr)) return DG_ERR_INVALID_VALUE;
+    if (!aligned16(x)) return DG_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(amax_out) & 3u) != 0 ||
+        (scale_out && (reinterpret_cast<uintptr_t>(scale_out) & 3u) != 0))
+        return DG_ERR_MISALIGNED;
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_amax(x, n, amax_out, scale_out, st->sm_count,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_t* q,
+                           dg_stream_t stream) {
+    if (n < 0 || scale == nullptr || (n > 0 && (x == nullptr || q == nullptr)))
+        return DG_ERR_INVALID_VALUE;
+    if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0)
+        return DG_ERR_MISALIGNED;
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_quantize_e4m3(x, n, scale, q, st->sm_count,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M, int64_t N,
+                      int64_t K, const float* scale_a, const float* scale_b,
+                      const float* scale_d, dg_dtype out, dg_stream_t stream) {
+    dg_status rc = check_sizes(M, N, K);
+    if (rc != DG_OK) return rc;
+    if (out != DG_BF16 && out != DG_E4M3 && out != DG_FP16) return DG_ERR_INVALID_VALUE;
+    if (M > 0 && N > 0) {
+        if (D == nullptr) return DG_ERR_INVALID_VALUE;
+        if (K > 0 && (A == nullptr || B == nullptr || scale_a == nullptr || scale_b == nullptr))
+            return DG_ERR_INVALID_VALUE;
+        if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0)
+            return DG_ERR_MISALIGNED;
+    }
+    return run_gemm(A, B, D, M, N, K, false, scale_a, scale_b, scale_d, out,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M, int64_t N,
+                   int64_t K, dg_dtype out, dg_stream_t stream) {
+    dg_status rc = check_sizes(M, N, K);
+    if (rc != DG_OK) return rc;
+    if (out != DG_FP16 && out != DG_BF16) return DG_ERR_INVALID_VALUE;
+    if (M > 0 && N > 0) {
+        if (D == nullptr) return DG_ERR_INVALID_VALUE;
+        if (K > 0 && (A == nullptr || B == nullptr)) return DG_ERR_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0)
+            return DG_ERR_MISALIGNED;
+    }
+    return run_gemm(A, B, D, M, N, K, true, nullptr, nullptr, nullptr, out,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_gemm_plan(int64_t M, int64_t N, int64_t K, dg_dtype in, dg_dtype out,
+                       int sm_count, dg_plan* plan) {
+    if (plan == nullptr) return DG_ERR_INVALID_VALUE;
+    dg_status rc = check_sizes(M, N, K);
+    if (rc != DG_OK) return rc;
+    if (in != DG_E4M3 && in != DG_FP16) return DG_ERR_INVALID_VALUE;
+    if (out != DG_BF16 && out != DG_E4M3 && out != DG_FP16) return DG_ERR_INVALID_VALUE;
+    if (sm_count <= 0) {
+        DeviceState* st = nullptr;
+        rc = current_device_state(&st);
+        if (rc != DG_OK) return rc;
+        sm_count = st->sm_count;
+    }
+    return make_plan(M, N, K, in == DG_FP16, sm_count, plan);
+}
+
+dg_status dg_init(void) {
+    DeviceState* st = nullptr;
+    return current_device_state(&st);
+}
+
+dg_status dg_sync_status(dg_stream_t stream) {
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DG_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DG_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess) return DG_ERR_CUDA;
+        if (word & kStatusTimeout) return DG_ERR_TIMEOUT;
+    }
+    return DG_OK;
+}
+
+void dg_set_wait_timeout_us(uint64_t us) {
+    g_timeout_ns.store(us * 1000ull, std::memory_order_relaxed);
+}
+
+void dg_debug_skip_first_load(int enable) { g_skip_first_load.store(enable ? 1 : 0); }
+
+const char* dg_status_string(dg_status s) {
+    switch (s) {
+        case DG_OK: return "DG_OK";
+        case DG_ERR_INVALID_VALUE: return "DG_ERR_INVALID_VALUE";
+        case DG_ERR_MISALIGNED: return "DG_ERR_MISALIGNED";
+        case DG_ERR_UNSUPPORTED: return "DG_ERR_UNSUPPORTED";
+        case DG_ERR_CUDA: return "DG_ERR_CUDA";
+        case DG_ERR_TIMEOUT: return "DG_ERR_TIMEOUT";
+    }
+    return "DG_ERR_UNKNOWN";
+}
+
+int dg_version(void) { return 100; }
+
+}  // extern "C"

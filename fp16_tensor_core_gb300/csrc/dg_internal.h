@@ -1,0 +1,61 @@
+// dg_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dg.h"
+
+namespace dg {
+
+enum OutKind : int { kOutBF16 = 0, kOutE4M3 = 1, kOutFP16 = 2 };
+
+inline int out_kind_of(dg_dtype t) {
+    return t == DG_E4M3 ? kOutE4M3 : (t == DG_FP16 ? kOutFP16 : kOutBF16);
+}
+inline int elem_bytes(dg_dtype t) { return t == DG_E4M3 ? 1 : 2; }
+
+// Per-device state, created once per device on first use.
+struct DeviceState {
+    int device = -1;
+    int sm_count = 0;
+    uint32_t* status = nullptr;  // device status word (kStatus* bits)
+};
+
+// Returns the current device's state, creating it on first use.
+dg_status current_device_state(DeviceState** out);
+
+// Runtime knobs (host globals, read at launch time).
+uint64_t wait_timeout_ns();
+bool take_skip_first_load();
+
+// Launchers; each returns the launch's cudaError_t.
+cudaError_t launch_amax(const float* x, int64_t n, float* amax_out,
+                        float* scale_out, int sm_count, cudaStream_t s);
+cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale,
+                                 uint8_t* q, int sm_count, cudaStream_t s);
+cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N,
+                        int K, bool fp16_in, const float* sa, const float* sb,
+                        const float* sd, int out_kind, cudaStream_t s);
+
+struct TcLaunch {
+    const void* A;
+    const void* B;
+    void* D;
+    int M, N, K;
+    bool fp16_in;
+    const float* sa;
+    const float* sb;
+    const float* sd;
+    int out_kind;
+    int out_elem;
+    const dg_plan* plan;
+    uint32_t* status;
+};
+cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s);
+
+// Tile table for the tensor-core path (fills block_n, stages, smem, grid).
+void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
+             dg_plan* p);
+
+}  // namespace dg

@@ -1,0 +1,426 @@
+// k_gemm_tc.cu -- the tensor-core GEMM for M > 16 (E4M3 or FP16 inputs,
+// FP32 accumulation in tensor memory, fused scale/convert epilogue).
+//
+// Page shorthands: [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南";
+// [DG-FP16] = the DeepGEMM FP16/WMMA deep-dive page; [HGEMM-L2] =
+// "HGEMM优化：深度学习中的矩阵乘法性能提升策略".
+//
+// What the pages prescribe, and how it maps onto sm_103a:
+//  * block tiling of C with a K-blocked main loop ([FP8-guide] §3.1) ->
+//    128 x BN output tiles, 128-byte K blocks, one tcgen05.mma (M=128,
+//    N=BN, K=32 bytes) per 32 bytes of K, accumulating in tensor memory;
+//  * loader warps separate from compute warps ([DG-FP16] §2.2) and a
+//    multi-stage prefetch pipeline ([FP8-guide] §2.3, §4.4; [HGEMM-L2]
+//    §3.2-§3.3) -> one TMA producer thread, one MMA-issuing thread and four
+//    epilogue warps, joined by full/empty mbarriers over a STAGES-deep
+//    shared-memory ring;
+//  * bank-conflict-free shared-memory layout ([DG-FP16] §3.2) -> TMA's
+//    128-byte swizzle, which the MMA's shared-memory descriptors read
+//    natively;
+//  * scale_A * scale_B applied once to the accumulator on write-back, and
+//    the output scale divided out for FP8 output ([FP8-guide] §3.2);
+//  * M/N edges by predication and K tails by zero fill, in one kernel
+//    ([FP8-guide] §3.3) -> TMA fills out-of-range box elements with zeros,
+//    and epilogue stores are predicated on m < M, n < N.
+// The kernel is persistent (one CTA per SM, tiles strided by the grid) and
+// double-buffers the accumulator in tensor memory so that the epilogue of
+// one tile overlaps the main loop of the next.  Every mbarrier wait is
+// bounded: on a timeout the CTA raises its abort flag, records
+// kStatusTimeout, lets in-flight copies and MMAs land, frees its tensor
+// memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "dg_internal.h"
+#include "dg_ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kThreads = 256;   // warps: 0 TMA, 1 MMA, 2 TMEM owner, 3 idle, 4-7 epilogue
+constexpr int kBM = 128;
+constexpr int kBKBytes = 128;   // one 128-byte swizzle row of K per stage
+constexpr int kGroupM = 16;     // tile raster: groups of 16 M-tiles sweep N
+
+template <int BN, int STAGES, bool kFp16In>
+struct Cfg {
+    static constexpr int kBK = kFp16In ? 64 : 128;        // K elements per stage
+    static constexpr int kABytes = kBM * kBKBytes;        // 16 KB
+    static constexpr int kBBytes = BN * kBKBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kTmemCols = 2 * BN;         // two accumulators
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes;
+    static constexpr uint32_t kIdesc = idesc_f32acc(kBM, BN, 0, 0);
+    static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+    static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
+};
+
+struct Params {
+    void* D;
+    int M, N, K;
+    const float* sa;
+    const float* sb;
+    const float* sd;
+    int out_kind;
+    int out_elem;
+    int vec_ok;
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int skip_first_load;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mt, int& nt) {
+    const int group = kGroupM * num_n;
+    const int g = t / group;
+    const int first_m = g * kGroupM;
+    const int gm = min(num_m - first_m, kGroupM);
+    const int r = t - g * group;
+    mt = first_m + r % gm;
+    nt = r / gm;
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Scale, convert and store 32 consecutive accumulator columns of one row.
+__device__ __forceinline__ void store_chunk(const Params& p, int row, int col0,
+                                            const uint32_t (&r)[32], float alpha) {
+    if (row >= p.M) return;
+    const int ncols = min(32, p.N - col0);
+    if (ncols <= 0) return;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
+    const int64_t off = static_cast<int64_t>(row) * p.N + col0;
+    if (p.out_kind == kOutE4M3) {
+        uint8_t* dst = static_cast<uint8_t*>(p.D) + off;
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            w[j] = static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j], v[4 * j + 1])) |
+                   (static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j + 2], v[4 * j + 3])) << 16);
+        if (ncols == 32 && p.vec_ok) {
+            st_global_v4(dst, w[0], w[1], w[2], w[3]);
+            st_global_v4(dst + 16, w[4], w[5], w[6], w[7]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncols) dst[i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+        }
+    } else {
+        uint16_t* dst = static_cast<uint16_t*>(p.D) + off;
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            w[j] = p.out_kind == kOutFP16 ? f32x2_to_f16x2(v[2 * j], v[2 * j + 1])
+                                          : f32x2_to_bf16x2(v[2 * j], v[2 * j + 1]);
+        if (ncols == 32 && p.vec_ok) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                st_global_v4(dst + 8 * j, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncols) dst[i] = static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1)));
+        }
+    }
+}
+
+template <int BN, int STAGES, bool kFp16In>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+               const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    using C = Cfg<BN, STAGES, kFp16In>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * C::kABytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;   // [2]
+    uint64_t* acc_empty = acc_full + 2;    // [2]
+    uint64_t* drain = acc_empty + 2;       // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+    }
+    if (warp == 2) {
+        tmem_alloc<C::kTmemCols>(tmem_slot);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    const int num_m = (p.M + kBM - 1) / kBM;
+    const int num_n = (p.N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (p.K + C::kBK - 1) / C::kBK;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0;          // stages with a load ever issued
+        uint32_t issued_phase = 0;         // parity of each stage's last load
+        bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int mt, nt;
+            tile_coords(t, num_m, num_n, mt, nt);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
+                if (skip) {
+                    skip = false;           // leave this stage unloaded
+                } else {
+                    mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                    tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kb * C::kBK, mt * kBM);
+                    tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kb * C::kBK, nt * BN);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        // Every load this thread issued must have landed before the CTA can
+        // exit.  After a normal run they all have (the MMA thread consumed
+        // each one) and these waits return at once; after an abort they let
+        // copies still in flight finish.
+        for (int s = 0; s < STAGES; ++s)
+            if (issued_mask & (1u << s))
+                wait_bounded(&full[s], (issued_phase >> s) & 1u, ctl, false);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        bool issued_any = false;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, ctl)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!wait_bounded(&full[stage], phase, ctl)) { ok = false; break; }
+                tc_fence_after_sync();
+                const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
+                const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBKBytes / 32; ++kk) {
+                    const uint64_t ad = sdesc_k_major_sw128(a0 + kk * 32);
+                    const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
+                    const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                    if constexpr (kFp16In)
+                        mma_f16(d_tmem, ad, bd, C::kIdesc, accum);
+                    else
+                        mma_f8f6f4(d_tmem, ad, bd, C::kIdesc, accum);
+                }
+                issued_any = true;
+                mma_commit(&empty[stage]);   // frees the stage when these MMAs finish
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit(&acc_full[acc]);      // accumulator ready for the epilogue
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (issued_any) {
+            // Tensor memory is freed below: wait for every MMA this thread
+            // issued (normal end or abort alike).
+            mma_commit(drain);
+            wait_bounded(drain, 0, ctl, false);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;              // TMEM lane quarter of this warp
+        float alpha = 1.0f;
+        if (p.sa != nullptr) alpha = (*p.sa) * (*p.sb);
+        if (p.out_kind == kOutE4M3) alpha = __fdiv_rn(alpha, *p.sd);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            int mt, nt;
+            tile_coords(t, num_m, num_n, mt, nt);
+            // Every lane waits; the vote reconverges the warp (tcgen05.ld is
+            // .sync.aligned) and makes the whole warp leave together.
+            const bool got = wait_bounded(&acc_full[acc], acc_phase, ctl);
+            if (!__all_sync(0xFFFFFFFFu, got)) break;
+            tc_fence_after_sync();
+            const int row = mt * kBM + q * 32 + lane;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_load_32cols(tbase + c * 32, r);
+                tmem_load_wait(r);
+                store_chunk(p, row, nt * BN + c * 32, r, alpha);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 2) tmem_dealloc<C::kTmemCols>(tmem_base);
+}
+
+// ------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D map over a rows x k row-major matrix, box = box_rows x 128 bytes,
+// 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap* map, const void* base, int rows, int k, bool fp16, int box_rows) {
+    auto encode = get_encode_fn();
+    if (!encode) return false;
+    const int elem = fp16 ? 2 : 1;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * elem};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes / elem), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                              2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool kFp16In>
+cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
+    using C = Cfg<BN, STAGES, kFp16In>;
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!attr_done[dev]) {
+            e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, kFp16In>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            if (e != cudaSuccess) return e;
+            attr_done[dev] = true;
+        }
+    }
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kBM) || !make_map(&tb, L.B, L.N, L.K, kFp16In, BN))
+        return cudaErrorInvalidValue;
+    gemm_tc_kernel<BN, STAGES, kFp16In><<<L.plan->grid, kThreads, C::kSmemBytes, s>>>(ta, tb, prm);
+    return cudaGetLastError();
+}
+
+template <bool kFp16In>
+cudaError_t launch_in(const TcLaunch& L, const Params& prm, cudaStream_t s) {
+    switch (L.plan->block_n) {
+        case 64: return launch_cfg<64, 8, kFp16In>(L, prm, s);
+        case 128: return launch_cfg<128, 6, kFp16In>(L, prm, s);
+        default: return launch_cfg<256, 4, kFp16In>(L, prm, s);
+    }
+}
+
+constexpr int stages_for(int bn) { return bn == 64 ? 8 : (bn == 128 ? 6 : 4); }
+
+int smem_for(int bn) {
+    switch (bn) {
+        case 64: return Cfg<64, 8, false>::kSmemBytes;
+        case 128: return Cfg<128, 6, false>::kSmemBytes;
+        default: return Cfg<256, 4, false>::kSmemBytes;
+    }
+}
+
+}  // namespace
+
+void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p) {
+    // Per-shape tile choice ([FP8-guide] §3.1, §3.3; [HGEMM-L2] §3.1):
+    // estimate each candidate's time as (waves of tiles over the SMs) x
+    // (tile width / relative MMA efficiency of that width) and keep the
+    // cheapest; narrow tiles win when the grid would otherwise leave SMs
+    // idle or strand a partial last wave.
+    const int64_t num_m = (M + kBM - 1) / kBM;
+    const int cand[3] = {256, 128, 64};
+    const double eff[3] = {1.0, 0.92, 0.75};
+    int best = 256;
+    double best_cost = 0.0;
+    for (int i = 0; i < 3; ++i) {
+        const int bn = cand[i];
+        const int64_t tiles = num_m * ((N + bn - 1) / bn);
+        const int64_t waves = (tiles + sm_count - 1) / sm_count;
+        const double cost = static_cast<double>(waves) * bn / eff[i];
+        if (i == 0 || cost < best_cost) { best = bn; best_cost = cost; }
+    }
+    const int64_t tiles = num_m * ((N + best - 1) / best);
+    p->block_m = kBM;
+    p->block_n = best;
+    p->block_k = fp16_in ? 64 : 128;
+    p->stages = stages_for(best);
+    p->tiles = static_cast<int>(tiles);
+    p->grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
+    p->smem_bytes = smem_for(best);
+    (void)K;
+}
+
+cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s) {
+    Params prm;
+    prm.D = L.D;
+    prm.M = L.M;
+    prm.N = L.N;
+    prm.K = L.K;
+    prm.sa = L.sa;
+    prm.sb = L.sb;
+    prm.sd = L.sd;
+    prm.out_kind = L.out_kind;
+    prm.out_elem = L.out_elem;
+    prm.vec_ok = ((static_cast<int64_t>(L.N) * L.out_elem) % 16 == 0) ? 1 : 0;
+    prm.status = L.status;
+    prm.timeout_ns = wait_timeout_ns();
+    prm.skip_first_load = take_skip_first_load() ? 1 : 0;
+    return L.fp16_in ? launch_in<true>(L, prm, s) : launch_in<false>(L, prm, s);
+}
+
+}  // namespace dg

@@ -1,0 +1,145 @@
+// k_scale.cu -- per-tensor amax, scale and the E4M3 quantiser.
+//
+// [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南".
+// §3.2: one scale per tensor, scale = max |x| / 448; §4.3: the quantiser
+// fp8 = clamp(round(x / scale), -448, 448).  Both kernels are HBM streams:
+// amax reads 4 B per element, the quantiser reads 4 B and writes 1 B.
+#include <cuda_runtime.h>
+
+#include "dg_internal.h"
+#include "dg_ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kAmaxThreads = 512;
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+// |x| as an ordered integer: for non-negative floats the bit pattern is
+// monotone in the value, and every NaN pattern is above +Inf, so an unsigned
+// max over (bits & 0x7fffffff) is max |x| with NaN propagating.
+__device__ __forceinline__ uint32_t abs_bits(float v) {
+    return __float_as_uint(v) & 0x7FFFFFFFu;
+}
+__device__ __forceinline__ uint32_t abs_bits4(float4 v) {
+    return max(max(abs_bits(v.x), abs_bits(v.y)), max(abs_bits(v.z), abs_bits(v.w)));
+}
+
+__global__ void __launch_bounds__(kAmaxThreads)
+amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_bits) {
+    const int64_t n4 = n >> 2;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    uint32_t m = 0;
+    for (; i + 3 * stride < n4; i += 4 * stride) {
+        const float4 v0 = ld_stream_f4(x4 + i);
+        const float4 v1 = ld_stream_f4(x4 + i + stride);
+        const float4 v2 = ld_stream_f4(x4 + i + 2 * stride);
+        const float4 v3 = ld_stream_f4(x4 + i + 3 * stride);
+        m = max(m, max(max(abs_bits4(v0), abs_bits4(v1)), max(abs_bits4(v2), abs_bits4(v3))));
+    }
+    for (; i < n4; i += stride) m = max(m, abs_bits4(ld_stream_f4(x4 + i)));
+    if (blockIdx.x == 0 && threadIdx.x < static_cast<unsigned>(n & 3))
+        m = max(m, abs_bits(x[(n4 << 2) + threadIdx.x]));
+
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __shared__ uint32_t partial[kAmaxThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) partial[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < kAmaxThreads / 32 ? partial[lane] : 0u;
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0 && m != 0u) atomicMax(out_bits, m);
+    }
+}
+
+// scale = amax / 448 (one IEEE binary32 division), 1 for an all-zero tensor.
+__global__ void scale_kernel(const float* __restrict__ amax, float* __restrict__ scale) {
+    const float a = *amax;
+    *scale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+}
+
+__device__ __forceinline__ uint32_t quant4(float4 v, float s) {
+    const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s));
+    const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s));
+    return lo | (hi << 16);
+}
+
+// Each warp iteration handles 512 consecutive elements: four fully coalesced
+// 512-byte loads (lane j reads float4 j, j+32, j+64, j+96 of the slab) and
+// four 128-byte stores of packed codes.
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict__ scale_p,
+                uint8_t* __restrict__ q) {
+    const float s = *scale_p;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t nslab = n >> 9;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    uint32_t* q4 = reinterpret_cast<uint32_t*>(q);
+    for (int64_t slab = warp; slab < nslab; slab += nwarps) {
+        const int64_t b = slab * 128 + lane;
+        const float4 v0 = ld_stream_f4(x4 + b);
+        const float4 v1 = ld_stream_f4(x4 + b + 32);
+        const float4 v2 = ld_stream_f4(x4 + b + 64);
+        const float4 v3 = ld_stream_f4(x4 + b + 96);
+        q4[b] = quant4(v0, s);
+        q4[b + 32] = quant4(v1, s);
+        q4[b + 64] = quant4(v2, s);
+        q4[b + 96] = quant4(v3, s);
+    }
+    // Ragged tail (< 512 elements): one element per thread of block 0.
+    if (blockIdx.x == 0) {
+        for (int64_t i = (nslab << 9) + threadIdx.x; i < n; i += blockDim.x)
+            q[i] = static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(x[i], s), 0.0f) & 0xFFu);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
+                        int sm_count, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    if (n > 0) {
+        const int64_t n4 = (n + 3) >> 2;
+        int64_t blocks = (n4 + kAmaxThreads - 1) / kAmaxThreads;
+        const int64_t cap = static_cast<int64_t>(sm_count) * 4;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        amax_kernel<<<static_cast<unsigned>(blocks), kAmaxThreads, 0, s>>>(
+            x, n, reinterpret_cast<uint32_t*>(amax_out));
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (scale_out) {
+        scale_kernel<<<1, 1, 0, s>>>(amax_out, scale_out);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_t* q,
+                                 int sm_count, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t slabs = n >> 9;
+    const int warps_per_block = kQuantThreads / 32;
+    int64_t blocks = (slabs + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    quantize_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, s>>>(x, n, scale, q);
+    return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,162 @@
+/*
+ * dg.h -- C ABI of libdg: per-tensor-scaled E4M3 GEMM, FP16 GEMM and the
+ * E4M3 quantiser on one NVIDIA GB300 (sm_103a).
+ *
+ * Page shorthands used in the citations:
+ *   [FP8-guide] "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南"
+ *               (sheratonhq.com/news/156926), sections as numbered there.
+ *   [DG-FP16]   the DeepGEMM FP16/WMMA deep-dive page (hnwysp.cn/news/84236).
+ *   [HGEMM-L2]  "HGEMM优化：深度学习中的矩阵乘法性能提升策略"
+ *               (jsqmd.com/news/710660).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.    Every data pointer is DEVICE memory on the current CUDA device,
+ *            owned by the caller.  The library allocates nothing per call and
+ *            takes no workspace.  The first call on a device (or dg_init)
+ *            allocates a 16-byte device status word that lives until exit.
+ * Layout.    Dense, row-major, no leading-dimension arguments: A is M x K,
+ *            B is N x K (both K contiguous, the "TN" form), D is M x N.
+ * Alignment. Every data pointer must be 16-byte aligned and K * element
+ *            size must be a multiple of 16 bytes; otherwise the call returns
+ *            DG_ERR_MISALIGNED and launches nothing (there is no slow path).
+ * Streams.   Work is enqueued on `stream` (NULL = the legacy default stream)
+ *            and nothing synchronises the host.  Scales are device pointers
+ *            so that amax -> quantise -> GEMM needs no host round trip.
+ * Errors.    Argument errors return a status and launch nothing.  A failed
+ *            launch returns DG_ERR_CUDA.  Every wait inside a kernel is
+ *            bounded; a wait that runs out records DG_ERR_TIMEOUT in the
+ *            device status word, the kernel returns cleanly, and
+ *            dg_sync_status() reports it.
+ * Aliasing.  Outputs must not overlap inputs.
+ * Threads.   Entry points are thread-safe; per-device set-up runs once.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that the header needs no CUDA
+ * include. */
+typedef struct CUstream_st* dg_stream_t;
+
+typedef enum {
+    DG_OK = 0,
+    DG_ERR_INVALID_VALUE = 1, /* null pointer, negative size, bad dtype     */
+    DG_ERR_MISALIGNED = 2,    /* pointer or row pitch not 16-byte aligned   */
+    DG_ERR_UNSUPPORTED = 3,   /* no CUDA device of compute capability 10.3  */
+    DG_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed          */
+    DG_ERR_TIMEOUT = 5        /* a bounded in-kernel wait ran out           */
+} dg_status;
+
+typedef enum {
+    DG_BF16 = 0, /* bfloat16, round to nearest even                        */
+    DG_E4M3 = 1, /* E4M3 "fn": bias 7, max 448, no Inf, RNE, saturating    */
+    DG_FP16 = 2  /* IEEE binary16, round to nearest even                   */
+} dg_dtype;
+
+/* amax and scale.  [FP8-guide] §3.2: the per-tensor scale is the largest
+ * absolute value of the tensor divided by 448, the largest E4M3 value.
+ *   x          FP32[n], device, 16-byte aligned.
+ *   amax_out   FP32[1], device: max_i |x_i|; NaN if any x_i is NaN; 0 for
+ *              n == 0.
+ *   scale_out  FP32[1], device, may be NULL: amax / 448 as one binary32
+ *              division, or 1 when amax == 0.
+ * Three stream operations: a 4-byte memset of amax_out, a reduction kernel,
+ * and (when scale_out is set) a one-thread kernel. */
+dg_status dg_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
+                  dg_stream_t stream);
+
+/* E4M3 quantiser.  [FP8-guide] §4.3: fp8 = clamp(round(x / scale), -448,
+ * 448), implemented as q_i = E4M3(fl32(x_i / *scale)) with an IEEE binary32
+ * division and round-to-nearest-even, saturating to +-448; NaN -> 0x7F.
+ *   x      FP32[n], device, 16-byte aligned.
+ *   scale  FP32[1], device.
+ *   q      uint8[n] E4M3 codes, device, 16-byte aligned; same order as x. */
+dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale,
+                           uint8_t* q, dg_stream_t stream);
+
+/* Per-tensor-scaled E4M3 GEMM.  [FP8-guide] §2.1, §3.2, §3.3:
+ *   D[m,n] = out( scale_a * scale_b * sum_k A[m,k] * B[n,k] )
+ * with FP8 inputs, FP32 accumulation and the scales applied once to the
+ * accumulator on write-back.  For out == DG_E4M3 the value is divided by
+ * *scale_d before the saturating E4M3 rounding.
+ *   A        uint8 E4M3 codes, M x K row-major, device.
+ *   B        uint8 E4M3 codes, N x K row-major (K contiguous), device.
+ *   D        M x N row-major of `out` (DG_BF16, DG_E4M3 or DG_FP16), device.
+ *            Elements outside [0,M) x [0,N) are never touched.
+ *   scale_a, scale_b  FP32[1], device.
+ *   scale_d  FP32[1], device; required iff out == DG_E4M3, else ignored.
+ *   M, N, K  >= 0 and < 2^31.  M == 0 or N == 0 is a no-op; K == 0 writes
+ *            zeros.  K must be a multiple of 16 (row pitch alignment).
+ * M <= 16 runs a bandwidth-bound split-K GEMV ([DG-FP16] §2.1 and §4.1,
+ * the decode QKV projection); larger M runs the tensor-core kernel with a
+ * tile chosen per shape (dg_gemm_plan).  K tails are zero-filled by the
+ * tensor-memory loads and M/N edges are predicated stores ([FP8-guide] §3.3).
+ */
+dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M,
+                      int64_t N, int64_t K, const float* scale_a,
+                      const float* scale_b, const float* scale_d, dg_dtype out,
+                      dg_stream_t stream);
+
+/* FP16 GEMM (HGEMM), FP32 accumulation, no scaling.  [HGEMM-L2] §1.3 (FP16
+ * inputs, FP32 accumulator) and §3; same layouts and edge rules as
+ * dg_fp8_gemm.  A, B hold IEEE binary16 bit patterns.  K must be a multiple
+ * of 8.  out is DG_FP16 or DG_BF16. */
+dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M,
+                   int64_t N, int64_t K, dg_dtype out, dg_stream_t stream);
+
+/* Tile / path selection for a GEMM shape, host only (launches nothing).
+ * [FP8-guide] §2.2, §3.1, §3.3 (per-shape tile choice, smaller tiles where
+ * edge waste is high) and [HGEMM-L2] §3.1-§3.3 (tile and stage count chosen
+ * from M, N, K); here the choice comes from a compiled table instead of a
+ * JIT.  in is DG_E4M3 or DG_FP16.  sm_count <= 0 queries the current device.
+ */
+typedef struct {
+    int path;       /* 0 no-op, 1 zero-fill (K == 0), 2 GEMV, 3 tensor core */
+    int block_m;    /* output rows per tile (tensor-core path)              */
+    int block_n;    /* output columns per tile                              */
+    int block_k;    /* K elements per pipeline stage                        */
+    int stages;     /* shared-memory pipeline depth                         */
+    int grid;       /* CTAs launched                                        */
+    int tiles;      /* output tiles (tensor-core path)                      */
+    int smem_bytes; /* dynamic shared memory per CTA                        */
+} dg_plan;
+
+dg_status dg_gemm_plan(int64_t M, int64_t N, int64_t K, dg_dtype in,
+                       dg_dtype out, int sm_count, dg_plan* plan);
+
+/* Per-device set-up for the current device: checks compute capability 10.3
+ * and allocates the device status word.  Optional (every entry point does it
+ * on first use); call it before capturing a stream into a CUDA graph. */
+dg_status dg_init(void);
+
+/* Synchronises `stream`, then returns and clears the current device's
+ * status word: DG_ERR_TIMEOUT if a kernel's bounded wait ran out since the
+ * last call, DG_ERR_CUDA if the synchronisation failed, else DG_OK. */
+dg_status dg_sync_status(dg_stream_t stream);
+
+/* Upper bound, in microseconds, on any single in-kernel wait (default
+ * 2 000 000).  Applies to launches made after the call. */
+void dg_set_wait_timeout_us(uint64_t us);
+
+/* Test hook: when non-zero, the next tensor-core GEMM launch leaves the
+ * first shared-memory stage of its first tile unloaded, so that the MMA
+ * warp's wait on it runs out (bounded) and the kernel reports
+ * DG_ERR_TIMEOUT.  Resets itself after one launch. */
+void dg_debug_skip_first_load(int enable);
+
+/* Human-readable name of a status code (static storage). */
+const char* dg_status_string(dg_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DG_H */

@@ -199,11 +199,53 @@ float dgo_scale_from_amax(float amax) {
 
 /* [FP8-guide] §4.3: fp8 = clamp(round(x / scale), -448, 448), read as
  * round-to-nearest-even onto the E4M3 grid after a binary32 division. */
-void dgo_quantize_e4m3(const float* x, int64_t n, float scale, uint8_t* q) {
-    for (int64_t i = 0; i < n; ++i) {
+static void quantize_range(const float* x, int64_t lo, int64_t hi, float scale,
+                           uint8_t* q) {
+    for (int64_t i = lo; i < hi; ++i) {
         float y = x[i] / scale;
         q[i] = dgo_e4m3_encode((double)y);
     }
+}
+
+typedef struct {
+    const float* x;
+    int64_t lo, hi;
+    float scale;
+    uint8_t* q;
+} qjob_t;
+
+static void* quantize_worker(void* p) {
+    qjob_t* j = (qjob_t*)p;
+    quantize_range(j->x, j->lo, j->hi, j->scale, j->q);
+    return NULL;
+}
+
+static int online_cores(void);
+
+/* Elements are independent, so large inputs are split into contiguous
+ * slices over threads; each element sees exactly the same two steps. */
+void dgo_quantize_e4m3(const float* x, int64_t n, float scale, uint8_t* q) {
+    ensure_tables();
+    int nt = n >= (1 << 20) ? online_cores() : 1;
+    if (nt > 256) nt = 256;
+    if (nt <= 1) {
+        quantize_range(x, 0, n, scale, q);
+        return;
+    }
+    qjob_t jobs[256];
+    pthread_t th[256];
+    int started[256];
+    int64_t per = (n + nt - 1) / nt;
+    for (int t = 0; t < nt; ++t) {
+        int64_t lo = (int64_t)t * per, hi = lo + per;
+        if (lo > n) lo = n;
+        if (hi > n) hi = n;
+        jobs[t] = (qjob_t){x, lo, hi, scale, q};
+        started[t] = pthread_create(&th[t], NULL, quantize_worker, &jobs[t]) == 0;
+        if (!started[t]) quantize_worker(&jobs[t]);
+    }
+    for (int t = 0; t < nt; ++t)
+        if (started[t]) pthread_join(th[t], NULL);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -1,0 +1,138 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+function include/dg.h declares, argument errors come back as status codes
+before anything touches a device, and the tile table behaves.  CPU only: no
+call here reaches a kernel launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp16_tensor_core_gb300 as dg
+from fp16_tensor_core_gb300 import build as dg_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dg.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    dg_build.build()
+    return dg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(dg.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    # and nothing from the oracle leaks into the product library
+    with pytest.raises(AttributeError):
+        getattr(L, "dgo_gemm_e4m3")
+
+
+def test_status_strings_and_version(L):
+    assert dg.dg_status_string(dg.DG_OK) == "DG_OK"
+    assert dg.dg_status_string(dg.DG_ERR_TIMEOUT) == "DG_ERR_TIMEOUT"
+    assert dg.dg_status_string(99) == "DG_ERR_UNKNOWN"
+    assert dg.dg_version() >= 100
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced: every call below fails validation
+
+
+@pytest.mark.parametrize("args,expect", [
+    # negative sizes
+    ((FAKE, FAKE, FAKE, -1, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_INVALID_VALUE),
+    ((FAKE, FAKE, FAKE, 8, 8, -16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_INVALID_VALUE),
+    # too large
+    ((FAKE, FAKE, FAKE, 1 << 31, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_INVALID_VALUE),
+    # null operands / scales / output
+    ((None, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_INVALID_VALUE),
+    ((FAKE, FAKE, None, 8, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_INVALID_VALUE),
+    ((FAKE, FAKE, FAKE, 8, 8, 16, None, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_INVALID_VALUE),
+    # E4M3 output needs an output scale
+    ((FAKE, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_E4M3, None), dg.DG_ERR_INVALID_VALUE),
+    # unknown output type
+    ((FAKE, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, None, 7, None), dg.DG_ERR_INVALID_VALUE),
+    # misaligned pointers or row pitch
+    ((FAKE + 1, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
+    ((FAKE, FAKE + 8, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE + 2, 8, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE, 8, 8, 24, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
+])
+def test_fp8_gemm_argument_errors(L, args, expect):
+    assert L.dg_fp8_gemm(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, FAKE, FAKE, 8, 8, 16, dg.DG_E4M3, None), dg.DG_ERR_INVALID_VALUE),  # bad out type
+    ((FAKE, FAKE, FAKE, 8, -1, 16, dg.DG_FP16, None), dg.DG_ERR_INVALID_VALUE),
+    ((None, FAKE, FAKE, 8, 8, 16, dg.DG_FP16, None), dg.DG_ERR_INVALID_VALUE),
+    ((FAKE, FAKE, FAKE, 8, 8, 12, dg.DG_FP16, None), dg.DG_ERR_MISALIGNED),   # K*2 % 16 != 0
+    ((FAKE, FAKE, FAKE + 4, 8, 8, 16, dg.DG_FP16, None), dg.DG_ERR_MISALIGNED),
+])
+def test_hgemm_argument_errors(L, args, expect):
+    assert L.dg_hgemm(*args) == expect
+
+
+def test_scale_and_quantise_argument_errors(L):
+    assert L.dg_amax(FAKE, -1, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_amax(FAKE, 10, None, None, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_amax(None, 10, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_amax(FAKE + 4, 10, FAKE, None, None) == dg.DG_ERR_MISALIGNED
+    assert L.dg_amax(FAKE, 10, FAKE + 2, None, None) == dg.DG_ERR_MISALIGNED
+    assert L.dg_quantize_e4m3(FAKE, 10, None, FAKE, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_quantize_e4m3(FAKE, -3, FAKE, FAKE, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_quantize_e4m3(FAKE, 10, FAKE, FAKE + 1, None) == dg.DG_ERR_MISALIGNED
+
+
+def test_plan_paths_and_tiles(L):
+    sm = 152
+    assert dg.dg_gemm_plan(0, 10, 16, sm_count=sm)["path"] == 0
+    assert dg.dg_gemm_plan(10, 0, 16, sm_count=sm)["path"] == 0
+    assert dg.dg_gemm_plan(10, 10, 0, sm_count=sm)["path"] == 1
+    for m in (1, 2, 16):
+        p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
+        assert p["path"] == 2 and p["grid"] == 12288 // 8
+    for m in (17, 63, 65, 129, 256, 4096, 8192):
+        p = dg.dg_gemm_plan(m, 1000, 1040, sm_count=sm)
+        assert p["path"] == 3
+        assert p["block_m"] == 128 and p["block_n"] in (64, 128, 256)
+        assert p["grid"] <= sm and p["grid"] <= p["tiles"]
+        assert p["smem_bytes"] <= 232448
+        assert p["block_k"] == 128
+    # FP16 operands: 64 K elements (128 bytes) per stage
+    assert dg.dg_gemm_plan(4096, 4096, 4096, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16,
+                           sm_count=sm)["block_k"] == 64
+    # edge waste: a narrow N problem gets narrower tiles than a wide one
+    small = dg.dg_gemm_plan(65, 1000, 1040, sm_count=sm)
+    big = dg.dg_gemm_plan(8192, 8192, 8192, sm_count=sm)
+    assert small["block_n"] < big["block_n"]
+    assert big["grid"] == sm
+
+
+def test_plan_argument_errors(L):
+    p = dg._Plan()
+    assert L.dg_gemm_plan(4, 4, 16, dg.DG_BF16, dg.DG_BF16, 10, ctypes.byref(p)) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_gemm_plan(-4, 4, 16, dg.DG_E4M3, dg.DG_BF16, 10, ctypes.byref(p)) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_gemm_plan(4, 4, 16, dg.DG_E4M3, dg.DG_BF16, 10, None) == dg.DG_ERR_INVALID_VALUE
+
+
+def test_product_package_does_not_import_oracle():
+    """The product path must not route through the CPU oracle."""
+    pkg = os.path.join(ROOT, "fp16_tensor_core_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "dg_oracle" not in src, f
