@@ -76,9 +76,10 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     }
     if (M <= 16) {
         p->path = 2;
-        p->grid = static_cast<int>((N + 7) / 8);
+        const int rows = M <= 4 ? 16 : 8;   // 8 warps x (2 or 1) rows of B
+        p->grid = static_cast<int>((N + rows - 1) / rows);
         p->block_m = static_cast<int>(M);
-        p->block_n = 8;
+        p->block_n = rows;
         p->block_k = fp16_in ? 8 * 32 : 16 * 32;
         p->stages = 1;
         return DG_OK;

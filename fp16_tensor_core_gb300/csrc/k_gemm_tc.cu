@@ -32,6 +32,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "dg_internal.h"
@@ -45,18 +46,34 @@ constexpr int kBM = 128;
 constexpr int kBKBytes = 128;   // one 128-byte swizzle row of K per stage
 constexpr int kGroupM = 16;     // tile raster: groups of 16 M-tiles sweep N
 
+constexpr uint32_t pow2_at_least(uint32_t v) {
+    uint32_t p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Shared memory per CTA: up to 227 KB; stage count = what fits, at most 8.
+constexpr int kSmemLimit = 232448;
+constexpr int stages_for(int bn) {
+    const int st = (kSmemLimit - 1024 - 256) / (kBM * kBKBytes + bn * kBKBytes);
+    return st > 8 ? 8 : st;
+}
+
 template <int BN, int STAGES, bool kFp16In>
 struct Cfg {
     static constexpr int kBK = kFp16In ? 64 : 128;        // K elements per stage
     static constexpr int kABytes = kBM * kBKBytes;        // 16 KB
     static constexpr int kBBytes = BN * kBKBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kTmemCols = 2 * BN;         // two accumulators
+    static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // two accumulators
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes;
     static constexpr uint32_t kIdesc = idesc_f32acc(kBM, BN, 0, 0);
-    static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
-    static_assert(kTmemCols >= 32 && kTmemCols <= 512, "TMEM columns");
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256,
+                  "BN: MMA N (multiple of 16, <= 256) and 32-column epilogue chunks");
+    static_assert(kTmemCols <= 512, "TMEM columns");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+    static_assert(kBBytes % 1024 == 0, "1024-byte aligned B stages (128-byte swizzle atoms)");
 };
 
 struct Params {
@@ -358,19 +375,23 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
 template <bool kFp16In>
 cudaError_t launch_in(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     switch (L.plan->block_n) {
-        case 64: return launch_cfg<64, 8, kFp16In>(L, prm, s);
-        case 128: return launch_cfg<128, 6, kFp16In>(L, prm, s);
-        default: return launch_cfg<256, 4, kFp16In>(L, prm, s);
+        case 64: return launch_cfg<64, stages_for(64), kFp16In>(L, prm, s);
+        case 128: return launch_cfg<128, stages_for(128), kFp16In>(L, prm, s);
+        case 160: return launch_cfg<160, stages_for(160), kFp16In>(L, prm, s);
+        case 192: return launch_cfg<192, stages_for(192), kFp16In>(L, prm, s);
+        case 224: return launch_cfg<224, stages_for(224), kFp16In>(L, prm, s);
+        default: return launch_cfg<256, stages_for(256), kFp16In>(L, prm, s);
     }
 }
 
-constexpr int stages_for(int bn) { return bn == 64 ? 8 : (bn == 128 ? 6 : 4); }
-
 int smem_for(int bn) {
     switch (bn) {
-        case 64: return Cfg<64, 8, false>::kSmemBytes;
-        case 128: return Cfg<128, 6, false>::kSmemBytes;
-        default: return Cfg<256, 4, false>::kSmemBytes;
+        case 64: return Cfg<64, stages_for(64), false>::kSmemBytes;
+        case 128: return Cfg<128, stages_for(128), false>::kSmemBytes;
+        case 160: return Cfg<160, stages_for(160), false>::kSmemBytes;
+        case 192: return Cfg<192, stages_for(192), false>::kSmemBytes;
+        case 224: return Cfg<224, stages_for(224), false>::kSmemBytes;
+        default: return Cfg<256, stages_for(256), false>::kSmemBytes;
     }
 }
 
@@ -383,16 +404,27 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     // cheapest; narrow tiles win when the grid would otherwise leave SMs
     // idle or strand a partial last wave.
     const int64_t num_m = (M + kBM - 1) / kBM;
-    const int cand[3] = {256, 128, 64};
-    const double eff[3] = {1.0, 0.92, 0.75};
+    // Relative throughput per CTA of a 128 x BN tile.  Each 32-byte K step
+    // reads 4 KB of A and BN*32 B of B from shared memory while the MMA runs
+    // for BN/2 cycles, so narrow tiles need more shared-memory bandwidth per
+    // flop (8192/BN + 64 B/clk).  Measured on GB300 (8192^3 E4M3): BN 256 ->
+    // 1.0, 128 -> 0.72, 64 -> 0.36; the widths in between are interpolated
+    // along that demand curve.
+    const int cand[6] = {256, 224, 192, 160, 128, 64};
+    const double eff[6] = {1.0, 0.95, 0.88, 0.80, 0.72, 0.36};
     int best = 256;
     double best_cost = 0.0;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 6; ++i) {
         const int bn = cand[i];
         const int64_t tiles = num_m * ((N + bn - 1) / bn);
         const int64_t waves = (tiles + sm_count - 1) / sm_count;
         const double cost = static_cast<double>(waves) * bn / eff[i];
         if (i == 0 || cost < best_cost) { best = bn; best_cost = cost; }
+    }
+    // DG_FORCE_BLOCK_N=64|128|160|192|224|256 pins the tile width (sweeps).
+    if (const char* f = std::getenv("DG_FORCE_BLOCK_N")) {
+        const int v = std::atoi(f);
+        if (v == 64 || v == 128 || v == 160 || v == 192 || v == 224 || v == 256) best = v;
     }
     const int64_t tiles = num_m * ((N + best - 1) / best);
     p->block_m = kBM;

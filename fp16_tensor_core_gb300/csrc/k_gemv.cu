@@ -8,12 +8,15 @@
 // [1, 4096] x [4096, 12288] the weight B is long-lived and read once, so it
 // is streamed from HBM without shared-memory staging; §4.1: the single A row
 // is broadcast to every thread instead of 2-D tiling.  [FP8-guide] §2.3:
-// 128-bit vector loads.  Here one warp owns one row n of B (N x K, K
-// contiguous): lane l reads 16-byte chunks l, l+32, l+64, ... of that row
-// (fully coalesced 512-byte warp loads, all of a 4 KB row in flight at
-// once), multiplies them with the matching A chunks (L1-resident, shared by
-// every warp) in FP32, and the warp's partial sums meet in a shuffle
-// reduction.  The epilogue applies scale_A * scale_B ([FP8-guide] §3.2) and
+// 128-bit vector loads.  Here one warp owns R consecutive rows of B (N x K,
+// K contiguous; R = 2 for M <= 4): lane l reads 16-byte chunks l, l+32,
+// l+64, ... of each row (fully coalesced 512-byte warp loads, several per
+// row in flight at once) and widens them to FP16 pairs; the matching A
+// chunk (L1-resident, shared by every warp) is widened once and used for all
+// R rows.  Products and sums use fma.rn.f32.f16 -- the exact product of two
+// FP16 values rounded once into an FP32 accumulator, the same arithmetic as
+// widening both to FP32 first.  The warp's partial sums meet in a shuffle
+// reduction; the epilogue applies scale_A * scale_B ([FP8-guide] §3.2) and
 // rounds to the output type.
 #include <cuda_runtime.h>
 
@@ -24,7 +27,6 @@ namespace dg {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kUnroll = 8;  // 16-byte chunks per lane in flight
 
 __device__ __forceinline__ uint4 ld_stream_u4(const uint4* p) {
     uint4 v;
@@ -33,31 +35,33 @@ __device__ __forceinline__ uint4 ld_stream_u4(const uint4* p) {
     return v;
 }
 
-// 16 bytes -> FP32 values (16 for E4M3 codes, 8 for FP16).  The conversion
-// is exact in both cases (E4M3 and FP16 are subsets of FP32).
+// 16 bytes of operand as f16x2 words: E4M3 codes are widened to FP16 (exact:
+// E4M3 is a subset of FP16); FP16 data is already in that form.
 template <bool kFp16>
-struct Chunk {
-    static constexpr int kVals = kFp16 ? 8 : 16;
-    float v[kVals];
-    __device__ __forceinline__ void load(const uint4& w) {
+__device__ __forceinline__ void to_h2(const uint4& w, uint32_t (&h)[kFp16 ? 4 : 8]) {
+    if constexpr (kFp16) {
+        h[0] = w.x; h[1] = w.y; h[2] = w.z; h[3] = w.w;
+    } else {
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            if constexpr (kFp16) {
-                const float2 f = f16x2_to_f32x2(ws[i]);
-                v[2 * i] = f.x;
-                v[2 * i + 1] = f.y;
-            } else {
-                const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] & 0xFFFFu)));
-                const float2 b = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] >> 16)));
-                v[4 * i] = a.x;
-                v[4 * i + 1] = a.y;
-                v[4 * i + 2] = b.x;
-                v[4 * i + 3] = b.y;
-            }
+            h[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] & 0xFFFFu));
+            h[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] >> 16));
         }
     }
-};
+}
+
+// acc += a.lo * b.lo + a.hi * b.hi with FP16 inputs and FP32 accumulation:
+// each fma.rn.f32.f16 forms the exact product and rounds once to FP32.
+__device__ __forceinline__ float fma2_f16(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc) : "r"(a), "r"(b));
+    return acc;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -65,53 +69,61 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-template <int MT, bool kFp16>
+// One warp owns R consecutive rows of B; each A chunk is widened once and
+// used for all R rows.  U chunks per lane per row are in flight at once.
+template <int MT, bool kFp16, int R, int U>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* __restrict__ D,
             int M, int N, int K, const float* __restrict__ sa, const float* __restrict__ sb,
             const float* __restrict__ sd, int out_kind) {
+    constexpr int H = kFp16 ? 4 : 8;   // f16x2 words per 16-byte chunk
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = blockIdx.x * kWarps + warp;
-    if (n >= N) return;  // warp-uniform
+    const int n0 = (blockIdx.x * kWarps + warp) * R;
+    if (n0 >= N) return;  // warp-uniform
     const int64_t row_bytes = static_cast<int64_t>(K) * (kFp16 ? 2 : 1);
     const int nch = static_cast<int>(row_bytes >> 4);
-    const uint4* brow = reinterpret_cast<const uint4*>(B + static_cast<int64_t>(n) * row_bytes);
 
-    float acc[MT];
+    float acc[MT][R];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
 
-    for (int c0 = 0; c0 < nch; c0 += 32 * kUnroll) {
-        uint4 bw[kUnroll];
+    for (int c0 = 0; c0 < nch; c0 += 32 * U) {
+        uint4 bw[R][U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int c = c0 + u * 32 + lane;
-            bw[u] = c < nch ? ld_stream_u4(brow + c) : make_uint4(0, 0, 0, 0);
+        for (int r = 0; r < R; ++r) {
+            const uint4* brow = reinterpret_cast<const uint4*>(
+                B + static_cast<int64_t>(min(n0 + r, N - 1)) * row_bytes);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = c0 + u * 32 + lane;
+                bw[r][u] = (c < nch && n0 + r < N) ? ld_stream_u4(brow + c) : make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int c = c0 + u * 32 + lane;
             if (c < nch) {
-                Chunk<kFp16> bc;
-                bc.load(bw[u]);
+                uint32_t bh[R][H];
+#pragma unroll
+                for (int r = 0; r < R; ++r) to_h2<kFp16>(bw[r][u], bh[r]);
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     if (m < M) {
                         const uint4 aw = __ldg(reinterpret_cast<const uint4*>(
                                                    A + static_cast<int64_t>(m) * row_bytes) + c);
-                        Chunk<kFp16> ac;
-                        ac.load(aw);
+                        uint32_t ah[H];
+                        to_h2<kFp16>(aw, ah);
 #pragma unroll
-                        for (int i = 0; i < Chunk<kFp16>::kVals; ++i)
-                            acc[m] = fmaf(ac.v[i], bc.v[i], acc[m]);
+                        for (int r = 0; r < R; ++r)
+#pragma unroll
+                            for (int i = 0; i < H; ++i) acc[m][r] = fma2_f16(ah[i], bh[r][i], acc[m][r]);
                     }
                 }
             }
         }
     }
-
-#pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = warp_sum(acc[m]);
 
     float alpha = 1.0f;
     if (sa != nullptr) alpha = (*sa) * (*sb);
@@ -120,10 +132,15 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
     float mine = 0.0f;
 #pragma unroll
     for (int m = 0; m < MT; ++m)
-        if (lane == m) mine = acc[m];
-    if (lane < M) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float s = warp_sum(acc[m][r]);
+            if (lane == m * R + r) mine = s;
+        }
+    const int m = lane / R, r = lane % R;
+    if (m < M && m < MT && n0 + r < N) {
         const float v = mine * alpha;
-        const int64_t off = static_cast<int64_t>(lane) * N + n;
+        const int64_t off = static_cast<int64_t>(m) * N + n0 + r;
         if (out_kind == kOutE4M3) {
             reinterpret_cast<uint8_t*>(D)[off] =
                 static_cast<uint8_t>(f32x2_to_e4m3x2(v, 0.0f) & 0xFFu);
@@ -137,21 +154,29 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
     }
 }
 
+template <int MT, bool kFp16, int R, int U>
+cudaError_t launch_one(const void* A, const void* B, void* D, int M, int N, int K,
+                       const float* sa, const float* sb, const float* sd, int out_kind,
+                       cudaStream_t s) {
+    const int rows_per_block = kWarps * R;
+    const dim3 grid((N + rows_per_block - 1) / rows_per_block), block(kWarps * 32);
+    gemv_kernel<MT, kFp16, R, U><<<grid, block, 0, s>>>(
+        static_cast<const uint8_t*>(A), static_cast<const uint8_t*>(B), D, M, N, K, sa, sb, sd,
+        out_kind);
+    return cudaGetLastError();
+}
+
 template <bool kFp16>
 cudaError_t launch_mt(int MT, const void* A, const void* B, void* D, int M, int N, int K,
                       const float* sa, const float* sb, const float* sd, int out_kind,
                       cudaStream_t s) {
-    const dim3 grid((N + kWarps - 1) / kWarps), block(kWarps * 32);
-    const auto* a = static_cast<const uint8_t*>(A);
-    const auto* b = static_cast<const uint8_t*>(B);
     switch (MT) {
-        case 1: gemv_kernel<1, kFp16><<<grid, block, 0, s>>>(a, b, D, M, N, K, sa, sb, sd, out_kind); break;
-        case 2: gemv_kernel<2, kFp16><<<grid, block, 0, s>>>(a, b, D, M, N, K, sa, sb, sd, out_kind); break;
-        case 4: gemv_kernel<4, kFp16><<<grid, block, 0, s>>>(a, b, D, M, N, K, sa, sb, sd, out_kind); break;
-        case 8: gemv_kernel<8, kFp16><<<grid, block, 0, s>>>(a, b, D, M, N, K, sa, sb, sd, out_kind); break;
-        default: gemv_kernel<16, kFp16><<<grid, block, 0, s>>>(a, b, D, M, N, K, sa, sb, sd, out_kind); break;
+        case 1: return launch_one<1, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
+        case 2: return launch_one<2, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
+        case 4: return launch_one<4, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
+        case 8: return launch_one<8, kFp16, 1, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
+        default: return launch_one<16, kFp16, 1, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

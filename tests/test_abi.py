@@ -100,9 +100,9 @@ def test_plan_paths_and_tiles(L):
     assert dg.dg_gemm_plan(0, 10, 16, sm_count=sm)["path"] == 0
     assert dg.dg_gemm_plan(10, 0, 16, sm_count=sm)["path"] == 0
     assert dg.dg_gemm_plan(10, 10, 0, sm_count=sm)["path"] == 1
-    for m in (1, 2, 16):
+    for m, rows in ((1, 16), (4, 16), (5, 8), (16, 8)):
         p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
-        assert p["path"] == 2 and p["grid"] == 12288 // 8
+        assert p["path"] == 2 and p["block_n"] == rows and p["grid"] == 12288 // rows
     for m in (17, 63, 65, 129, 256, 4096, 8192):
         p = dg.dg_gemm_plan(m, 1000, 1040, sm_count=sm)
         assert p["path"] == 3
