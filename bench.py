@@ -51,6 +51,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["own", "reference"], default="own")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-workload kernel numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default=None, help="time one kernel workload alone")
+    ap.add_argument("--settle-seconds", type=float, default=1.5,
+                    help="untimed busy period before the timed steps (clock sampling)")
     return ap.parse_args(argv)
 
 
@@ -234,73 +237,121 @@ def time_kernel(torch, stream, fn, iters: int, warmup: int = 3) -> float:
     return s.elapsed_time(e) / iters
 
 
-def extras(torch, dg, synth, stream, peaks) -> dict:
-    """Kernel-level numbers for the other workloads (L2 defeated by rotating
-    several copies of every operand that would otherwise stay resident)."""
-    out = {}
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+def kernel_cases(torch, dg):
+    """Single-kernel workloads for the `extra` numbers, `--kernel` runs and
+    ncu captures.  Operands that would stay L2-resident between launches are
+    rotated over several copies (together more than 3 x L2)."""
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     dev = "cuda"
 
     def codes(shape, seed):
-        # any E4M3 code pattern works for timing; NaN codes are avoided
+        # timing only: any E4M3 code pattern (NaN codes avoided)
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
         t = torch.randint(0, 256, shape, dtype=torch.uint8, device=dev, generator=g)
         return torch.where((t & 0x7F) == 0x7F, torch.zeros_like(t), t)
 
+    def ncopies(nbytes):
+        return max(1, int(3 * l2 // max(nbytes, 1)) + 1)
+
     one = torch.ones(4, dtype=torch.float32, device=dev)
-    sd = torch.ones(4, dtype=torch.float32, device=dev)
 
-    # decode QKV projection: A [1,4096], B [12288,4096], BF16 out
-    Mq, Nq, Kq = 1, 12288, 4096
-    nb = int(3 * l2 // (Nq * Kq)) + 1
-    As = [codes((Mq, Kq), 10 + i) for i in range(nb)]
-    Bs = [codes((Nq, Kq), 20 + i) for i in range(nb)]
-    Dq = torch.empty((Mq, Nq), dtype=torch.bfloat16, device=dev)
-    ms = time_kernel(torch, stream, lambda i: dg.dg_fp8_gemm(As[i % nb], Bs[i % nb], Dq, one, one,
-                                                             None, dg.DG_BF16, stream=stream), 200)
-    qkv_bytes = Nq * Kq + Mq * Kq + Mq * Nq * 2
-    out["qkv_gemv_1x12288x4096"] = {"us": ms * 1e3, "GB/s": qkv_bytes / (ms * 1e-3) / 1e9,
-                                    "frac_hbm": qkv_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                                    "bytes": qkv_bytes, "l2": f"{nb} rotating copies"}
-    del As, Bs
+    def qkv():
+        Mq, Nq, Kq = 1, 12288, 4096
+        nb = ncopies(Nq * Kq)
+        As = [codes((Mq, Kq), 10 + i) for i in range(nb)]
+        Bs = [codes((Nq, Kq), 20 + i) for i in range(nb)]
+        D = torch.empty((Mq, Nq), dtype=torch.bfloat16, device=dev)
+        fn = lambda i, s: dg.dg_fp8_gemm(As[i % nb], Bs[i % nb], D, one, one, None,  # noqa: E731
+                                         dg.DG_BF16, stream=s)
+        return fn, 2.0 * Mq * Nq * Kq, Nq * Kq + Mq * Kq + Mq * Nq * 2, "hbm", f"{nb} rotating copies"
 
-    # 4096^3 FP8 (BF16 out) and FP16 (FP16 out)
-    S = 4096
-    flop = 2.0 * S ** 3
-    As = [codes((S, S), 30 + i) for i in range(4)]
-    Bs = [codes((S, S), 40 + i) for i in range(4)]
-    D = torch.empty((S, S), dtype=torch.bfloat16, device=dev)
-    ms = time_kernel(torch, stream, lambda i: dg.dg_fp8_gemm(As[i % 4], Bs[i % 4], D, one, one, None,
-                                                             dg.DG_BF16, stream=stream), 50)
-    fp8_peak = 2.0 * peaks["bf16_tflops"]
-    out["fp8_gemm_4096"] = {"us": ms * 1e3, "TFLOPS": flop / (ms * 1e-3) / 1e12,
-                            "frac_fp8_peak": flop / (ms * 1e-3) / 1e12 / fp8_peak}
-    del As, Bs
-    g = torch.Generator(device=dev)
-    g.manual_seed(5)
-    Hs = [(torch.rand((S, S), device=dev, generator=g) * 2 - 1).half() for _ in range(4)]
-    Hb = [(torch.rand((S, S), device=dev, generator=g) * 2 - 1).half() for _ in range(4)]
-    Dh = torch.empty((S, S), dtype=torch.float16, device=dev)
-    ms = time_kernel(torch, stream, lambda i: dg.dg_hgemm(Hs[i % 4], Hb[i % 4], Dh, dg.DG_FP16,
-                                                          stream=stream), 30)
-    out["fp16_hgemm_4096"] = {"us": ms * 1e3, "TFLOPS": flop / (ms * 1e-3) / 1e12,
-                              "frac_fp16_peak": flop / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
-    del Hs, Hb, Dh, D
+    def fp8_sq(S, out):
+        nb = ncopies(2 * S * S)
+        As = [codes((S, S), 30 + i) for i in range(nb)]
+        Bs = [codes((S, S), 40 + i) for i in range(nb)]
+        D = torch.empty((S, S), dtype=torch.uint8 if out == dg.DG_E4M3 else torch.bfloat16, device=dev)
+        fn = lambda i, s: dg.dg_fp8_gemm(As[i % nb], Bs[i % nb], D, one, one, one, out,  # noqa: E731
+                                         stream=s)
+        return fn, 2.0 * S ** 3, 2 * S * S + S * S * (1 if out == dg.DG_E4M3 else 2), "tensor_fp8", \
+            f"{nb} rotating copies"
 
-    # amax and quantise on an 8192^2 FP32 tensor (268 MB, > L2)
-    x = torch.randn((8192, 8192), device=dev)
-    am = torch.zeros(4, dtype=torch.float32, device=dev)
-    sc = torch.zeros(4, dtype=torch.float32, device=dev)
-    q = torch.empty((8192, 8192), dtype=torch.uint8, device=dev)
-    n = x.numel()
-    ms = time_kernel(torch, stream, lambda i: dg.dg_amax(x, am, sc, stream=stream), 50)
-    out["amax_8192sq"] = {"us": ms * 1e3, "GB/s": 4 * n / (ms * 1e-3) / 1e9,
-                          "frac_hbm": 4 * n / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
-    ms = time_kernel(torch, stream, lambda i: dg.dg_quantize_e4m3(x, sc, q, stream=stream), 50)
-    out["quantise_8192sq"] = {"us": ms * 1e3, "GB/s": 5 * n / (ms * 1e-3) / 1e9,
-                              "frac_hbm": 5 * n / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    def hgemm(S):
+        nb = ncopies(4 * S * S)
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        Hs = [(torch.rand((S, S), device=dev, generator=g) * 2 - 1).half() for _ in range(nb)]
+        Hb = [(torch.rand((S, S), device=dev, generator=g) * 2 - 1).half() for _ in range(nb)]
+        D = torch.empty((S, S), dtype=torch.float16, device=dev)
+        fn = lambda i, s: dg.dg_hgemm(Hs[i % nb], Hb[i % nb], D, dg.DG_FP16, stream=s)  # noqa: E731
+        return fn, 2.0 * S ** 3, 6 * S * S, "tensor_fp16", f"{nb} rotating copies"
+
+    def amax():
+        x = torch.randn((8192, 8192), device=dev)
+        am = torch.zeros(4, dtype=torch.float32, device=dev)
+        sc = torch.zeros(4, dtype=torch.float32, device=dev)
+        fn = lambda i, s: dg.dg_amax(x, am, sc, stream=s)  # noqa: E731
+        return fn, 0.0, 4 * x.numel(), "hbm", "268 MB input > L2"
+
+    def quant():
+        x = torch.randn((8192, 8192), device=dev)
+        sc = torch.full((4,), 0.01, dtype=torch.float32, device=dev)
+        q = torch.empty((8192, 8192), dtype=torch.uint8, device=dev)
+        fn = lambda i, s: dg.dg_quantize_e4m3(x, sc, q, stream=s)  # noqa: E731
+        return fn, 0.0, 5 * x.numel(), "hbm", "268 MB input > L2"
+
+    return {
+        "qkv_gemv_1x12288x4096": qkv,
+        "fp8_gemm_4096": lambda: fp8_sq(4096, dg.DG_BF16),
+        "fp8_gemm_8192_e4m3out": lambda: fp8_sq(8192, dg.DG_E4M3),
+        "fp16_hgemm_4096": lambda: hgemm(4096),
+        "amax_8192sq": amax,
+        "quantise_8192sq": quant,
+    }
+
+
+def measure_case(torch, dg, make, stream, peaks, iters, warmup=3) -> dict:
+    fn, flop, nbytes, bound, note = make()
+    ms = time_kernel(torch, stream, lambda i: fn(i, stream), iters, warmup)
+    st = dg.dg_sync_status()
+    assert st == dg.DG_OK, dg.dg_status_string(st)
+    rec = {"us": ms * 1e3, "GB/s": nbytes / (ms * 1e-3) / 1e9, "l2": note}
+    if flop:
+        rec["TFLOPS"] = flop / (ms * 1e-3) / 1e12
+    if bound == "hbm":
+        rec["frac_hbm"] = rec["GB/s"] / peaks["hbm_gbs"]
+    elif bound == "tensor_fp8":
+        rec["frac_fp8_peak"] = rec["TFLOPS"] / (2.0 * peaks["bf16_tflops"])
+    elif bound == "tensor_fp16":
+        rec["frac_fp16_peak"] = rec["TFLOPS"] / peaks["bf16_tflops"]
+    return rec
+
+
+def extras(torch, dg, stream, peaks) -> dict:
+    out = {}
+    for name, make in kernel_cases(torch, dg).items():
+        if name == "fp8_gemm_8192_e4m3out":
+            continue  # the headline step already times this kernel
+        out[name] = measure_case(torch, dg, make, stream, peaks, 50)
+        torch.cuda.empty_cache()
     return out
+
+
+def run_kernel(args):
+    """`--kernel NAME`: time one kernel workload alone (W warm-up + K timed
+    launches); used for ncu captures and tile sweeps."""
+    import torch
+
+    import fp16_tensor_core_gb300 as dg
+    torch.cuda.set_device(0)
+    dg.dg_init()
+    peaks = load_peaks()
+    cases = kernel_cases(torch, dg)
+    rec = measure_case(torch, dg, cases[args.kernel], torch.cuda.current_stream(), peaks,
+                       args.steps, args.warmup)
+    rec["kernel"] = args.kernel
+    rec["force_block_n"] = os.environ.get("DG_FORCE_BLOCK_N")
+    print(json.dumps(rec), flush=True)
 
 
 def cpu_baseline_sample(A32, B32, sd: float, rows: int) -> dict:
@@ -351,7 +402,7 @@ def run_own(args):
     torch.cuda.synchronize()
     # keep the GPU busy for ~1.5 s before the timed region so that the clock
     # sampler (100 ms period) sees the step under sustained load
-    t_end = time.time() + 1.5
+    t_end = time.time() + args.settle_seconds
     while time.time() < t_end:
         wl.step(stream)
         torch.cuda.synchronize()
@@ -449,7 +500,7 @@ def run_own(args):
     }
     del hA, hB, hD
     if rank == 0 and not args.no_extra:
-        line["extra"] = extras(torch, dg, synth, stream, peaks)
+        line["extra"] = extras(torch, dg, stream, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline_sample(A32, B32, sd, rows=768)
         line["cpu_baseline"] = {
@@ -503,6 +554,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel:
+        run_kernel(args)
     else:
         run_own(args)
 
