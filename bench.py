@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 M = N = K = 8192
 FLOP_PER_STEP = 2.0 * M * N * K
 WORKLOAD = "fp8_8192_e4m3out"
+CPU_SAMPLE_ROWS = 3072  # ~10-20 s of oracle work on 16 cores
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 GEMM_SOURCES = [os.path.join(ROOT, "fp16_tensor_core_gb300", "csrc", f)
                 for f in ("k_gemm_tc.cu", "dg_ptx.cuh")]
@@ -220,7 +221,7 @@ class Workload:
         if ev is not None:
             ev[1].record(stream)
 
-    KERNELS_PER_STEP = 7  # 2 x (amax + scale), 2 x quantise, 1 GEMM
+    KERNELS_PER_STEP = 9  # 2 x (amax init + amax + scale), 2 x quantise, 1 GEMM
 
 
 def time_kernel(torch, stream, fn, iters: int, warmup: int = 3) -> float:
@@ -457,6 +458,7 @@ def run_own(args):
     assert st == dg.DG_OK, dg.dg_status_string(st)
 
     fp8_peak = 2.0 * peaks["bf16_tflops"]
+    plan = dg.dg_gemm_plan(M, N, K, dg.DG_E4M3, dg.DG_E4M3)
     achieved = FLOP_PER_STEP / (gemm_ms * 1e-3) / 1e12
     traffic = recorded_traffic()
     line = {
@@ -482,7 +484,8 @@ def run_own(args):
         },
         "roofline": {
             "bound": "tensor",
-            "kernel": "gemm_tc_kernel (tcgen05 E4M3, 128x256 tiles)",
+            "kernel": f"gemm_tc_kernel (tcgen05 E4M3, {plan['block_m']}x{plan['block_n']} tiles, "
+                      f"{plan['stages']} stages, grid {plan['grid']})",
             "achieved": achieved,
             "peak": fp8_peak,
             "unit": "TFLOP/s",
@@ -502,11 +505,12 @@ def run_own(args):
     if rank == 0 and not args.no_extra:
         line["extra"] = extras(torch, dg, stream, peaks)
     if rank == 0 and not args.no_cpu_baseline:
-        cb = cpu_baseline_sample(A32, B32, sd, rows=768)
+        cb = cpu_baseline_sample(A32, B32, sd, rows=CPU_SAMPLE_ROWS)
         line["cpu_baseline"] = {
             "value": cb["flop"] / cb["seconds"] / 1e12, "unit": "TFLOPS", "cores": cb["cores"],
             "kind": "oracle", "seconds": cb["seconds"],
-            "sample": "rows 0-767 of A against all 8192 rows of B (768x8192x8192): full-tensor "
+            "sample": f"rows 0-{CPU_SAMPLE_ROWS - 1} of A against all 8192 rows of B "
+                      f"({CPU_SAMPLE_ROWS}x8192x8192): full-tensor "
                       "amax/scale of A and B, quantise of the sampled rows and all of B, FP64 "
                       "contraction, E4M3 epilogue"}
     if rank == 0:

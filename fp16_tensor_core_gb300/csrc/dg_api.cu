@@ -5,6 +5,7 @@
 #include <atomic>
 #include <climits>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "dg.h"
@@ -27,6 +28,14 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline dg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
 
 }  // namespace
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("DG_PDL");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 

@@ -25,6 +25,30 @@ struct DeviceState {
 // Returns the current device's state, creating it on first use.
 dg_status current_device_state(DeviceState** out);
 
+// Whether launches use programmatic dependent launch (on unless the
+// environment sets DG_PDL=0; read once).
+bool pdl_enabled();
+
+// Launches `kern` on `s`, with programmatic stream serialization when
+// pdl_enabled(): the kernel may be scheduled while the preceding kernel in
+// the stream drains, and waits (pdl_wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Runtime knobs (host globals, read at launch time).
 uint64_t wait_timeout_ns();
 bool take_skip_first_load();

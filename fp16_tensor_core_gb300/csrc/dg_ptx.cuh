@@ -21,6 +21,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Programmatic dependent launch: block until every grid this one depends on
+// has completed and its memory is visible.  Kernels launched with
+// programmatic stream serialization call this before their first access to
+// global memory, so that only their launch and prologue overlap the
+// preceding kernel's tail.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -194,6 +194,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();   // the prologue above overlaps the preceding kernel's tail
 
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     const int num_m = (p.M + kBM - 1) / kBM;
@@ -368,8 +369,8 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     CUtensorMap ta, tb;
     if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kBM) || !make_map(&tb, L.B, L.N, L.K, kFp16In, BN))
         return cudaErrorInvalidValue;
-    gemm_tc_kernel<BN, STAGES, kFp16In><<<L.plan->grid, kThreads, C::kSmemBytes, s>>>(ta, tb, prm);
-    return cudaGetLastError();
+    return launch_kernel(gemm_tc_kernel<BN, STAGES, kFp16In>, dim3(L.plan->grid), dim3(kThreads),
+                         C::kSmemBytes, s, ta, tb, prm);
 }
 
 template <bool kFp16In>

@@ -77,6 +77,7 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
             int M, int N, int K, const float* __restrict__ sa, const float* __restrict__ sb,
             const float* __restrict__ sd, int out_kind) {
     constexpr int H = kFp16 ? 4 : 8;   // f16x2 words per 16-byte chunk
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * kWarps + warp) * R;
     if (n0 >= N) return;  // warp-uniform
@@ -160,10 +161,9 @@ cudaError_t launch_one(const void* A, const void* B, void* D, int M, int N, int 
                        cudaStream_t s) {
     const int rows_per_block = kWarps * R;
     const dim3 grid((N + rows_per_block - 1) / rows_per_block), block(kWarps * 32);
-    gemv_kernel<MT, kFp16, R, U><<<grid, block, 0, s>>>(
-        static_cast<const uint8_t*>(A), static_cast<const uint8_t*>(B), D, M, N, K, sa, sb, sd,
-        out_kind);
-    return cudaGetLastError();
+    return launch_kernel(gemv_kernel<MT, kFp16, R, U>, grid, block, 0, s,
+                         static_cast<const uint8_t*>(A), static_cast<const uint8_t*>(B), D, M, N, K,
+                         sa, sb, sd, out_kind);
 }
 
 template <bool kFp16>

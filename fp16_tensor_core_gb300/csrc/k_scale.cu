@@ -34,6 +34,7 @@ __device__ __forceinline__ uint32_t abs_bits4(float4 v) {
 
 __global__ void __launch_bounds__(kAmaxThreads)
 amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_bits) {
+    pdl_wait();
     const int64_t n4 = n >> 2;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -62,8 +63,15 @@ amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_b
     }
 }
 
+// Zeroes the running maximum before the reduction.
+__global__ void amax_init_kernel(uint32_t* __restrict__ out_bits) {
+    pdl_wait();
+    *out_bits = 0u;
+}
+
 // scale = amax / 448 (one IEEE binary32 division), 1 for an all-zero tensor.
 __global__ void scale_kernel(const float* __restrict__ amax, float* __restrict__ scale) {
+    pdl_wait();
     const float a = *amax;
     *scale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
 }
@@ -80,6 +88,7 @@ __device__ __forceinline__ uint32_t quant4(float4 v, float s) {
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict__ scale_p,
                 uint8_t* __restrict__ q) {
+    pdl_wait();
     const float s = *scale_p;
     const int lane = threadIdx.x & 31;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -109,7 +118,8 @@ quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict_
 
 cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
                         int sm_count, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    uint32_t* bits = reinterpret_cast<uint32_t*>(amax_out);
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
     if (e != cudaSuccess) return e;
     if (n > 0) {
         const int64_t n4 = (n + 3) >> 2;
@@ -117,15 +127,12 @@ cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale
         const int64_t cap = static_cast<int64_t>(sm_count) * 4;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
-        amax_kernel<<<static_cast<unsigned>(blocks), kAmaxThreads, 0, s>>>(
-            x, n, reinterpret_cast<uint32_t*>(amax_out));
-        e = cudaGetLastError();
+        e = launch_kernel(amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kAmaxThreads), 0, s,
+                          x, n, bits);
         if (e != cudaSuccess) return e;
     }
-    if (scale_out) {
-        scale_kernel<<<1, 1, 0, s>>>(amax_out, scale_out);
-        e = cudaGetLastError();
-    }
+    if (scale_out) e = launch_kernel(scale_kernel, dim3(1), dim3(1), 0, s,
+                                     static_cast<const float*>(amax_out), scale_out);
     return e;
 }
 
@@ -138,8 +145,8 @@ cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale, 
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    quantize_kernel<<<static_cast<unsigned>(blocks), kQuantThreads, 0, s>>>(x, n, scale, q);
-    return cudaGetLastError();
+    return launch_kernel(quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads), 0,
+                         s, x, n, scale, q);
 }
 
 }  // namespace dg
