@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdg.so")
 
 SOURCES = ["dg_api.cu", "k_scale.cu", "k_gemv.cu", "k_gemm_tc.cu"]
-HEADERS = ["dg_ptx.cuh", "dg_internal.h"]
+HEADERS = ["dg_ptx.cuh", "dg_internal.h", "gemm_common.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -1,0 +1,138 @@
+// gemm_common.cuh -- pieces shared by the single-CTA and CTA-pair
+// tensor-core GEMM kernels: launch parameters, tile raster, the fused
+// scale/convert epilogue store and TMA tensor-map creation.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "dg_internal.h"
+#include "dg_ptx.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kThreads = 256;   // warps: 0 TMA, 1 MMA, 2 TMEM owner, 3 idle, 4-7 epilogue
+constexpr int kBKBytes = 128;   // one 128-byte swizzle row of K per stage
+
+constexpr uint32_t pow2_at_least(uint32_t v) {
+    uint32_t p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Shared memory per CTA available to a kernel (227 KB).
+constexpr int kSmemLimit = 232448;
+
+struct Params {
+    void* D;
+    int M, N, K;
+    const float* sa;
+    const float* sb;
+    const float* sd;
+    int out_kind;
+    int out_elem;
+    int vec_ok;
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int skip_first_load;
+    int group_m;   // tiles are rastered in groups of group_m M-tiles sweeping N
+};
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mt,
+                                            int& nt) {
+    const int group = group_m * num_n;
+    const int g = t / group;
+    const int first_m = g * group_m;
+    const int gm = min(num_m - first_m, group_m);
+    const int r = t - g * group;
+    mt = first_m + r % gm;
+    nt = r / gm;
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Scale, convert and store 32 consecutive accumulator columns of one row.
+__device__ __forceinline__ void store_chunk(const Params& p, int row, int col0,
+                                            const uint32_t (&r)[32], float alpha) {
+    if (row >= p.M) return;
+    const int ncols = min(32, p.N - col0);
+    if (ncols <= 0) return;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
+    const int64_t off = static_cast<int64_t>(row) * p.N + col0;
+    if (p.out_kind == kOutE4M3) {
+        uint8_t* dst = static_cast<uint8_t*>(p.D) + off;
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            w[j] = static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j], v[4 * j + 1])) |
+                   (static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j + 2], v[4 * j + 3])) << 16);
+        if (ncols == 32 && p.vec_ok) {
+            st_global_v4(dst, w[0], w[1], w[2], w[3]);
+            st_global_v4(dst + 16, w[4], w[5], w[6], w[7]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncols) dst[i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+        }
+    } else {
+        uint16_t* dst = static_cast<uint16_t*>(p.D) + off;
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            w[j] = p.out_kind == kOutFP16 ? f32x2_to_f16x2(v[2 * j], v[2 * j + 1])
+                                          : f32x2_to_bf16x2(v[2 * j], v[2 * j + 1]);
+        if (ncols == 32 && p.vec_ok) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                st_global_v4(dst + 8 * j, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < ncols) dst[i] = static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1)));
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D map over a rows x k row-major matrix, box = box_rows x 128 bytes,
+// 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap* map, const void* base, int rows, int k, bool fp16, int box_rows) {
+    auto encode = get_encode_fn();
+    if (!encode) return false;
+    const int elem = fp16 ? 2 : 1;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * elem};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes / elem), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                              2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace dg
