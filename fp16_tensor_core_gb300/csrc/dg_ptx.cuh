@@ -91,6 +91,67 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
     }
 }
 
+// ------------------------------------------------------- CTA-pair clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Whole-cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of this CTA's shared object `p` as seen in the
+// CTA of cluster rank `rank` (same offset, that CTA's shared memory).
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+
+// Arrive once on an mbarrier of another CTA of the cluster (release at
+// cluster scope, ordering this thread's earlier writes before the arrival).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 :: "r"(cluster_addr) : "memory");
+}
+
+// try_wait with acquire at cluster scope: the completing arrivals may come
+// from the peer CTA.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait as wait_bounded, with cluster-scope acquire.
+__device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity,
+                                                     const WaitCtl& ctl,
+                                                     bool honour_abort = true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t it = 0;
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((++it & 31u) == 0) {
+            if (honour_abort && *ctl.abort_flag) return false;
+            if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                *ctl.abort_flag = 1;
+                atomicOr(ctl.status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // -------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -107,6 +168,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
         " [%0], [%1, {%3, %4}], [%2];"
         :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)),
            "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// CTA-pair form of tma_load_2d: the box lands in this CTA's shared memory
+// and its bytes complete on the mbarrier at shared::cluster address
+// `bar_cluster`, which may belong to the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster),
+           "r"(x), "r"(y)
         : "memory");
 }
 
@@ -134,6 +208,57 @@ __device__ __forceinline__ void tc_fence_before_sync() {
 
 __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// CTA-pair forms.  Tensor memory for a pair is allocated and freed
+// collectively by one warp of each of the two CTAs; the pair MMA (M = 256)
+// is issued by one thread of the even CTA, reads A rows 0-127 from the even
+// CTA's shared memory and rows 128-255 from the odd CTA's (same offsets),
+// B's first N/2 rows from the even CTA and the rest from the odd CTA, and
+// writes each CTA's 128 rows of D into that CTA's tensor memory.
+template <uint32_t kCols>
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_in_smem) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_addr(dst_in_smem)), "r"(kCols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+template <uint32_t kCols>
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                 :: "r"(taddr), "r"(kCols) : "memory");
+}
+
+__device__ __forceinline__ void mma_f8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on the mbarrier at this shared-memory offset in every CTA of
+// `cta_mask` when all pair MMAs this thread issued before have completed.
+__device__ __forceinline__ void mma_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;"
+        :: "r"(smem_addr(bar)), "h"(cta_mask) : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one instruction of the given kind.

@@ -14,19 +14,6 @@
 #include "dg_ptx.cuh"
 
 namespace dg {
-namespace {
-
-constexpr int kThreads = 256;   // warps: 0 TMA, 1 MMA, 2 TMEM owner, 3 idle, 4-7 epilogue
-constexpr int kBKBytes = 128;   // one 128-byte swizzle row of K per stage
-
-constexpr uint32_t pow2_at_least(uint32_t v) {
-    uint32_t p = 32;
-    while (p < v) p <<= 1;
-    return p;
-}
-
-// Shared memory per CTA available to a kernel (227 KB).
-constexpr int kSmemLimit = 232448;
 
 struct Params {
     void* D;
@@ -42,6 +29,27 @@ struct Params {
     int skip_first_load;
     int group_m;   // tiles are rastered in groups of group_m M-tiles sweeping N
 };
+
+// CTA-pair kernel (k_gemm_tc2.cu): shared memory and stage count of the
+// 256 x bn pair tile, and its launcher.
+int pair_smem_for(int bn);
+int pair_stages(int bn);
+cudaError_t launch_gemm_tc_pair(const TcLaunch& L, const Params& prm, cudaStream_t s);
+
+namespace {
+
+constexpr int kThreads = 256;   // warps: 0 TMA, 1 MMA, 2 TMEM owner, 3 idle, 4-7 epilogue
+constexpr int kBKBytes = 128;   // one 128-byte swizzle row of K per stage
+
+constexpr uint32_t pow2_at_least(uint32_t v) {
+    uint32_t p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Shared memory per CTA available to a kernel (227 KB).
+constexpr int kSmemLimit = 232448;
+
 
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mt,
                                             int& nt) {

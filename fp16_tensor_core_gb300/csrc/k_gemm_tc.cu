@@ -322,6 +322,44 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     p->tiles = static_cast<int>(tiles);
     p->grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
     p->smem_bytes = smem_for(best);
+
+    // CTA pairs (256 x BN tiles over sm_count / 2 clusters), for M >= 256.
+    // Per-SM throughput relative to the single-CTA 128 x 256 tile: each SM
+    // stores and reads only half of the tile's B rows.  Measured on GB300:
+    // 8192^3 E4M3 3607 vs 3399 TFLOP/s (1.06); at 4096^3 (BN 224) both run
+    // 48 us.  Pairs are used when their estimate is no worse; DG_2CTA=0
+    // disables them, DG_2CTA=1 forces them for M >= 256.
+    const char* pair_env = std::getenv("DG_2CTA");
+    const bool pairs_off = pair_env != nullptr && pair_env[0] == '0';
+    const bool pairs_forced = pair_env != nullptr && pair_env[0] == '1';
+    if (!pairs_off && M >= 256 && sm_count >= 2) {
+        const int64_t pm = (M + 255) / 256;
+        const int slots = sm_count / 2;
+        const int pcand[5] = {256, 224, 192, 160, 128};
+        const double peff[5] = {1.06, 1.0, 0.93, 0.85, 0.76};
+        int pbest = 256;
+        double pcost = 0.0;
+        for (int i = 0; i < 5; ++i) {
+            const int bn = pcand[i];
+            const int64_t pt = pm * ((N + bn - 1) / bn);
+            const int64_t waves = (pt + slots - 1) / slots;
+            const double cost = static_cast<double>(waves) * bn / peff[i];
+            if (i == 0 || cost < pcost) { pbest = bn; pcost = cost; }
+        }
+        if (const char* f = std::getenv("DG_FORCE_BLOCK_N")) {
+            const int v = std::atoi(f);
+            if (v == 128 || v == 160 || v == 192 || v == 224 || v == 256) pbest = v;
+        }
+        if (pairs_forced || pcost <= best_cost) {
+            const int64_t pt = pm * ((N + pbest - 1) / pbest);
+            p->block_m = 256;
+            p->block_n = pbest;
+            p->stages = pair_stages(pbest);
+            p->tiles = static_cast<int>(pt);
+            p->grid = static_cast<int>(2 * (pt < slots ? pt : slots));
+            p->smem_bytes = pair_smem_for(pbest);
+        }
+    }
     (void)K;
 }
 
@@ -343,11 +381,13 @@ cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s) {
     // Raster: groups of 32 M-tiles when there are many (8192^3: 3361 vs 3285
     // TFLOP/s at 16, measured), 8 otherwise (4096^3: 2865 vs 2830).
     prm.group_m = ((L.M + kBM - 1) / kBM) >= 48 ? 32 : 8;
+    if (L.plan->block_m == 256) prm.group_m /= 2;   // pair tiles are 256 rows
     // DG_GROUP_M=<n> overrides the raster group size (sweeps).
     if (const char* g = std::getenv("DG_GROUP_M")) {
         const int v = std::atoi(g);
         if (v >= 1 && v <= 4096) prm.group_m = v;
     }
+    if (L.plan->block_m == 256) return launch_gemm_tc_pair(L, prm, s);
     return L.fp16_in ? launch_in<true>(L, prm, s) : launch_in<false>(L, prm, s);
 }
 

@@ -1,0 +1,344 @@
+// k_gemm_tc2.cu -- CTA-pair variant of the tensor-core GEMM (M >= 256).
+//
+// Page shorthands: [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南";
+// [DG-FP16] = the DeepGEMM FP16/WMMA deep-dive page.
+//
+// Same computation and epilogue as k_gemm_tc.cu ([FP8-guide] §2.3, §3.1-§3.3;
+// [DG-FP16] §2.2), but two CTAs on two SMs (a cluster of 2) share one
+// 256 x BN output tile.  Each CTA holds its own 128 rows of A and half of the
+// tile's BN rows of B; one pair MMA (M = 256) reads A from both CTAs and B
+// from both CTAs, and writes each CTA's 128 rows of the accumulator into that
+// CTA's tensor memory.  Per SM this halves the B bytes that TMA writes into
+// shared memory and that the MMA reads from it, the traffic that limits the
+// single-CTA kernel with 128 x 256 tiles.
+//
+// Signalling (all waits bounded):
+//  * each CTA's producer loads its halves into its own shared memory; every
+//    box completes on the even CTA's `full` barrier of the stage, whose
+//    producer arms it for the bytes of both CTAs;
+//  * the even CTA's MMA thread issues the pair MMAs and frees a stage in both
+//    CTAs with one multicast commit to `empty`; at the end of a tile it
+//    commits to `acc_full` in both CTAs;
+//  * both CTAs' epilogue warps release an accumulator buffer by arriving on
+//    the even CTA's `acc_empty` (count 8: four warps per CTA);
+//  * a final multicast commit to `drain` tells both CTAs that no pair MMA
+//    still reads their shared memory or writes their tensor memory; only
+//    then is tensor memory freed (collectively) and the CTAs exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "dg_internal.h"
+#include "dg_ptx.cuh"
+#include "gemm_common.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kPairBM = 256;   // output rows of a pair tile
+constexpr int kHalfBM = 128;   // rows of it per CTA
+
+constexpr int pair_stages_for(int bn) {
+    const int st = (kSmemLimit - 1024 - 256) / (kHalfBM * kBKBytes + (bn / 2) * kBKBytes);
+    return st > 8 ? 8 : st;
+}
+
+template <int BN, int STAGES, bool kFp16In>
+struct PairCfg {
+    static constexpr int kBK = kFp16In ? 64 : 128;         // K elements per stage
+    static constexpr int kABytes = kHalfBM * kBKBytes;     // this CTA's 128 rows of A
+    static constexpr int kBRows = BN / 2;                  // this CTA's rows of B
+    static constexpr int kBBytes = kBRows * kBKBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + 256;
+    static constexpr uint32_t kIdesc = idesc_f32acc(kPairBM, BN, 0, 0);
+    static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "BN");
+    static_assert(kBBytes % 1024 == 0, "1024-byte aligned B stages (128-byte swizzle atoms)");
+    static_assert(kTmemCols <= 512, "TMEM columns");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+};
+
+template <int BN, int STAGES, bool kFp16In>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+    using C = PairCfg<BN, STAGES, kFp16In>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * C::kABytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;   // [2]
+    uint64_t* acc_empty = acc_full + 2;    // [2], used in the even CTA
+    uint64_t* drain = acc_empty + 2;       // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 8);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+    }
+    // Both CTAs' barriers are initialised before either can signal the other.
+    __syncwarp();
+    cluster_sync_all();
+    if (warp == 2) {
+        tmem_alloc_pair<C::kTmemCols>(tmem_slot);
+        tmem_relinquish_pair();
+    }
+    // Tensor memory exists in both CTAs before the even CTA's MMAs write it.
+    tc_fence_before_sync();
+    cluster_sync_all();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();
+
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    const int num_m = (p.M + kPairBM - 1) / kPairBM;
+    const int num_n = (p.N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (p.K + C::kBK - 1) / C::kBK;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_phase = 0;
+        bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
+        bool ok = true;
+        const uint32_t leader_full = map_to_rank(full, 0);
+        for (int t = pair; t < num_tiles && ok; t += npairs) {
+            int mt, nt;
+            tile_coords(t, num_m, num_n, p.group_m, mt, nt);
+            const int a_row = mt * kPairBM + static_cast<int>(rank) * kHalfBM;
+            const int b_row = nt * BN + static_cast<int>(rank) * C::kBRows;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
+                if (skip) {
+                    skip = false;            // leave this stage unloaded
+                } else {
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+                    const uint32_t bar = leader_full + static_cast<uint32_t>(stage) * 8u;
+                    tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, bar, kb * C::kBK, a_row);
+                    tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, bar, kb * C::kBK, b_row);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        // The even CTA's barriers cover both CTAs' boxes: once every stage it
+        // armed has completed, every box of both CTAs has landed.  (The odd
+        // CTA's boxes were all consumed by MMAs before the final `drain`
+        // commit, which the odd CTA waits for.)
+        if (leader)
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_mask & (1u << s))
+                    wait_bounded_cluster(&full[s], (issued_phase >> s) & 1u, ctl, false);
+    } else if (warp == 1 && lane == 0) {
+        if (leader) {
+            // -------------------------------------------- pair MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = pair; t < num_tiles && ok; t += npairs) {
+                if (!wait_bounded_cluster(&acc_empty[acc], acc_phase ^ 1u, ctl)) { ok = false; break; }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!wait_bounded_cluster(&full[stage], phase, ctl)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
+                    const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBKBytes / 32; ++kk) {
+                        const uint64_t ad = sdesc_k_major_sw128(a0 + kk * 32);
+                        const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
+                        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (kFp16In)
+                            mma_f16_pair(d_tmem, ad, bd, C::kIdesc, accum);
+                        else
+                            mma_f8f6f4_pair(d_tmem, ad, bd, C::kIdesc, accum);
+                    }
+                    mma_commit_pair_multicast(&empty[stage], 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit_pair_multicast(&acc_full[acc], 0x3);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            // Both CTAs learn here that every pair MMA has completed.
+            mma_commit_pair_multicast(drain, 0x3);
+            wait_bounded(drain, 0, ctl, false);
+        } else {
+            // Odd CTA: its shared and tensor memory stay in use until the
+            // even CTA's MMAs are done.
+            wait_bounded_cluster(drain, 0, ctl, false);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        float alpha = 1.0f;
+        if (p.sa != nullptr) alpha = (*p.sa) * (*p.sb);
+        if (p.out_kind == kOutE4M3) alpha = __fdiv_rn(alpha, *p.sd);
+        const uint32_t leader_acc_empty = map_to_rank(acc_empty, 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = pair; t < num_tiles; t += npairs) {
+            int mt, nt;
+            tile_coords(t, num_m, num_n, p.group_m, mt, nt);
+            const bool got = wait_bounded_cluster(&acc_full[acc], acc_phase, ctl);
+            if (!__all_sync(0xFFFFFFFFu, got)) break;
+            tc_fence_after_sync();
+            const int row = mt * kPairBM + static_cast<int>(rank) * kHalfBM + q * 32 + lane;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                __syncwarp();
+                tmem_load_32cols(tbase + c * 32, r);
+                tmem_load_wait(r);
+                store_chunk(p, row, nt * BN + c * 32, r, alpha);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(&acc_empty[acc]);
+                else
+                    mbar_arrive_cluster(leader_acc_empty + static_cast<uint32_t>(acc) * 8u);
+            }
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncwarp();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 2) tmem_dealloc_pair<C::kTmemCols>(tmem_base);
+    // No arrival from one CTA may land in the other after it has exited.
+    __syncwarp();
+    cluster_sync_all();
+}
+
+template <typename Kern>
+cudaError_t launch_pair(Kern kern, dim3 grid, size_t smem, cudaStream_t s,
+                        const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, prm);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int BN, int STAGES, bool kFp16In>
+cudaError_t launch_pair_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
+    using C = PairCfg<BN, STAGES, kFp16In>;
+    auto kern = gemm_tc_pair_kernel<BN, STAGES, kFp16In>;
+    static std::mutex mu;
+    static int max_clusters[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int clusters;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (max_clusters[dev] == 0) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            if (e != cudaSuccess) return e;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = C::kSmemBytes;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            if (n < 1) return cudaErrorInvalidConfiguration;
+            max_clusters[dev] = n;
+        }
+        clusters = max_clusters[dev];
+    }
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kHalfBM) ||
+        !make_map(&tb, L.B, L.N, L.K, kFp16In, C::kBRows))
+        return cudaErrorInvalidValue;
+    const int pairs = L.plan->tiles < clusters ? L.plan->tiles : clusters;
+    return launch_pair(kern, dim3(2 * pairs), C::kSmemBytes, s, ta, tb, prm);
+}
+
+template <bool kFp16In>
+cudaError_t launch_pair_in(const TcLaunch& L, const Params& prm, cudaStream_t s) {
+    switch (L.plan->block_n) {
+        case 128: return launch_pair_cfg<128, pair_stages_for(128), kFp16In>(L, prm, s);
+        case 160: return launch_pair_cfg<160, pair_stages_for(160), kFp16In>(L, prm, s);
+        case 192: return launch_pair_cfg<192, pair_stages_for(192), kFp16In>(L, prm, s);
+        case 224: return launch_pair_cfg<224, pair_stages_for(224), kFp16In>(L, prm, s);
+        default: return launch_pair_cfg<256, pair_stages_for(256), kFp16In>(L, prm, s);
+    }
+}
+
+}  // namespace
+
+int pair_smem_for(int bn) {
+    switch (bn) {
+        case 128: return PairCfg<128, pair_stages_for(128), false>::kSmemBytes;
+        case 160: return PairCfg<160, pair_stages_for(160), false>::kSmemBytes;
+        case 192: return PairCfg<192, pair_stages_for(192), false>::kSmemBytes;
+        case 224: return PairCfg<224, pair_stages_for(224), false>::kSmemBytes;
+        default: return PairCfg<256, pair_stages_for(256), false>::kSmemBytes;
+    }
+}
+
+int pair_stages(int bn) { return pair_stages_for(bn); }
+
+cudaError_t launch_gemm_tc_pair(const TcLaunch& L, const Params& prm, cudaStream_t s) {
+    return L.fp16_in ? launch_pair_in<true>(L, prm, s) : launch_pair_in<false>(L, prm, s);
+}
+
+}  // namespace dg

@@ -106,8 +106,12 @@ def test_plan_paths_and_tiles(L):
     for m in (17, 63, 65, 129, 256, 4096, 8192):
         p = dg.dg_gemm_plan(m, 1000, 1040, sm_count=sm)
         assert p["path"] == 3
-        assert p["block_m"] == 128 and p["block_n"] in (64, 128, 256)
-        assert p["grid"] <= sm and p["grid"] <= p["tiles"]
+        assert p["block_n"] in (64, 128, 160, 192, 224, 256)
+        if p["block_m"] == 256:            # CTA pairs: M >= 256, even grid
+            assert m >= 256 and p["grid"] % 2 == 0 and p["grid"] <= 2 * p["tiles"]
+        else:
+            assert p["block_m"] == 128 and p["grid"] <= p["tiles"]
+        assert p["grid"] <= sm
         assert p["smem_bytes"] <= 232448
         assert p["block_k"] == 128
     # FP16 operands: 64 K elements (128 bytes) per stage
@@ -117,7 +121,10 @@ def test_plan_paths_and_tiles(L):
     small = dg.dg_gemm_plan(65, 1000, 1040, sm_count=sm)
     big = dg.dg_gemm_plan(8192, 8192, 8192, sm_count=sm)
     assert small["block_n"] < big["block_n"]
-    assert big["grid"] == sm
+    assert big["grid"] == sm and big["block_m"] == 256 and big["block_n"] == 256
+    # 4096^3: 304 pair tiles of 256 x 224 = exactly four waves over 76 pairs
+    sq = dg.dg_gemm_plan(4096, 4096, 4096, sm_count=sm)
+    assert (sq["block_m"], sq["block_n"], sq["tiles"]) == (256, 224, 304)
 
 
 def test_plan_argument_errors(L):
