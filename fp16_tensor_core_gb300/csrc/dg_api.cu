@@ -108,7 +108,7 @@ dg_status check_sizes(int64_t M, int64_t N, int64_t K) {
 
 dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                    bool fp16_in, const float* sa, const float* sb, const float* sd,
-                   dg_dtype out, cudaStream_t s) {
+                   dg_dtype out, cudaStream_t s, float* amax_d = nullptr) {
     DeviceState* st = nullptr;
     dg_status rc = current_device_state(&st);
     if (rc != DG_OK) return rc;
@@ -116,6 +116,12 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
     rc = make_plan(M, N, K, fp16_in, st->sm_count, &plan);
     if (rc != DG_OK) return rc;
     const int ok = out_kind_of(out);
+    uint32_t* amax_bits = reinterpret_cast<uint32_t*>(amax_d);
+    if (amax_bits != nullptr) {
+        // The running maximum starts at +0 (also the result for an empty or
+        // K == 0 product).
+        if (launch_zero_word(amax_bits, s) != cudaSuccess) return DG_ERR_CUDA;
+    }
     switch (plan.path) {
         case 0:
             return DG_OK;
@@ -123,7 +129,8 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             return from_cuda(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * elem_bytes(out)), s));
         case 2:
             return from_cuda(launch_gemv(A, B, D, static_cast<int>(M), static_cast<int>(N),
-                                         static_cast<int>(K), fp16_in, sa, sb, sd, ok, s));
+                                         static_cast<int>(K), fp16_in, sa, sb, sd, ok, amax_bits,
+                                         s));
         default: {
             TcLaunch L;
             L.A = A;
@@ -140,6 +147,7 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             L.out_elem = elem_bytes(out);
             L.plan = &plan;
             L.status = st->status;
+            L.amax_out = amax_bits;
             return from_cuda(launch_gemm_tc(L, s));
         }
     }
@@ -195,6 +203,27 @@ dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M, in
     }
     return run_gemm(A, B, D, M, N, K, false, scale_a, scale_b, scale_d, out,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp8_gemm_amax(const uint8_t* A, const uint8_t* B, void* D, int64_t M, int64_t N,
+                           int64_t K, const float* scale_a, const float* scale_b,
+                           const float* scale_d, dg_dtype out, float* amax_d,
+                           dg_stream_t stream) {
+    if (amax_d == nullptr) return DG_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(amax_d) & 3u) != 0) return DG_ERR_MISALIGNED;
+    dg_status rc = check_sizes(M, N, K);
+    if (rc != DG_OK) return rc;
+    if (out != DG_BF16 && out != DG_E4M3 && out != DG_FP16) return DG_ERR_INVALID_VALUE;
+    if (M > 0 && N > 0) {
+        if (D == nullptr) return DG_ERR_INVALID_VALUE;
+        if (K > 0 && (A == nullptr || B == nullptr || scale_a == nullptr || scale_b == nullptr))
+            return DG_ERR_INVALID_VALUE;
+        if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0)
+            return DG_ERR_MISALIGNED;
+    }
+    return run_gemm(A, B, D, M, N, K, false, scale_a, scale_b, scale_d, out,
+                    reinterpret_cast<cudaStream_t>(stream), amax_d);
 }
 
 dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M, int64_t N,

@@ -60,7 +60,10 @@ cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale,
                                  uint8_t* q, int sm_count, cudaStream_t s);
 cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N,
                         int K, bool fp16_in, const float* sa, const float* sb,
-                        const float* sd, int out_kind, cudaStream_t s);
+                        const float* sd, int out_kind, uint32_t* amax_out,
+                        cudaStream_t s);
+// Sets *bits = 0 on stream s (one-thread kernel).
+cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s);
 
 struct TcLaunch {
     const void* A;
@@ -75,6 +78,7 @@ struct TcLaunch {
     int out_elem;
     const dg_plan* plan;
     uint32_t* status;
+    uint32_t* amax_out;   // optional running max |sa*sb*acc| (float bits)
 };
 cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s);
 

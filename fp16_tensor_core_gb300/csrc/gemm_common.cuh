@@ -28,6 +28,7 @@ struct Params {
     uint64_t timeout_ns;
     int skip_first_load;
     int group_m;   // tiles are rastered in groups of group_m M-tiles sweeping N
+    uint32_t* amax_out;  // optional: running max |sa*sb*acc| as float bits
 };
 
 // CTA-pair kernel (k_gemm_tc2.cu): shared memory and stage count of the
@@ -68,11 +69,19 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 }
 
 // Scale, convert and store 32 consecutive accumulator columns of one row.
-__device__ __forceinline__ void store_chunk(const Params& p, int row, int col0,
-                                            const uint32_t (&r)[32], float alpha) {
-    if (row >= p.M) return;
+// Returns max |acc| over the stored elements as ordered bits (the bit
+// pattern of a non-negative float; NaN above every number), 0 if none.
+__device__ __forceinline__ uint32_t store_chunk(const Params& p, int row, int col0,
+                                                const uint32_t (&r)[32], float alpha) {
+    if (row >= p.M) return 0u;
     const int ncols = min(32, p.N - col0);
-    if (ncols <= 0) return;
+    if (ncols <= 0) return 0u;
+    uint32_t amax_bits = 0u;
+    if (p.amax_out != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < ncols) amax_bits = max(amax_bits, r[i] & 0x7FFFFFFFu);
+    }
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
@@ -108,6 +117,21 @@ __device__ __forceinline__ void store_chunk(const Params& p, int row, int col0,
             for (int i = 0; i < 32; ++i)
                 if (i < ncols) dst[i] = static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1)));
         }
+    }
+    return amax_bits;
+}
+
+// Publishes one warp's running max |acc| (ordered bits) as
+// max |acc| * (sa * sb) into p.amax_out.  Rounding is monotone, so
+// fl(max|acc| * c) = max fl(|acc| * c) exactly.  Whole warp, converged.
+__device__ __forceinline__ void publish_amax(const Params& p, uint32_t amax_bits) {
+    if (p.amax_out == nullptr) return;
+    amax_bits = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+    if ((threadIdx.x & 31) == 0 && amax_bits != 0u) {
+        float ab = 1.0f;
+        if (p.sa != nullptr) ab = (*p.sa) * (*p.sb);
+        const float v = __uint_as_float(amax_bits) * ab;
+        atomicMax(p.amax_out, __float_as_uint(v) & 0x7FFFFFFFu);
     }
 }
 

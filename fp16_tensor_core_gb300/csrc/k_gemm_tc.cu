@@ -199,6 +199,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         float alpha = 1.0f;
         if (p.sa != nullptr) alpha = (*p.sa) * (*p.sb);
         if (p.out_kind == kOutE4M3) alpha = __fdiv_rn(alpha, *p.sd);
+        uint32_t amax_bits = 0u;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -218,13 +219,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 tmem_load_32cols(tbase + c * 32, r);
                 tmem_load_wait(r);
-                store_chunk(p, row, nt * BN + c * 32, r, alpha);
+                amax_bits = max(amax_bits, store_chunk(p, row, nt * BN + c * 32, r, alpha));
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        __syncwarp();
+        publish_amax(p, amax_bits);
     }
 
     tc_fence_before_sync();
@@ -378,6 +381,7 @@ cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s) {
     prm.status = L.status;
     prm.timeout_ns = wait_timeout_ns();
     prm.skip_first_load = take_skip_first_load() ? 1 : 0;
+    prm.amax_out = L.amax_out;
     // Raster: groups of 32 M-tiles when there are many (8192^3: 3361 vs 3285
     // TFLOP/s at 16, measured), 8 otherwise (4096^3: 2865 vs 2830).
     prm.group_m = ((L.M + kBM - 1) / kBM) >= 48 ? 32 : 8;

@@ -207,6 +207,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (p.sa != nullptr) alpha = (*p.sa) * (*p.sb);
         if (p.out_kind == kOutE4M3) alpha = __fdiv_rn(alpha, *p.sd);
         const uint32_t leader_acc_empty = map_to_rank(acc_empty, 0);
+        uint32_t amax_bits = 0u;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = pair; t < num_tiles; t += npairs) {
@@ -224,7 +225,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 tmem_load_32cols(tbase + c * 32, r);
                 tmem_load_wait(r);
-                store_chunk(p, row, nt * BN + c * 32, r, alpha);
+                amax_bits = max(amax_bits, store_chunk(p, row, nt * BN + c * 32, r, alpha));
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -236,6 +237,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        __syncwarp();
+        publish_amax(p, amax_bits);
     }
 
     tc_fence_before_sync();

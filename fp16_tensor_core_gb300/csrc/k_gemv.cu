@@ -75,7 +75,7 @@ template <int MT, bool kFp16, int R, int U>
 __global__ void __launch_bounds__(kWarps * 32)
 gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* __restrict__ D,
             int M, int N, int K, const float* __restrict__ sa, const float* __restrict__ sb,
-            const float* __restrict__ sd, int out_kind) {
+            const float* __restrict__ sd, int out_kind, uint32_t* __restrict__ amax_out) {
     constexpr int H = kFp16 ? 4 : 8;   // f16x2 words per 16-byte chunk
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,7 +139,18 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
             if (lane == m * R + r) mine = s;
         }
     const int m = lane / R, r = lane % R;
-    if (m < M && m < MT && n0 + r < N) {
+    const bool writes = m < M && m < MT && n0 + r < N;
+    if (amax_out != nullptr) {
+        // max |sa*sb*acc| over this warp's outputs; monotone rounding makes
+        // fl(max|acc| * c) the exact maximum of fl(|acc| * c).
+        const uint32_t bits = __reduce_max_sync(0xFFFFFFFFu, writes ? (__float_as_uint(mine) & 0x7FFFFFFFu) : 0u);
+        if (lane == 0 && bits != 0u) {
+            float ab = 1.0f;
+            if (sa != nullptr) ab = (*sa) * (*sb);
+            atomicMax(amax_out, __float_as_uint(__uint_as_float(bits) * ab) & 0x7FFFFFFFu);
+        }
+    }
+    if (writes) {
         const float v = mine * alpha;
         const int64_t off = static_cast<int64_t>(m) * N + n0 + r;
         if (out_kind == kOutE4M3) {
@@ -158,24 +169,24 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
 template <int MT, bool kFp16, int R, int U>
 cudaError_t launch_one(const void* A, const void* B, void* D, int M, int N, int K,
                        const float* sa, const float* sb, const float* sd, int out_kind,
-                       cudaStream_t s) {
+                       uint32_t* amax_out, cudaStream_t s) {
     const int rows_per_block = kWarps * R;
     const dim3 grid((N + rows_per_block - 1) / rows_per_block), block(kWarps * 32);
     return launch_kernel(gemv_kernel<MT, kFp16, R, U>, grid, block, 0, s,
                          static_cast<const uint8_t*>(A), static_cast<const uint8_t*>(B), D, M, N, K,
-                         sa, sb, sd, out_kind);
+                         sa, sb, sd, out_kind, amax_out);
 }
 
 template <bool kFp16>
 cudaError_t launch_mt(int MT, const void* A, const void* B, void* D, int M, int N, int K,
                       const float* sa, const float* sb, const float* sd, int out_kind,
-                      cudaStream_t s) {
+                      uint32_t* amax_out, cudaStream_t s) {
     switch (MT) {
-        case 1: return launch_one<1, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
-        case 2: return launch_one<2, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
-        case 4: return launch_one<4, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
-        case 8: return launch_one<8, kFp16, 1, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
-        default: return launch_one<16, kFp16, 1, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, s);
+        case 1: return launch_one<1, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
+        case 2: return launch_one<2, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
+        case 4: return launch_one<4, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
+        case 8: return launch_one<8, kFp16, 1, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
+        default: return launch_one<16, kFp16, 1, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
     }
 }
 
@@ -183,10 +194,10 @@ cudaError_t launch_mt(int MT, const void* A, const void* B, void* D, int M, int 
 
 cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N, int K, bool fp16_in,
                         const float* sa, const float* sb, const float* sd, int out_kind,
-                        cudaStream_t s) {
+                        uint32_t* amax_out, cudaStream_t s) {
     const int MT = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
-    return fp16_in ? launch_mt<true>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, s)
-                   : launch_mt<false>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, s);
+    return fp16_in ? launch_mt<true>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s)
+                   : launch_mt<false>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
 }
 
 }  // namespace dg

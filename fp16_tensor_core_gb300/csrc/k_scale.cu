@@ -136,6 +136,10 @@ cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale
     return e;
 }
 
+cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s) {
+    return launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
+}
+
 cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_t* q,
                                  int sm_count, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;

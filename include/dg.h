@@ -103,6 +103,26 @@ dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M,
                       const float* scale_b, const float* scale_d, dg_dtype out,
                       dg_stream_t stream);
 
+/* dg_fp8_gemm that also reports the output's largest magnitude, for delayed
+ * output scaling.  [FP8-guide] §3.2: calibration records each GEMM's largest
+ * absolute output, and the output scale is that value over 448.  Besides
+ * everything dg_fp8_gemm does, this call writes
+ *   *amax_d = max over m < M, n < N of |scale_a * scale_b * acc[m,n]|
+ * -- the unrounded output before the division by scale_d and the output
+ * rounding -- in binary32 (NaN-propagating; +0 when M, N or K is 0), so that
+ * the next call's output scale can be fl32(*amax_d / 448) with no host round
+ * trip.  The maximum is taken on the epilogue's registers: no extra pass
+ * over D.
+ *   amax_d  FP32[1], device, 4-byte aligned; zeroed by the call (a
+ *           one-thread kernel) before the GEMM runs.
+ * Other arguments, layouts and errors as dg_fp8_gemm; amax_d == NULL is
+ * DG_ERR_INVALID_VALUE. */
+dg_status dg_fp8_gemm_amax(const uint8_t* A, const uint8_t* B, void* D,
+                           int64_t M, int64_t N, int64_t K,
+                           const float* scale_a, const float* scale_b,
+                           const float* scale_d, dg_dtype out, float* amax_d,
+                           dg_stream_t stream);
+
 /* FP16 GEMM (HGEMM), FP32 accumulation, no scaling.  [HGEMM-L2] §1.3 (FP16
  * inputs, FP32 accumulator) and §3; same layouts and edge rules as
  * dg_fp8_gemm.  A, B hold IEEE binary16 bit patterns.  K must be a multiple

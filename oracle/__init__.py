@@ -58,6 +58,8 @@ def lib():
             L.dgo_amax.restype = ctypes.c_float
             L.dgo_scale_from_amax.argtypes = [ctypes.c_float]
             L.dgo_scale_from_amax.restype = ctypes.c_float
+            L.dgo_scale_pow2_from_amax.argtypes = [ctypes.c_float]
+            L.dgo_scale_pow2_from_amax.restype = ctypes.c_float
             L.dgo_quantize_e4m3.argtypes = [_f32p, _i64, ctypes.c_float, _u8p]
             L.dgo_quantize_e4m3.restype = None
             L.dgo_gemm_e4m3.argtypes = [_u8p, _u8p, _i64, _i64, _i64, _f64p,
@@ -150,6 +152,18 @@ def amax(x) -> np.float32:
 def scale_from_amax(a) -> np.float32:
     """fl32(amax / 448), 1 for amax == 0 ([FP8-guide] §3.2)."""
     return np.float32(lib().dgo_scale_from_amax(float(np.float32(a))))
+
+
+def scale_pow2_from_amax(a) -> np.float32:
+    """Smallest power of two p with 448 p >= amax ([FP8-guide] §2.1)."""
+    return np.float32(lib().dgo_scale_pow2_from_amax(float(np.float32(a))))
+
+
+def quantize_tensor_pow2(x):
+    """(codes, scale, amax) with the power-of-two per-tensor scale."""
+    a = amax(x)
+    s = scale_pow2_from_amax(a)
+    return quantize_e4m3(x, s), s, a
 
 
 def quantize_e4m3(x, scale) -> np.ndarray:

@@ -197,6 +197,19 @@ float dgo_scale_from_amax(float amax) {
     return amax / 448.0f; /* one binary32 division */
 }
 
+/* [FP8-guide] §2.1: instead of amax/448 itself, a power of two slightly
+ * larger, so that dividing by the scale is exact.  Smallest p = 2^e, e >=
+ * -149, with 448 * p >= amax; both sides exact in double. */
+float dgo_scale_pow2_from_amax(float amax) {
+    if (isnan(amax)) return NAN;
+    if (amax == 0.0f) return 1.0f;
+    if (isinf(amax)) return INFINITY;
+    const double a = (double)amax;
+    int e = -149;
+    while (448.0 * ldexp(1.0, e) < a) ++e;
+    return (float)ldexp(1.0, e);
+}
+
 /* [FP8-guide] §4.3: fp8 = clamp(round(x / scale), -448, 448), read as
  * round-to-nearest-even onto the E4M3 grid after a binary32 division. */
 static void quantize_range(const float* x, int64_t lo, int64_t hi, float scale,

@@ -48,6 +48,11 @@ uint16_t dgo_fp16_encode(double y);
 float dgo_amax(const float* x, int64_t n);
 /* scale = fl32(amax / 448); 1 when amax == 0.  [FP8-guide] §3.2. */
 float dgo_scale_from_amax(float amax);
+/* Power-of-two scale: the smallest power of two p (a binary32 value, at
+ * least 2^-149) with 448 * p >= amax, compared exactly; 1 when amax == 0,
+ * NaN for NaN, +Inf for +Inf.  [FP8-guide] §2.1: a power of two just above
+ * the range, so that scaling and unscaling are exponent shifts. */
+float dgo_scale_pow2_from_amax(float amax);
 /* q_i = e4m3(fl32(x_i / scale)), binary32 division.  [FP8-guide] §4.3. */
 void  dgo_quantize_e4m3(const float* x, int64_t n, float scale, uint8_t* q);
 

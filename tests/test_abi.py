@@ -84,6 +84,16 @@ def test_hgemm_argument_errors(L, args, expect):
     assert L.dg_hgemm(*args) == expect
 
 
+def test_gemm_amax_argument_errors(L):
+    ok = (FAKE, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_BF16)
+    assert L.dg_fp8_gemm_amax(*ok, None, None) == dg.DG_ERR_INVALID_VALUE       # no amax_d
+    assert L.dg_fp8_gemm_amax(*ok, FAKE + 2, None) == dg.DG_ERR_MISALIGNED      # amax_d
+    bad = (FAKE, FAKE, FAKE, 8, 8, 24, FAKE, FAKE, None, dg.DG_BF16)
+    assert L.dg_fp8_gemm_amax(*bad, FAKE, None) == dg.DG_ERR_MISALIGNED        # K pitch
+    e4 = (FAKE, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_E4M3)
+    assert L.dg_fp8_gemm_amax(*e4, FAKE, None) == dg.DG_ERR_INVALID_VALUE      # no scale_d
+
+
 def test_scale_and_quantise_argument_errors(L):
     assert L.dg_amax(FAKE, -1, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE
     assert L.dg_amax(FAKE, 10, None, None, None) == dg.DG_ERR_INVALID_VALUE

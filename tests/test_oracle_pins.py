@@ -368,3 +368,56 @@ def test_generator_is_deterministic_and_distributed():
     A, B = synth.make_inputs("fp8_sweep_m1")
     frac = np.mean(np.abs(np.concatenate([A.ravel(), B.ravel()])) > 6.0)
     assert 0.0003 < frac < 0.002   # the 0.1% outliers times 50
+
+
+# ------------------------------------------------------- power-of-two scale
+
+@pytest.mark.parametrize("amax,scale", [
+    (448.0, 1.0),            # exactly the top of the range
+    (449.0, 2.0),
+    (224.0, 0.5),
+    (224.0001, 1.0),
+    (1.0, 2.0 ** -8),        # 448 * 2^-9 = 0.875 < 1 <= 448 * 2^-8
+    (0.875, 2.0 ** -9),
+    (3.0e38, 2.0 ** 120),    # 448 * 2^119 ~ 2.98e38 < 3e38
+    (1e-45, 2.0 ** -149),    # clamps at the smallest binary32 power of two
+    (0.0, 1.0),
+])
+def test_pow2_scale_worked_cases(amax, scale):
+    assert oracle.scale_pow2_from_amax(amax) == np.float32(scale)
+
+
+def test_pow2_scale_properties():
+    """448 p >= amax > 224 p for every normal amax: the tensor's largest value
+    lands in (224, 448] and never saturates; division by p is exact."""
+    a = np.abs(synth.normal_f32(40, (5000,)) * np.float32(1e3)) + np.float32(1e-3)
+    for v in a[:500]:
+        p = float(oracle.scale_pow2_from_amax(v))
+        assert np.log2(p) == int(np.log2(p))
+        assert 448.0 * p >= float(v) > 224.0 * p
+    assert np.isnan(oracle.scale_pow2_from_amax(np.nan))
+    assert np.isinf(oracle.scale_pow2_from_amax(np.inf))
+    x = synth.normal_f32(41, (4096,))
+    q, s, am = oracle.quantize_tensor_pow2(x)
+    # division by a power of two is exact, so quantising x/p equals encoding x*2^-e
+    ref = oracle.e4m3_encode(x.astype(np.float64) / float(s))
+    assert np.array_equal(q, ref)
+    assert np.max(q & 0x7F) <= 0x7E
+
+
+def test_pow2_scale_accuracy_against_amax_scale():
+    """Accuracy of the chain with the power-of-two scale compared with the
+    amax/448 scale on the same inputs ([FP8-guide] §2.1 vs §3.2): both stay
+    inside the page's 10% bound; the power of two uses at most one binade
+    less of the E4M3 range, so its error is at most about twice as large."""
+    A = synth.normal_f32(42, (48, 2048))
+    B = synth.normal_f32(43, (64, 2048))
+    exact = A.astype(np.float64) @ B.astype(np.float64).T
+    errs = []
+    for qt in (oracle.quantize_tensor, oracle.quantize_tensor_pow2):
+        qa, sa, _ = qt(A)
+        qb, sb, _ = qt(B)
+        D = oracle.epilogue_scale(oracle.gemm_e4m3(qa, qb, with_abs=False), sa, sb)
+        errs.append(np.linalg.norm(D - exact) / np.linalg.norm(exact))
+    assert all(e < FACTS["quantisation_error_guide"]["wrong_above_rel"] for e in errs)
+    assert errs[1] <= 2.5 * errs[0]
