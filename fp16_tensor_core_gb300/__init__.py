@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "DG_OK", "DG_ERR_INVALID_VALUE", "DG_ERR_MISALIGNED", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_TIMEOUT", "DG_BF16", "DG_E4M3", "DG_FP16", "DgError",
-    "lib", "library_path", "dg_amax", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax",
+    "lib", "library_path", "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax",
     "dg_hgemm",
     "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
     "dg_debug_skip_first_load", "dg_status_string", "dg_version", "EXPORTED_SYMBOLS",
@@ -28,7 +28,7 @@ DG_BF16, DG_E4M3, DG_FP16 = 0, 1, 2
 
 #: Every function include/dg.h declares.
 EXPORTED_SYMBOLS = (
-    "dg_amax", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm", "dg_gemm_plan",
+    "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm", "dg_gemm_plan",
     "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
     "dg_status_string", "dg_version",
 )
@@ -66,6 +66,7 @@ def lib():
             L = ctypes.CDLL(_LIB_PATH)
             vp, i64, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
             L.dg_amax.argtypes = [vp, i64, vp, vp, vp]
+            L.dg_amax_pow2.argtypes = [vp, i64, vp, vp, vp]
             L.dg_quantize_e4m3.argtypes = [vp, i64, vp, vp, vp]
             L.dg_fp8_gemm.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, ctypes.c_int, vp]
             L.dg_fp8_gemm_amax.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, ctypes.c_int,
@@ -82,7 +83,7 @@ def lib():
             L.dg_status_string.argtypes = [ctypes.c_int]
             L.dg_status_string.restype = ctypes.c_char_p
             L.dg_version.argtypes = []
-            for name in ("dg_amax", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm",
+            for name in ("dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm",
                          "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_version"):
                 getattr(L, name).restype = st
             _lib = L
@@ -128,6 +129,12 @@ def dg_amax(x, amax_out, scale_out=None, stream=None) -> None:
     """amax_out[0] = max |x|; scale_out[0] = amax / 448 (1 if amax == 0)."""
     _check(lib().dg_amax(_ptr(x), x.numel(), _ptr(amax_out), _ptr(scale_out), _stream(stream)),
            "dg_amax")
+
+
+def dg_amax_pow2(x, amax_out, scale_out, stream=None) -> None:
+    """amax_out[0] = max |x|; scale_out[0] = smallest power of two p with 448 p >= amax."""
+    _check(lib().dg_amax_pow2(_ptr(x), x.numel(), _ptr(amax_out), _ptr(scale_out), _stream(stream)),
+           "dg_amax_pow2")
 
 
 def dg_quantize_e4m3(x, scale, q, stream=None) -> None:

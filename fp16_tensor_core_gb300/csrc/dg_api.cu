@@ -174,6 +174,21 @@ dg_status dg_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dg_status dg_amax_pow2(const float* x, int64_t n, float* amax_out, float* scale_out,
+                       dg_stream_t stream) {
+    if (n < 0 || amax_out == nullptr || scale_out == nullptr || (n > 0 && x == nullptr))
+        return DG_ERR_INVALID_VALUE;
+    if (!aligned16(x)) return DG_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(amax_out) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(scale_out) & 3u) != 0)
+        return DG_ERR_MISALIGNED;
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_amax(x, n, amax_out, scale_out, st->sm_count,
+                                 reinterpret_cast<cudaStream_t>(stream), true));
+}
+
 dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_t* q,
                            dg_stream_t stream) {
     if (n < 0 || scale == nullptr || (n > 0 && (x == nullptr || q == nullptr)))

@@ -55,7 +55,8 @@ bool take_skip_first_load();
 
 // Launchers; each returns the launch's cudaError_t.
 cudaError_t launch_amax(const float* x, int64_t n, float* amax_out,
-                        float* scale_out, int sm_count, cudaStream_t s);
+                        float* scale_out, int sm_count, cudaStream_t s,
+                        bool pow2 = false);
 cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale,
                                  uint8_t* q, int sm_count, cudaStream_t s);
 cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N,

@@ -63,6 +63,35 @@ amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_b
     }
 }
 
+// Power-of-two scale ([FP8-guide] §2.1): the smallest p = 2^e (e >= -149,
+// so p is a binary32 value) with 448 * p >= amax, compared exactly in
+// double; 1 for amax == 0, NaN for NaN, +Inf for +Inf.  Dividing by p is
+// then exact: the quantiser only shifts exponents.
+__global__ void scale_pow2_kernel(const float* __restrict__ amax, float* __restrict__ scale) {
+    pdl_wait();
+    const float a = *amax;
+    float p;
+    if (a != a) {
+        p = a;
+    } else if (a == 0.0f) {
+        p = 1.0f;
+    } else if (a > 3.4028234663852886e38f) {
+        p = a;
+    } else {
+        const int ebits = static_cast<int>((__float_as_uint(a) >> 23) & 0xFFu);
+        int e = ebits == 0 ? -149 : max(-149, ebits - 127 - 10);
+        const double ad = static_cast<double>(a);
+        // 448 * 2^e for e >= -149 is an exact double; at most a few steps.
+        for (int it = 0; it < 400; ++it) {
+            const double pe = __longlong_as_double(static_cast<long long>(e + 1023) << 52);
+            if (448.0 * pe >= ad) break;
+            ++e;
+        }
+        p = static_cast<float>(__longlong_as_double(static_cast<long long>(e + 1023) << 52));
+    }
+    *scale = p;
+}
+
 // Zeroes the running maximum before the reduction.
 __global__ void amax_init_kernel(uint32_t* __restrict__ out_bits) {
     pdl_wait();
@@ -117,7 +146,7 @@ quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict_
 }  // namespace
 
 cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
-                        int sm_count, cudaStream_t s) {
+                        int sm_count, cudaStream_t s, bool pow2) {
     uint32_t* bits = reinterpret_cast<uint32_t*>(amax_out);
     cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
     if (e != cudaSuccess) return e;
@@ -131,7 +160,7 @@ cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale
                           x, n, bits);
         if (e != cudaSuccess) return e;
     }
-    if (scale_out) e = launch_kernel(scale_kernel, dim3(1), dim3(1), 0, s,
+    if (scale_out) e = launch_kernel(pow2 ? scale_pow2_kernel : scale_kernel, dim3(1), dim3(1), 0, s,
                                      static_cast<const float*>(amax_out), scale_out);
     return e;
 }

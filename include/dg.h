@@ -71,6 +71,18 @@ typedef enum {
 dg_status dg_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
                   dg_stream_t stream);
 
+/* amax and a power-of-two scale.  [FP8-guide] §2.1: instead of amax/448
+ * itself, take a power of two just above it, so that scaling and unscaling
+ * are exponent shifts (division by the scale is exact).
+ *   amax_out   FP32[1], device: as dg_amax.
+ *   scale_out  FP32[1], device, required: the smallest power of two p
+ *              (2^-149 <= p) with 448 * p >= amax, compared exactly; 1 when
+ *              amax == 0; NaN for NaN and +Inf for +Inf inputs.
+ * The tensor's largest magnitude quantises into (224, 448]: no saturation,
+ * at most one binade of the E4M3 range unused.  Errors as dg_amax. */
+dg_status dg_amax_pow2(const float* x, int64_t n, float* amax_out,
+                       float* scale_out, dg_stream_t stream);
+
 /* E4M3 quantiser.  [FP8-guide] §4.3: fp8 = clamp(round(x / scale), -448,
  * 448), implemented as q_i = E4M3(fl32(x_i / *scale)) with an IEEE binary32
  * division and round-to-nearest-even, saturating to +-448; NaN -> 0x7F.

@@ -100,6 +100,8 @@ def test_scale_and_quantise_argument_errors(L):
     assert L.dg_amax(None, 10, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE
     assert L.dg_amax(FAKE + 4, 10, FAKE, None, None) == dg.DG_ERR_MISALIGNED
     assert L.dg_amax(FAKE, 10, FAKE + 2, None, None) == dg.DG_ERR_MISALIGNED
+    assert L.dg_amax_pow2(FAKE, 10, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE  # scale required
+    assert L.dg_amax_pow2(FAKE + 8, 10, FAKE, FAKE, None) == dg.DG_ERR_MISALIGNED
     assert L.dg_quantize_e4m3(FAKE, 10, None, FAKE, None) == dg.DG_ERR_INVALID_VALUE
     assert L.dg_quantize_e4m3(FAKE, -3, FAKE, FAKE, None) == dg.DG_ERR_INVALID_VALUE
     assert L.dg_quantize_e4m3(FAKE, 10, FAKE, FAKE + 1, None) == dg.DG_ERR_MISALIGNED
