@@ -301,7 +301,37 @@ def kernel_cases(torch, dg):
         fn = lambda i, s: dg.dg_quantize_e4m3(x, sc, q, stream=s)  # noqa: E731
         return fn, 0.0, 5 * x.numel(), "hbm", "268 MB input > L2"
 
+    def moe(grouped: bool):
+        # 16 experts, 8192 routed rows with a skewed load, N = 2048, K = 4096
+        import synth
+        G, total, Nm, Km = 16, 8192, 2048, 4096
+        sizes = synth.moe_group_sizes(7, G, total)
+        offs = torch.zeros(G + 1, dtype=torch.int32)
+        offs[1:] = torch.from_numpy(sizes.cumsum()).to(torch.int32)
+        doffs = offs.to(dev)
+        nb = ncopies(total * Km + G * Nm * Km)
+        As = [codes((total, Km), 50 + i) for i in range(nb)]
+        Bs = [codes((G * Nm, Km), 60 + i) for i in range(nb)]
+        sg = torch.ones(G, dtype=torch.float32, device=dev)
+        D = torch.empty((total, Nm), dtype=torch.bfloat16, device=dev)
+        o = offs.tolist()
+
+        def fn(i, s):
+            A, B = As[i % nb], Bs[i % nb]
+            if grouped:
+                dg.dg_fp8_gemm_grouped(A, B, D, doffs, sg, sg, None, dg.DG_BF16, stream=s,
+                                       M=total, N=Nm, K=Km, groups=G)
+            else:
+                for g in range(G):
+                    if o[g + 1] > o[g]:
+                        dg.dg_fp8_gemm(A[o[g]:o[g + 1]], B[g * Nm:(g + 1) * Nm], D[o[g]:o[g + 1]],
+                                       sg[g:g + 1], sg[g:g + 1], None, dg.DG_BF16, stream=s)
+        return fn, 2.0 * total * Nm * Km, total * Km + G * Nm * Km + total * Nm * 2, "tensor_fp8", \
+            f"{nb} rotating copies; group sizes {sizes.min()}..{sizes.max()}"
+
     return {
+        "moe_grouped_16x8192x2048x4096": lambda: moe(True),
+        "moe_per_group_calls_16x8192x2048x4096": lambda: moe(False),
         "qkv_gemv_1x12288x4096": qkv,
         "fp8_gemm_4096": lambda: fp8_sq(4096, dg.DG_BF16),
         "fp8_gemm_8192_e4m3out": lambda: fp8_sq(8192, dg.DG_E4M3),

@@ -148,6 +148,8 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             L.plan = &plan;
             L.status = st->status;
             L.amax_out = amax_bits;
+            L.group_off = nullptr;
+            L.groups = 0;
             return from_cuda(launch_gemm_tc(L, s));
         }
     }
@@ -241,6 +243,60 @@ dg_status dg_fp8_gemm_amax(const uint8_t* A, const uint8_t* B, void* D, int64_t 
                     reinterpret_cast<cudaStream_t>(stream), amax_d);
 }
 
+dg_status dg_fp8_gemm_grouped(const uint8_t* A, const uint8_t* B, void* D, int64_t M, int64_t N,
+                              int64_t K, int groups, const int32_t* group_offsets,
+                              const float* scale_a, const float* scale_b, const float* scale_d,
+                              dg_dtype out, dg_stream_t stream) {
+    dg_status rc = check_sizes(M, N, K);
+    if (rc != DG_OK) return rc;
+    if (groups < 1 || groups > kMaxGemmGroups || group_offsets == nullptr) return DG_ERR_INVALID_VALUE;
+    if (out != DG_BF16 && out != DG_E4M3 && out != DG_FP16) return DG_ERR_INVALID_VALUE;
+    if (static_cast<int64_t>(groups) * N > INT_MAX) return DG_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(group_offsets) & 3u) != 0) return DG_ERR_MISALIGNED;
+    if (M == 0 || N == 0) return DG_OK;
+    if (D == nullptr) return DG_ERR_INVALID_VALUE;
+    if (K > 0 && (A == nullptr || B == nullptr || scale_a == nullptr || scale_b == nullptr))
+        return DG_ERR_INVALID_VALUE;
+    if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0) return DG_ERR_MISALIGNED;
+    DeviceState* st = nullptr;
+    rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return from_cuda(cudaMemsetAsync(D, 0, static_cast<size_t>(M * N * elem_bytes(out)), s));
+    dg_plan plan{};
+    plan.path = 3;
+    plan.block_m = 128;
+    plan.block_n = N >= 512 ? 256 : 128;
+    plan.block_k = 128;
+    // Upper bound on tiles: each group adds at most one partial 128-row tile.
+    const int64_t num_n = (N + plan.block_n - 1) / plan.block_n;
+    const int64_t tiles = ((M + 127) / 128 + groups) * num_n;
+    if (tiles > INT_MAX) return DG_ERR_UNSUPPORTED;
+    plan.tiles = static_cast<int>(tiles);
+    plan.grid = static_cast<int>(tiles < st->sm_count ? tiles : st->sm_count);
+    TcLaunch L{};
+    L.A = A;
+    L.B = B;
+    L.D = D;
+    L.M = static_cast<int>(M);
+    L.N = static_cast<int>(N);
+    L.K = static_cast<int>(K);
+    L.fp16_in = false;
+    L.sa = scale_a;
+    L.sb = scale_b;
+    L.sd = scale_d;
+    L.out_kind = out_kind_of(out);
+    L.out_elem = elem_bytes(out);
+    L.plan = &plan;
+    L.status = st->status;
+    L.amax_out = nullptr;
+    L.group_off = group_offsets;
+    L.groups = groups;
+    return from_cuda(launch_gemm_tc_grouped(L, s));
+}
+
 dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M, int64_t N,
                    int64_t K, dg_dtype out, dg_stream_t stream) {
     dg_status rc = check_sizes(M, N, K);
@@ -289,6 +345,7 @@ dg_status dg_sync_status(dg_stream_t stream) {
     if (word != 0) {
         if (cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess) return DG_ERR_CUDA;
         if (word & kStatusTimeout) return DG_ERR_TIMEOUT;
+        if (word & kStatusBadArgument) return DG_ERR_INVALID_VALUE;
     }
     return DG_OK;
 }

@@ -80,8 +80,13 @@ struct TcLaunch {
     const dg_plan* plan;
     uint32_t* status;
     uint32_t* amax_out;   // optional running max |sa*sb*acc| (float bits)
+    const int* group_off; // grouped GEMM: device offsets [groups + 1], else null
+    int groups;
 };
 cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s);
+// Grouped variant (single-CTA tiles; L.plan->block_n is 128 or 256).
+cudaError_t launch_gemm_tc_grouped(const TcLaunch& L, cudaStream_t s);
+constexpr int kMaxGemmGroups = 1024;
 
 // Tile table for the tensor-core path (fills block_n, stages, smem, grid).
 void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,

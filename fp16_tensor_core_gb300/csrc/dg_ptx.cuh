@@ -9,7 +9,7 @@
 namespace dg {
 
 // Device status bits (the library's per-device status word).
-enum : uint32_t { kStatusTimeout = 1u };
+enum : uint32_t { kStatusTimeout = 1u, kStatusBadArgument = 2u };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

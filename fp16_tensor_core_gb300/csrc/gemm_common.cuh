@@ -29,7 +29,13 @@ struct Params {
     int skip_first_load;
     int group_m;   // tiles are rastered in groups of group_m M-tiles sweeping N
     uint32_t* amax_out;  // optional: running max |sa*sb*acc| as float bits
+    // Grouped GEMM: group g covers rows [group_off[g], group_off[g+1]) of A
+    // and D and rows [g*N, g*N + N) of B; sa/sb/sd hold one scale per group.
+    const int* group_off;
+    int groups;
 };
+
+constexpr int kMaxGroups = 1024;
 
 // CTA-pair kernel (k_gemm_tc2.cu): shared memory and stage count of the
 // 256 x bn pair tile, and its launcher.
@@ -71,9 +77,9 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 // Scale, convert and store 32 consecutive accumulator columns of one row.
 // Returns max |acc| over the stored elements as ordered bits (the bit
 // pattern of a non-negative float; NaN above every number), 0 if none.
-__device__ __forceinline__ uint32_t store_chunk(const Params& p, int row, int col0,
+__device__ __forceinline__ uint32_t store_chunk(const Params& p, int row, int row_end, int col0,
                                                 const uint32_t (&r)[32], float alpha) {
-    if (row >= p.M) return 0u;
+    if (row >= row_end) return 0u;
     const int ncols = min(32, p.N - col0);
     if (ncols <= 0) return 0u;
     uint32_t amax_bits = 0u;

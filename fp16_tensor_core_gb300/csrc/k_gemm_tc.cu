@@ -44,13 +44,17 @@ namespace {
 
 constexpr int kBM = 128;
 
+// Shared memory for the grouped variant's per-group tile prefix.
+constexpr int kGroupSmem = 4 * (kMaxGroups + 1) + 12;
+
 // Stage count = what fits in 227 KB, at most 8.
-constexpr int stages_for(int bn) {
-    const int st = (kSmemLimit - 1024 - 256) / (kBM * kBKBytes + bn * kBKBytes);
+constexpr int stages_for(int bn, bool grouped = false) {
+    const int st = (kSmemLimit - 1024 - 256 - (grouped ? kGroupSmem : 0)) /
+                   (kBM * kBKBytes + bn * kBKBytes);
     return st > 8 ? 8 : st;
 }
 
-template <int BN, int STAGES, bool kFp16In>
+template <int BN, int STAGES, bool kFp16In, bool kGrouped = false>
 struct Cfg {
     static constexpr int kBK = kFp16In ? 64 : 128;        // K elements per stage
     static constexpr int kABytes = kBM * kBKBytes;        // 16 KB
@@ -58,7 +62,8 @@ struct Cfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // two accumulators
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes;
+    static constexpr int kSmemBytes =
+        1024 + STAGES * kStageBytes + kBarBytes + (kGrouped ? kGroupSmem : 0);
     static constexpr uint32_t kIdesc = idesc_f32acc(kBM, BN, 0, 0);
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256,
                   "BN: MMA N (multiple of 16, <= 256) and 32-column epilogue chunks");
@@ -67,11 +72,17 @@ struct Cfg {
     static_assert(kBBytes % 1024 == 0, "1024-byte aligned B stages (128-byte swizzle atoms)");
 };
 
-template <int BN, int STAGES, bool kFp16In>
+// Output tile t of this launch: A rows from a_row, B rows from b_row,
+// output rows [a_row, row_end) and columns from col0.
+struct Tile {
+    int a_row, b_row, row_end, col0, g;
+};
+
+template <int BN, int STAGES, bool kFp16In, bool kGrouped = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
-    using C = Cfg<BN, STAGES, kFp16In>;
+    using C = Cfg<BN, STAGES, kFp16In, kGrouped>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -84,6 +95,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint64_t* drain = acc_empty + 2;       // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    // grouped only: tile_start[g] = first tile of group g (G + 1 entries)
+    int* tile_start = reinterpret_cast<int*>(smem + STAGES * C::kStageBytes + C::kBarBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -117,8 +130,67 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     const int num_m = (p.M + kBM - 1) / kBM;
     const int num_n = (p.N + BN - 1) / BN;
-    const int num_tiles = num_m * num_n;
+    int num_tiles = num_m * num_n;
     const int num_kb = (p.K + C::kBK - 1) / C::kBK;
+    if constexpr (kGrouped) {
+        // Tiles of group g: ceil(M_g / 128) x num_n, numbered group by group.
+        // The offsets are validated here; invalid ones store nothing.
+        if (warp == 3) {
+            const int G = p.groups;
+            bool valid = p.group_off[0] == 0 && p.group_off[G] == p.M;
+            int base = 0;
+            for (int g0 = 0; g0 < G; g0 += 32) {
+                const int g = g0 + lane;
+                int n_tiles = 0;
+                if (g < G) {
+                    const int m_g = p.group_off[g + 1] - p.group_off[g];
+                    if (m_g < 0) valid = false;
+                    n_tiles = (max(m_g, 0) + kBM - 1) / kBM * num_n;
+                }
+                int incl = n_tiles;   // inclusive warp scan
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                if (g < G) tile_start[g] = base + incl - n_tiles;
+                base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            }
+            valid = __all_sync(0xFFFFFFFFu, valid);
+            if (lane == 0) {
+                tile_start[G] = valid ? base : 0;
+                if (!valid) atomicOr(p.status, kStatusBadArgument);
+            }
+            if (!valid)
+                for (int g = lane; g < G; g += 32) tile_start[g] = 0;
+        }
+        __syncthreads();
+        num_tiles = tile_start[p.groups];
+    }
+    // Tile coordinates for tile t (cursor g only moves forward: every role
+    // visits its tiles in increasing t).
+    auto tile_of = [&](int t, int& g) -> Tile {
+        Tile T;
+        if constexpr (kGrouped) {
+            while (t >= tile_start[g + 1]) ++g;
+            const int local = t - tile_start[g];
+            const int mt = local / num_n, nt = local - mt * num_n;
+            T.a_row = p.group_off[g] + mt * kBM;
+            T.row_end = p.group_off[g + 1];
+            T.b_row = g * p.N + nt * BN;
+            T.col0 = nt * BN;
+            T.g = g;
+        } else {
+            int mt, nt;
+            tile_coords(t, num_m, num_n, p.group_m, mt, nt);
+            T.a_row = mt * kBM;
+            T.row_end = p.M;
+            T.b_row = nt * BN;
+            T.col0 = nt * BN;
+            T.g = 0;
+        }
+        return T;
+    };
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
@@ -128,17 +200,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         uint32_t issued_phase = 0;         // parity of each stage's last load
         bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
         bool ok = true;
+        int gcur = 0;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            int mt, nt;
-            tile_coords(t, num_m, num_n, p.group_m, mt, nt);
+            const Tile T = tile_of(t, gcur);
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
                 if (skip) {
                     skip = false;           // leave this stage unloaded
                 } else {
                     mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-                    tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kb * C::kBK, mt * kBM);
-                    tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kb * C::kBK, nt * BN);
+                    tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kb * C::kBK, T.a_row);
+                    tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kb * C::kBK, T.b_row);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 }
@@ -196,21 +268,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;              // TMEM lane quarter of this warp
-        float alpha = 1.0f;
-        if (p.sa != nullptr) alpha = (*p.sa) * (*p.sb);
-        if (p.out_kind == kOutE4M3) alpha = __fdiv_rn(alpha, *p.sd);
+        auto alpha_of = [&](int g) {
+            float a = 1.0f;
+            if (p.sa != nullptr) a = p.sa[g] * p.sb[g];
+            if (p.out_kind == kOutE4M3) a = __fdiv_rn(a, p.sd[g]);
+            return a;
+        };
+        float alpha = alpha_of(0);
+        int alpha_g = 0;
         uint32_t amax_bits = 0u;
         int acc = 0;
         uint32_t acc_phase = 0;
+        int gcur = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            int mt, nt;
-            tile_coords(t, num_m, num_n, p.group_m, mt, nt);
+            const Tile T = tile_of(t, gcur);
+            if (T.g != alpha_g) {
+                alpha = alpha_of(T.g);
+                alpha_g = T.g;
+            }
             // Every lane waits; the vote reconverges the warp (tcgen05.ld is
             // .sync.aligned) and makes the whole warp leave together.
             const bool got = wait_bounded(&acc_full[acc], acc_phase, ctl);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
             tc_fence_after_sync();
-            const int row = mt * kBM + q * 32 + lane;
+            const int row = T.a_row + q * 32 + lane;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -219,7 +300,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 tmem_load_32cols(tbase + c * 32, r);
                 tmem_load_wait(r);
-                amax_bits = max(amax_bits, store_chunk(p, row, nt * BN + c * 32, r, alpha));
+                amax_bits = max(amax_bits, store_chunk(p, row, T.row_end, T.col0 + c * 32, r, alpha));
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -238,9 +319,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
 // ------------------------------------------------------------- host side
 
-template <int BN, int STAGES, bool kFp16In>
+template <int BN, int STAGES, bool kFp16In, bool kGrouped = false>
 cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
-    using C = Cfg<BN, STAGES, kFp16In>;
+    using C = Cfg<BN, STAGES, kFp16In, kGrouped>;
     static std::mutex mu;
     static bool attr_done[64] = {};
     int dev = 0;
@@ -250,17 +331,18 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
         std::lock_guard<std::mutex> lk(mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!attr_done[dev]) {
-            e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, kFp16In>,
+            e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
             if (e != cudaSuccess) return e;
             attr_done[dev] = true;
         }
     }
     CUtensorMap ta, tb;
-    if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kBM) || !make_map(&tb, L.B, L.N, L.K, kFp16In, BN))
+    const int b_rows = kGrouped ? L.N * L.groups : L.N;   // grouped: B is (G*N) x K
+    if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kBM) || !make_map(&tb, L.B, b_rows, L.K, kFp16In, BN))
         return cudaErrorInvalidValue;
-    return launch_kernel(gemm_tc_kernel<BN, STAGES, kFp16In>, dim3(L.plan->grid), dim3(kThreads),
-                         C::kSmemBytes, s, ta, tb, prm);
+    return launch_kernel(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped>, dim3(L.plan->grid),
+                         dim3(kThreads), C::kSmemBytes, s, ta, tb, prm);
 }
 
 template <bool kFp16In>
@@ -366,7 +448,7 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     (void)K;
 }
 
-cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s) {
+Params make_params(const TcLaunch& L) {
     Params prm;
     prm.D = L.D;
     prm.M = L.M;
@@ -391,8 +473,23 @@ cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s) {
         const int v = std::atoi(g);
         if (v >= 1 && v <= 4096) prm.group_m = v;
     }
+    prm.group_off = L.group_off;
+    prm.groups = L.groups;
+    return prm;
+}
+
+cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s) {
+    const Params prm = make_params(L);
     if (L.plan->block_m == 256) return launch_gemm_tc_pair(L, prm, s);
     return L.fp16_in ? launch_in<true>(L, prm, s) : launch_in<false>(L, prm, s);
+}
+
+cudaError_t launch_gemm_tc_grouped(const TcLaunch& L, cudaStream_t s) {
+    if (L.fp16_in || L.groups < 1 || L.groups > kMaxGroups) return cudaErrorInvalidValue;
+    const Params prm = make_params(L);
+    if (L.plan->block_n == 128)
+        return launch_cfg<128, stages_for(128, true), false, true>(L, prm, s);
+    return launch_cfg<256, stages_for(256, true), false, true>(L, prm, s);
 }
 
 }  // namespace dg

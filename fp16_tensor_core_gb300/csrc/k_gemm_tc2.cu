@@ -225,7 +225,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 tmem_load_32cols(tbase + c * 32, r);
                 tmem_load_wait(r);
-                amax_bits = max(amax_bits, store_chunk(p, row, nt * BN + c * 32, r, alpha));
+                amax_bits = max(amax_bits, store_chunk(p, row, p.M, nt * BN + c * 32, r, alpha));
             }
             tc_fence_before_sync();
             __syncwarp();

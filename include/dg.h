@@ -135,6 +135,34 @@ dg_status dg_fp8_gemm_amax(const uint8_t* A, const uint8_t* B, void* D,
                            const float* scale_d, dg_dtype out, float* amax_d,
                            dg_stream_t stream);
 
+/* Grouped per-tensor-scaled E4M3 GEMM: a batch of GEMMs that share N and K
+ * (the expert projections of a mixture-of-experts layer) in one launch.
+ * [DG-FP16] §1 (an MoE forward pass as the workload) and [FP8-guide] §4.4
+ * (merge many small GEMMs into one launch).  Group g, 0 <= g < groups,
+ * computes rows [off[g], off[g+1]) of D:
+ *   D[m,n] = out( scale_a[g] * scale_b[g] * sum_k A[m,k] * B[g*N + n, k] )
+ * (divided by scale_d[g] before the rounding when out == DG_E4M3).
+ *   A      M x K E4M3 codes, the groups' rows stacked, device.
+ *   B      (groups * N) x K E4M3 codes: group g's N x K matrix at rows g*N.
+ *   D      M x N of `out`, device.
+ *   group_offsets  int32[groups + 1], device, 4-byte aligned:
+ *          0 = off[0] <= off[1] <= ... <= off[groups] = M.  Read by the
+ *          kernel (no host round trip, no padding of group sizes; empty
+ *          groups allowed).  Offsets that break these rules make the kernel
+ *          store nothing and dg_sync_status report DG_ERR_INVALID_VALUE.
+ *   scale_a, scale_b  FP32[groups], device; scale_d FP32[groups], device,
+ *          required iff out == DG_E4M3.
+ *   groups 1 .. 1024.
+ * Layout, alignment and other errors as dg_fp8_gemm.  The tiles are 128 x
+ * BN per group (one tensor-core kernel, tiles of all groups scheduled over
+ * all SMs). */
+dg_status dg_fp8_gemm_grouped(const uint8_t* A, const uint8_t* B, void* D,
+                              int64_t M, int64_t N, int64_t K, int groups,
+                              const int32_t* group_offsets,
+                              const float* scale_a, const float* scale_b,
+                              const float* scale_d, dg_dtype out,
+                              dg_stream_t stream);
+
 /* FP16 GEMM (HGEMM), FP32 accumulation, no scaling.  [HGEMM-L2] §1.3 (FP16
  * inputs, FP32 accumulator) and §3; same layouts and edge rules as
  * dg_fp8_gemm.  A, B hold IEEE binary16 bit patterns.  K must be a multiple

@@ -154,3 +154,30 @@ def make_inputs(name: str, M: int | None = None, N: int | None = None,
         z[hit] *= 50.0
     x = z.astype(np.float32)
     return x[:na].reshape(M, K).copy(), x[na:].reshape(N, K).copy()
+
+
+def moe_group_sizes(seed: int, groups: int, total: int, empty: int = 0) -> np.ndarray:
+    """Skewed expert loads summing to `total` (a mixture-of-experts routing
+    mix): weights u^3 + 0.02 from the counter stream, floor-rounded, the
+    remainder spread one row at a time over the largest groups; the first
+    `empty` groups get no rows."""
+    u = uniform(seed, 0, groups)
+    w = u * u * u + 0.02
+    w[:empty] = 0.0
+    sizes = np.floor(total * w / w.sum()).astype(np.int64)
+    rest = total - int(sizes.sum())
+    order = np.argsort(-w, kind="stable")
+    for i in range(rest):
+        sizes[order[i % (groups - empty)]] += 1
+    return sizes
+
+
+def make_moe_inputs(groups: int, total: int, N: int, K: int, seed: int = 0, empty: int = 0):
+    """FP32 A (total x K, groups' rows stacked), FP32 B (groups*N x K) and
+    int32 offsets [groups + 1]; A and B ~ N(0, 1) from stream `seed`, A first."""
+    sizes = moe_group_sizes(seed + 7, groups, total, empty)
+    offs = np.zeros(groups + 1, dtype=np.int32)
+    offs[1:] = np.cumsum(sizes)
+    z = normal(seed, total * K + groups * N * K).astype(np.float32)
+    return (z[:total * K].reshape(total, K).copy(), z[total * K:].reshape(groups * N, K).copy(),
+            offs)

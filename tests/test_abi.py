@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import fp16_tensor_core_gb300 as dg
@@ -92,6 +93,34 @@ def test_gemm_amax_argument_errors(L):
     assert L.dg_fp8_gemm_amax(*bad, FAKE, None) == dg.DG_ERR_MISALIGNED        # K pitch
     e4 = (FAKE, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_E4M3)
     assert L.dg_fp8_gemm_amax(*e4, FAKE, None) == dg.DG_ERR_INVALID_VALUE      # no scale_d
+
+
+def test_grouped_argument_errors(L):
+    base = dict(A=FAKE, B=FAKE, D=FAKE, M=64, N=32, K=16, G=4, off=FAKE, sa=FAKE, sb=FAKE, sd=None,
+                out=dg.DG_BF16)
+
+    def call(**kw):
+        a = dict(base, **kw)
+        return L.dg_fp8_gemm_grouped(a["A"], a["B"], a["D"], a["M"], a["N"], a["K"], a["G"],
+                                     a["off"], a["sa"], a["sb"], a["sd"], a["out"], None)
+    assert call(G=0) == dg.DG_ERR_INVALID_VALUE
+    assert call(G=1025) == dg.DG_ERR_INVALID_VALUE
+    assert call(off=None) == dg.DG_ERR_INVALID_VALUE
+    assert call(off=FAKE + 2) == dg.DG_ERR_MISALIGNED
+    assert call(sa=None) == dg.DG_ERR_INVALID_VALUE
+    assert call(out=dg.DG_E4M3) == dg.DG_ERR_INVALID_VALUE      # scale_d missing
+    assert call(K=24) == dg.DG_ERR_MISALIGNED
+    assert call(M=-1) == dg.DG_ERR_INVALID_VALUE
+    assert call(N=1 << 30, G=8) == dg.DG_ERR_INVALID_VALUE      # groups * N overflows
+
+
+def test_moe_group_sizes_recipe():
+    import synth
+    s = synth.moe_group_sizes(3, 16, 8192, empty=2)
+    assert s.sum() == 8192 and (s[:2] == 0).all() and (s[2:] > 0).all()
+    assert s.max() > 4 * max(1, int(np.median(s[2:])))   # skewed load
+    A, B, off = synth.make_moe_inputs(4, 300, 32, 64, empty=1)
+    assert A.shape == (300, 64) and B.shape == (128, 64) and off[0] == 0 and off[-1] == 300
 
 
 def test_scale_and_quantise_argument_errors(L):
