@@ -184,3 +184,18 @@ def test_product_package_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "dg_oracle" not in src, f
+
+
+def test_plain_c_client_builds_and_runs(L, tmp_path):
+    """include/dg.h is valid C and libdg.so links and answers from C."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    exe = tmp_path / "abi_smoke"
+    lib_dir = os.path.dirname(dg.library_path())
+    src = os.path.join(ROOT, "tests", "c_abi", "abi_smoke.c")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    src, "-o", str(exe), "-L", lib_dir, "-ldg", f"-Wl,-rpath,{lib_dir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and "c abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
