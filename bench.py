@@ -38,8 +38,9 @@ FLOP_PER_STEP = 2.0 * M * N * K
 WORKLOAD = "fp8_8192_e4m3out"
 CPU_SAMPLE_ROWS = 3072  # ~10-20 s of oracle work on 16 cores
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+# Sources of the kernel the headline step runs (CTA-pair tensor-core GEMM).
 GEMM_SOURCES = [os.path.join(ROOT, "fp16_tensor_core_gb300", "csrc", f)
-                for f in ("k_gemm_tc.cu", "dg_ptx.cuh")]
+                for f in ("k_gemm_tc2.cu", "gemm_common.cuh", "dg_ptx.cuh")]
 
 
 # ---------------------------------------------------------------- plumbing
@@ -461,6 +462,28 @@ def run_own(args):
     ms_step = ms_total / args.steps
     value = world * FLOP_PER_STEP / (ms_step * 1e-3) / 1e12
 
+    # The same step captured once into a CUDA graph, K replays timed.
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        wl.step(torch.cuda.current_stream())
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    g_s, g_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g_s.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g_e.record(stream)
+    g_e.synchronize()
+    graph_ms = reduce_max(g_s.elapsed_time(g_e), world, device=f"cuda:{local}") / args.steps
+    del graph
+    st = dg.dg_sync_status()
+    assert st == dg.DG_OK, dg.dg_status_string(st)
+
     # End to end: every step copies its FP32 inputs in from pinned host
     # memory and its E4M3 result back out.  Two device buffer sets let the
     # host->device copy of step i+1 and the device->host copy of step i-1
@@ -533,6 +556,7 @@ def run_own(args):
             "inputs": "FP32 A, B ~ N(0,1) seed 0, resident in HBM; sD from tests/golden/sd_8192.json",
             "l2": "inputs larger than L2 (2 x 268 MB FP32 per step), no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "launch": "9 stream launches per step (graph_replay: the same step as one CUDA-graph replay)",
         },
         "roofline": {
             "bound": "tensor",
@@ -552,6 +576,8 @@ def run_own(args):
                         "copies of neighbouring steps overlap the kernels (double-buffered)",
                 "h2d_bytes_per_step": A32.nbytes + B32.nbytes,
                 "d2h_bytes_per_step": M * N},
+        "graph_replay": {"value": world * FLOP_PER_STEP / (graph_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                         "ms_per_step": graph_ms},
         "gpu_launches": Workload.KERNELS_PER_STEP * args.steps,
         "clocks": clk,
     }
