@@ -268,6 +268,16 @@ def kernel_cases(torch, dg):
                                          dg.DG_BF16, stream=s)
         return fn, 2.0 * Mq * Nq * Kq, Nq * Kq + Mq * Kq + Mq * Nq * 2, "hbm", f"{nb} rotating copies"
 
+    def gemv_m(m):
+        Nq, Kq = 12288, 4096
+        nb = ncopies(Nq * Kq)
+        As = [codes((m, Kq), 70 + i) for i in range(nb)]
+        Bs = [codes((Nq, Kq), 80 + i) for i in range(nb)]
+        D = torch.empty((m, Nq), dtype=torch.bfloat16, device=dev)
+        fn = lambda i, s: dg.dg_fp8_gemm(As[i % nb], Bs[i % nb], D, one, one, None,  # noqa: E731
+                                         dg.DG_BF16, stream=s)
+        return fn, 2.0 * m * Nq * Kq, Nq * Kq + m * Kq + m * Nq * 2, "hbm", f"{nb} rotating copies"
+
     def fp8_sq(S, out):
         nb = ncopies(2 * S * S)
         As = [codes((S, S), 30 + i) for i in range(nb)]
@@ -334,6 +344,9 @@ def kernel_cases(torch, dg):
         "moe_grouped_16x8192x2048x4096": lambda: moe(True),
         "moe_per_group_calls_16x8192x2048x4096": lambda: moe(False),
         "qkv_gemv_1x12288x4096": qkv,
+        "qkv_m4_4x12288x4096": lambda: gemv_m(4),
+        "qkv_m8_8x12288x4096": lambda: gemv_m(8),
+        "qkv_m16_16x12288x4096": lambda: gemv_m(16),
         "fp8_gemm_4096": lambda: fp8_sq(4096, dg.DG_BF16),
         "fp8_gemm_8192_e4m3out": lambda: fp8_sq(8192, dg.DG_E4M3),
         "fp16_hgemm_4096": lambda: hgemm(4096),

@@ -99,6 +99,8 @@ def _ptr(t):
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError("tensor must be in CUDA device memory")
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
     return t.data_ptr()

@@ -83,7 +83,16 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
         p->path = 1;
         return DG_OK;
     }
-    if (M <= 16) {
+    // GEMV for M <= 2, tensor cores above.  Measured on GB300 for N = 12288,
+    // K = 4096 (B read from HBM): GEMV 11.2 / 21.7 / 37.4 / 74.0 us at
+    // M = 1 / 4 / 8 / 16 (its FMA count grows with M) against a flat ~17 us
+    // for the tensor-core kernel.  DG_GEMV_MAX_M (0..16) moves the crossover.
+    int gemv_max_m = 2;
+    if (const char* v = std::getenv("DG_GEMV_MAX_M")) {
+        const int x = std::atoi(v);
+        if (x >= 0 && x <= 16) gemv_max_m = x;
+    }
+    if (M <= gemv_max_m) {
         p->path = 2;
         const int rows = M <= 4 ? 16 : 8;   // 8 warps x (2 or 1) rows of B
         p->grid = static_cast<int>((N + rows - 1) / rows);

@@ -105,9 +105,9 @@ dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale,
  *   scale_d  FP32[1], device; required iff out == DG_E4M3, else ignored.
  *   M, N, K  >= 0 and < 2^31.  M == 0 or N == 0 is a no-op; K == 0 writes
  *            zeros.  K must be a multiple of 16 (row pitch alignment).
- * M <= 16 runs a bandwidth-bound split-K GEMV ([DG-FP16] §2.1 and §4.1,
- * the decode QKV projection); larger M runs the tensor-core kernel with a
- * tile chosen per shape (dg_gemm_plan).  K tails are zero-filled by the
+ * M <= 2 runs a bandwidth-bound GEMV with the K sum split across a warp
+ * ([DG-FP16] §2.1 and §4.1, the decode QKV projection); larger M runs the
+ * tensor-core kernel with a tile chosen per shape (dg_gemm_plan).  K tails are zero-filled by the
  * tensor-memory loads and M/N edges are predicated stores ([FP8-guide] §3.3).
  */
 dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M,

@@ -141,10 +141,19 @@ def test_plan_paths_and_tiles(L):
     assert dg.dg_gemm_plan(0, 10, 16, sm_count=sm)["path"] == 0
     assert dg.dg_gemm_plan(10, 0, 16, sm_count=sm)["path"] == 0
     assert dg.dg_gemm_plan(10, 10, 0, sm_count=sm)["path"] == 1
-    for m, rows in ((1, 16), (4, 16), (5, 8), (16, 8)):
+    for m in (1, 2):
         p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
-        assert p["path"] == 2 and p["block_n"] == rows and p["grid"] == 12288 // rows
-    for m in (17, 63, 65, 129, 256, 4096, 8192):
+        assert p["path"] == 2 and p["block_n"] == 16 and p["grid"] == 12288 // 16
+    for m in (3, 16):
+        assert dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)["path"] == 3
+    os.environ["DG_GEMV_MAX_M"] = "16"
+    try:
+        for m, rows in ((4, 16), (5, 8), (16, 8)):
+            p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
+            assert p["path"] == 2 and p["block_n"] == rows and p["grid"] == 12288 // rows
+    finally:
+        del os.environ["DG_GEMV_MAX_M"]
+    for m in (3, 17, 63, 65, 129, 256, 4096, 8192):
         p = dg.dg_gemm_plan(m, 1000, 1040, sm_count=sm)
         assert p["path"] == 3
         assert p["block_n"] in (64, 128, 160, 192, 224, 256)

@@ -302,3 +302,18 @@ def test_bounded_wait_reports_timeout_and_context_survives():
         dg.dg_set_wait_timeout_us(2_000_000)
         dg.dg_debug_skip_first_load(False)
     fp8_chain(A, B)
+
+
+@pytest.mark.parametrize("M,N,K", [(4, 1000, 1040), (7, 513, 512), (16, 513, 4096), (3, 300, 272)])
+def test_gemv_for_larger_m_when_forced(M, N, K):
+    """The GEMV handles M up to 16 (its 2-, 4-, 8- and 16-row instantiations),
+    although the planner only sends M <= 2 to it by default."""
+    os.environ["DG_GEMV_MAX_M"] = "16"
+    try:
+        assert dg.dg_gemm_plan(M, N, K)["path"] == 2
+        A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+        fp8_chain(A, B)
+        A16, B16 = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
+        hgemm_case(A16, B16)
+    finally:
+        del os.environ["DG_GEMV_MAX_M"]
