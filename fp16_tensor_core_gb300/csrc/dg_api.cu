@@ -5,6 +5,7 @@
 #include <atomic>
 #include <climits>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <mutex>
 
@@ -72,6 +73,25 @@ dg_status current_device_state(DeviceState** out) {
 
 namespace {
 
+// DG_LOG=1: one line per GEMM call on stderr with the chosen path and tile.
+bool log_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("DG_LOG");
+        return v != nullptr && v[0] != '\0' && v[0] != '0';
+    }();
+    return on;
+}
+
+void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& p) {
+    if (!log_enabled()) return;
+    static const char* const kPath[4] = {"no-op", "zero-fill", "gemv", "tensor-core"};
+    std::fprintf(stderr,
+                 "dg: %s M=%lld N=%lld K=%lld path=%s tile=%dx%d stages=%d tiles=%d grid=%d\n",
+                 what, static_cast<long long>(M), static_cast<long long>(N),
+                 static_cast<long long>(K), kPath[p.path & 3], p.block_m, p.block_n, p.stages,
+                 p.tiles, p.grid);
+}
+
 // Shared path selection for dg_gemm_plan and the GEMM entry points.
 dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p) {
     *p = dg_plan{};
@@ -124,6 +144,7 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
     dg_plan plan;
     rc = make_plan(M, N, K, fp16_in, st->sm_count, &plan);
     if (rc != DG_OK) return rc;
+    log_plan(fp16_in ? "hgemm" : "fp8_gemm", M, N, K, plan);
     const int ok = out_kind_of(out);
     uint32_t* amax_bits = reinterpret_cast<uint32_t*>(amax_d);
     if (amax_bits != nullptr) {
@@ -285,6 +306,7 @@ dg_status dg_fp8_gemm_grouped(const uint8_t* A, const uint8_t* B, void* D, int64
     if (tiles > INT_MAX) return DG_ERR_UNSUPPORTED;
     plan.tiles = static_cast<int>(tiles);
     plan.grid = static_cast<int>(tiles < st->sm_count ? tiles : st->sm_count);
+    log_plan("fp8_gemm_grouped", M, N, K, plan);
     TcLaunch L{};
     L.A = A;
     L.B = B;
