@@ -1,5 +1,6 @@
-// k_gemv.cu -- the M <= 16 path: a bandwidth-bound GEMV with the K sum split
-// across the 32 lanes of a warp.
+// k_gemv.cu -- the small-M path (any M <= 16; the planner sends M <= 2
+// here): a bandwidth-bound GEMV with the K sum split across the 32 lanes of
+// a warp.
 //
 // Page shorthands: [DG-FP16] = the DeepGEMM FP16/WMMA deep-dive page;
 // [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南".

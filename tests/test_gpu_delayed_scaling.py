@@ -2,8 +2,9 @@
 that value, over 448, serves as the next call's E4M3 output scale (delayed
 scaling; [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南" §3.2).
 
-Checked against the oracle's max |Dref| on every kernel path: GEMV (M <= 16),
-single CTA, CTA pairs, and FP8 / BF16 outputs.
+Checked against the oracle's max |Dref| on every kernel path: GEMV (M <= 2 by
+default, M = 7 with the crossover raised), single CTA, CTA pairs, and FP8 /
+BF16 outputs.
 """
 import os
 
@@ -37,17 +38,21 @@ def _amax_bound(R, S, sa, sb):
     return ref, tol
 
 
-@pytest.mark.parametrize("M,N,K,pairs", [
-    (1, 1000, 1040, "0"),      # GEMV
-    (7, 300, 512, "0"),        # GEMV, several rows
-    (65, 1000, 1040, "0"),     # single CTA
-    (129, 777, 272, "0"),      # single CTA, ragged
-    (300, 777, 272, "1"),      # CTA pairs, odd CTA partly out of range
-    (640, 1536, 2048, "1"),    # CTA pairs, several tiles per pair
+@pytest.mark.parametrize("M,N,K,pairs,path", [
+    (1, 1000, 1040, "0", 2),      # GEMV
+    (7, 300, 512, "0", 2),        # GEMV, several rows (crossover raised to 16)
+    (7, 300, 512, "0", 3),        # the same shape on the tensor-core kernel
+    (65, 1000, 1040, "0", 3),     # single CTA
+    (129, 777, 272, "0", 3),      # single CTA, ragged
+    (300, 777, 272, "1", 3),      # CTA pairs, odd CTA partly out of range
+    (640, 1536, 2048, "1", 3),    # CTA pairs, several tiles per pair
 ])
-def test_output_amax_matches_oracle(M, N, K, pairs):
+def test_output_amax_matches_oracle(M, N, K, pairs, path):
     os.environ["DG_2CTA"] = pairs
+    if path == 2:
+        os.environ["DG_GEMV_MAX_M"] = "16"
     try:
+        assert dg.dg_gemm_plan(M, N, K, dg.DG_E4M3, dg.DG_BF16)["path"] == path
         A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
         qa, _, sa = gpu_quantize(A)
         qb, _, sb = gpu_quantize(B)
@@ -66,6 +71,7 @@ def test_output_amax_matches_oracle(M, N, K, pairs):
         check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16)), R, S, sa_ref, sb_ref)
     finally:
         os.environ.pop("DG_2CTA", None)
+        os.environ.pop("DG_GEMV_MAX_M", None)
 
 
 def test_delayed_scaling_round_trip():
