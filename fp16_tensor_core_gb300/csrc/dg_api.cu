@@ -64,6 +64,23 @@ dg_status current_device_state(DeviceState** out) {
             return DG_ERR_CUDA;
         }
         st.status = static_cast<uint32_t*>(p);
+        // Split-K workspace (fixed size, so that nothing is allocated later,
+        // e.g. while a stream is being captured into a graph).
+        const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(st.sm_count) *
+                                  kSkinnyMaxM * kSkinnyTileRows;
+        const size_t count_bytes = sizeof(uint32_t) * kSkinnyMaxTiles;
+        void* w = nullptr;
+        if (cudaMalloc(&w, part_bytes + count_bytes) != cudaSuccess) {
+            cudaFree(p);
+            return DG_ERR_CUDA;
+        }
+        if (cudaMemset(w, 0, part_bytes + count_bytes) != cudaSuccess) {
+            cudaFree(w);
+            cudaFree(p);
+            return DG_ERR_CUDA;
+        }
+        st.splitk_partials = static_cast<float*>(w);
+        st.splitk_counts = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(w) + part_bytes);
         g_dev[dev] = st;
         g_dev_ready[dev] = true;
     }
@@ -84,12 +101,13 @@ bool log_enabled() {
 
 void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& p) {
     if (!log_enabled()) return;
-    static const char* const kPath[4] = {"no-op", "zero-fill", "gemv", "tensor-core"};
+    static const char* const kPath[5] = {"no-op", "zero-fill", "gemv", "tensor-core",
+                                         "split-k"};
     std::fprintf(stderr,
                  "dg: %s M=%lld N=%lld K=%lld path=%s tile=%dx%d stages=%d tiles=%d grid=%d\n",
                  what, static_cast<long long>(M), static_cast<long long>(N),
-                 static_cast<long long>(K), kPath[p.path & 3], p.block_m, p.block_n, p.stages,
-                 p.tiles, p.grid);
+                 static_cast<long long>(K), kPath[p.path >= 0 && p.path <= 4 ? p.path : 0],
+                 p.block_m, p.block_n, p.stages, p.tiles, p.grid);
 }
 
 // Shared path selection for dg_gemm_plan and the GEMM entry points.
@@ -103,10 +121,11 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
         p->path = 1;
         return DG_OK;
     }
-    // GEMV for M <= 2, tensor cores above.  Measured on GB300 for N = 12288,
-    // K = 4096 (B read from HBM): GEMV 11.2 / 21.7 / 37.4 / 74.0 us at
-    // M = 1 / 4 / 8 / 16 (its FMA count grows with M) against a flat ~17 us
-    // for the tensor-core kernel.  DG_GEMV_MAX_M (0..16) moves the crossover.
+    // GEMV for M <= 2, split-K tensor cores up to M = 16.  Measured on GB300
+    // for N = 12288 (B read from HBM, graph-replayed launches): at K = 4096
+    // the GEMV takes 10.2 us at M = 1 and grows with M (its FMA count), the
+    // split-K kernel a flat 11.3-11.7 us for M = 1..16; at K = 1024 4.4
+    // against 6.9 us.  DG_GEMV_MAX_M (0..16) moves the crossover.
     int gemv_max_m = 2;
     if (const char* v = std::getenv("DG_GEMV_MAX_M")) {
         const int x = std::atoi(v);
@@ -120,6 +139,16 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
         p->block_n = rows;
         p->block_k = fp16_in ? 8 * 32 : 16 * 32;
         p->stages = 1;
+        return DG_OK;
+    }
+    // Split-K with swapped operands for the remaining skinny shapes (every
+    // SM streams an equal share of B; DG_SPLITK=0 turns it off).
+    const char* sk = std::getenv("DG_SPLITK");
+    const bool splitk_off = sk != nullptr && sk[0] == '0';
+    if (!splitk_off && M <= kSkinnyMaxM &&
+        (N + kSkinnyTileRows - 1) / kSkinnyTileRows <= kSkinnyMaxTiles) {
+        p->path = 4;
+        plan_skinny(M, N, K, fp16_in, sm_count, p);
         return DG_OK;
     }
     const int64_t tiles = ((M + 127) / 128) * ((N + 63) / 64);
@@ -161,6 +190,7 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             return from_cuda(launch_gemv(A, B, D, static_cast<int>(M), static_cast<int>(N),
                                          static_cast<int>(K), fp16_in, sa, sb, sd, ok, amax_bits,
                                          s));
+        case 4:
         default: {
             TcLaunch L;
             L.A = A;
@@ -180,6 +210,8 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             L.amax_out = amax_bits;
             L.group_off = nullptr;
             L.groups = 0;
+            if (plan.path == 4)
+                return from_cuda(launch_gemm_skinny(L, st->splitk_partials, st->splitk_counts, s));
             return from_cuda(launch_gemm_tc(L, s));
         }
     }
@@ -375,7 +407,14 @@ dg_status dg_sync_status(dg_stream_t stream) {
         return DG_ERR_CUDA;
     if (word != 0) {
         if (cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess) return DG_ERR_CUDA;
-        if (word & kStatusTimeout) return DG_ERR_TIMEOUT;
+        if (word & kStatusTimeout) {
+            // A CTA that gave up may have left split-K arrival counters
+            // part-way: clear them (every launch expects zeros).
+            if (cudaDeviceSynchronize() != cudaSuccess ||
+                cudaMemset(st->splitk_counts, 0, sizeof(uint32_t) * kSkinnyMaxTiles) != cudaSuccess)
+                return DG_ERR_CUDA;
+            return DG_ERR_TIMEOUT;
+        }
         if (word & kStatusBadArgument) return DG_ERR_INVALID_VALUE;
     }
     return DG_OK;

@@ -15,11 +15,21 @@ inline int out_kind_of(dg_dtype t) {
 }
 inline int elem_bytes(dg_dtype t) { return t == DG_E4M3 ? 1 : 2; }
 
+// Split-K path for skinny GEMMs (M <= 16): 128 rows of B per tile, the M
+// rows of A padded to 16, K blocks of every tile spread evenly over the SMs.
+constexpr int kSkinnyMaxM = 16;
+constexpr int kSkinnyTileRows = 128;
+constexpr int kSkinnyMaxTiles = 8192;   // N <= 1,048,576
+
 // Per-device state, created once per device on first use.
 struct DeviceState {
     int device = -1;
     int sm_count = 0;
     uint32_t* status = nullptr;  // device status word (kStatus* bits)
+    // Split-K workspace: two FP32 partial-tile slots of 16 x 128 per SM and
+    // one arrival counter per tile (all zero between launches).
+    float* splitk_partials = nullptr;
+    uint32_t* splitk_counts = nullptr;
 };
 
 // Returns the current device's state, creating it on first use.
@@ -87,6 +97,11 @@ cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s);
 // Grouped variant (single-CTA tiles; L.plan->block_n is 128 or 256).
 cudaError_t launch_gemm_tc_grouped(const TcLaunch& L, cudaStream_t s);
 constexpr int kMaxGemmGroups = 1024;
+
+// Skinny split-K tensor-core GEMM (plan path 4).
+cudaError_t launch_gemm_skinny(const TcLaunch& L, float* partials, uint32_t* counts,
+                               cudaStream_t s);
+void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p);
 
 // Tile table for the tensor-core path (fills block_n, stages, smem, grid).
 void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,

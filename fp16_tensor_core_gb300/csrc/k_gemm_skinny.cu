@@ -1,0 +1,475 @@
+// k_gemm_skinny.cu -- the tensor-core path for skinny GEMMs (M <= 16):
+// split-K over every SM, with the operands swapped so that the long side
+// fills the 128-row MMA.
+//
+// Page shorthands: [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南";
+// [DG-FP16] = the DeepGEMM FP16/WMMA deep-dive page.
+//
+// For a decode-style product (a handful of activation rows against a large
+// weight matrix) the weight B is read once and the work is bound by HBM
+// ([DG-FP16] §2.1, weight-aware tiling).  A 128 x BN output tile with
+// M <= 16 would leave 7/8 of each MMA empty and give N/BN tiles -- too few
+// to occupy 152 SMs.  Here instead:
+//  * operands are swapped: the MMA computes D^T = B * A^T, its M side (128)
+//    is 128 rows of B and its N side (16) the M rows of A, zero-filled by TMA
+//    past M ([FP8-guide] §3.3's edge handling);
+//  * the K blocks of all tiles form one sequence of `units` (tile, k block)
+//    that is cut into gridDim.x equal contiguous ranges, one per CTA, so every
+//    SM streams the same number of bytes (split-K, balanced);
+//  * a CTA's range splits at tile boundaries into segments.  A segment that
+//    covers a whole tile writes D directly; otherwise the CTA stores its FP32
+//    partial tile in a workspace slot and bumps the tile's arrival counter,
+//    and the CTA that arrives last adds the partials in segment order (fixed,
+//    so the result does not depend on arrival order), applies
+//    scale_A * scale_B (/ scale_D for E4M3 out, [FP8-guide] §3.2), stores D
+//    and resets the counter to zero.  No CTA waits for another.
+// Pipeline: one TMA thread, one MMA thread, four epilogue warps, a ring of
+// 12 K blocks (16 KB of B + 2 KB of A each, 1 / 2 / 4 blocks per stage) and
+// two 16-column accumulators in tensor memory.  Launch overlap: before its
+// dependency wait a CTA prefetches its first ring of B into L2, and right
+// after it the grid lets the next kernel take over SMs as CTAs exit, so the
+// start-up of one launch hides in the straggling tail of the one before.
+// All mbarrier waits are bounded as in the other GEMMs.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "dg_internal.h"
+#include "dg_ptx.cuh"
+#include "gemm_common.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kRows = kSkinnyTileRows;            // MMA M: rows of B per tile
+constexpr int kCols = kSkinnyMaxM;                // MMA N: rows of A (padded)
+constexpr int kWBytes = kRows * kBKBytes;         // 16 KB of B per K block
+constexpr int kXBytes = kCols * kBKBytes;         // 2 KB of A per K block
+constexpr int kKBBytes = kWBytes + kXBytes;       // 18 KB per K block
+constexpr int kRingKBlocks = 12;                  // K blocks in flight per CTA
+constexpr int kBarBytes = 256;
+constexpr int kSkSmemBytes = 1024 + kRingKBlocks * kKBBytes + kBarBytes;
+constexpr uint32_t kTmemCols = 32;                // two 16-column accumulators
+constexpr uint32_t kIdesc = idesc_f32acc(kRows, kCols, 0, 0);
+constexpr uint32_t kEpiBar = 1;                   // named barrier of the epilogue warps
+constexpr uint32_t kEpiThreads = 128;
+static_assert(kSkSmemBytes <= kSmemLimit, "shared memory");
+static_assert(kXBytes % 1024 == 0, "1024-byte aligned A blocks (128-byte swizzle atoms)");
+
+// A stage holds up to KPS consecutive K blocks of one tile, loaded together
+// so that each row of B is requested KPS x 128 contiguous bytes at a time.
+template <int KPS>
+struct SkCfg {
+    static_assert(kRingKBlocks % KPS == 0, "ring");
+    static constexpr int kStages = kRingKBlocks / KPS;
+    static constexpr int kStageW = KPS * kWBytes;
+    static constexpr int kStageX = KPS * kXBytes;
+};
+
+struct SkParams {
+    void* D;
+    int M, N, K;
+    const float* sa;
+    const float* sb;
+    const float* sd;
+    int out_kind;
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int skip_first_load;
+    uint32_t* amax_out;
+    float* partials;       // [2 * gridDim.x][16][128]
+    uint32_t* counts;      // [tiles]
+    int tiles;             // ceil(N / 128)
+    int kblocks;           // ceil(K / BK)
+};
+
+// CTA i's range of units is [range_start(i), range_start(i + 1)).
+__device__ __forceinline__ int64_t range_start(int i, int G, int64_t units) {
+    return static_cast<int64_t>(i) * units / G;
+}
+
+// The CTA whose range holds unit u.
+__device__ __forceinline__ int cta_of_unit(int64_t u, int G, int64_t units) {
+    return static_cast<int>(((u + 1) * G - 1) / units);
+}
+
+// Workspace slots: a CTA has at most two partial segments, its first (slot
+// 2c) and its last (2c + 1).  In a split tile t, every CTA after the first
+// one (c_first) starts its range inside t, so its segment there is its first
+// (slot 2c); c_first's segment is its first only if its range starts exactly
+// at the tile.
+
+// Scale, convert and store one output element.
+__device__ __forceinline__ void store_one(const SkParams& p, int m, int n, float v) {
+    const int64_t off = static_cast<int64_t>(m) * p.N + n;
+    if (p.out_kind == kOutE4M3) {
+        static_cast<uint8_t*>(p.D)[off] = static_cast<uint8_t>(f32x2_to_e4m3x2(v, 0.0f) & 0xFFu);
+    } else if (p.out_kind == kOutFP16) {
+        static_cast<uint16_t*>(p.D)[off] = static_cast<uint16_t>(f32x2_to_f16x2(v, 0.0f) & 0xFFFFu);
+    } else {
+        static_cast<uint16_t*>(p.D)[off] = static_cast<uint16_t>(f32x2_to_bf16x2(v, 0.0f) & 0xFFFFu);
+    }
+}
+
+template <bool kFp16In, int KPS>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_x, const SkParams p) {
+    constexpr int kBK = kFp16In ? 64 : 128;   // K elements per K block
+    using C = SkCfg<KPS>;
+    constexpr int kStages = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sW = smem;                          // B rows (MMA operand A)
+    uint8_t* sX = smem + kStages * C::kStageW;   // A rows (MMA operand B)
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRingKBlocks * kKBBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* acc_full = empty + kStages;   // [2]
+    uint64_t* acc_empty = acc_full + 2;     // [2]
+    uint64_t* drain = acc_empty + 2;        // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    volatile int* last_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_x);
+    }
+    if (warp == 2) {
+        tmem_alloc<kTmemCols>(tmem_slot);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+    const int G = gridDim.x;
+    const int KB = p.kblocks;
+    const int64_t units = static_cast<int64_t>(p.tiles) * KB;
+    const int64_t u_begin = range_start(blockIdx.x, G, units);
+    const int64_t n_units = range_start(blockIdx.x + 1, G, units) - u_begin;
+    const int t_begin = static_cast<int>(u_begin / KB);
+    const int kb_begin = static_cast<int>(u_begin - static_cast<int64_t>(t_begin) * KB);
+
+    if (warp == 0 && lane == 0) {
+        // Warm L2 with this CTA's first ring of B blocks while the preceding
+        // kernel finishes (a prefetch only moves lines into L2).
+        int t = t_begin, kb = kb_begin;
+        for (int i = 0; i < kRingKBlocks && i < n_units; ++i) {
+            tma_prefetch_l2_2d(&tmap_w, kb * kBK, t * kRows);
+            if (++kb == KB) { kb = 0; ++t; }
+        }
+    }
+    pdl_wait();   // the prologue above overlaps the preceding kernel's tail
+    // The next kernel may now take over each SM as soon as this grid's CTA
+    // on it exits; it waits for the whole grid before touching memory.
+    pdl_launch_dependents();
+
+    // Every role walks the same segments: tile t from K block kb0 to kb_end.
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0;
+        uint32_t issued_phase = 0;
+        bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
+        bool ok = true;
+        int t = t_begin, kb0 = kb_begin;
+        for (int64_t left = n_units; left > 0 && ok; ++t, kb0 = 0) {
+            const int kb_end = static_cast<int>(min(static_cast<int64_t>(KB), kb0 + left));
+            left -= kb_end - kb0;
+            for (int kb = kb0; kb < kb_end; kb += KPS) {
+                const int nk = min(KPS, kb_end - kb);
+                if (!wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
+                if (skip) {
+                    skip = false;   // leave this stage unloaded
+                } else {
+                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nk * kKBBytes));
+#pragma unroll
+                    for (int i = 0; i < KPS; ++i) {
+                        if (i < nk) {
+                            tma_load_2d(sW + stage * C::kStageW + i * kWBytes, &tmap_w, &full[stage],
+                                        (kb + i) * kBK, t * kRows);
+                            tma_load_2d(sX + stage * C::kStageX + i * kXBytes, &tmap_x, &full[stage],
+                                        (kb + i) * kBK, 0);
+                        }
+                    }
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                }
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+        }
+        // Let every issued copy land before the CTA exits (immediate after a
+        // normal run; after an abort, copies still in flight finish).
+        for (int s = 0; s < kStages; ++s)
+            if (issued_mask & (1u << s))
+                wait_bounded(&full[s], (issued_phase >> s) & 1u, ctl, false);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        bool issued_any = false;
+        int kb0 = kb_begin;
+        for (int64_t left = n_units; left > 0 && ok; kb0 = 0) {
+            const int kb_end = static_cast<int>(min(static_cast<int64_t>(KB), kb0 + left));
+            left -= kb_end - kb0;
+            if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, ctl)) break;
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kCols);
+            for (int kb = kb0; kb < kb_end; kb += KPS) {
+                const int nk = min(KPS, kb_end - kb);
+                if (!wait_bounded(&full[stage], phase, ctl)) { ok = false; break; }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int i = 0; i < KPS; ++i) {
+                    if (i < nk) {
+                        const uint32_t a0 = smem_addr(sW + stage * C::kStageW + i * kWBytes);
+                        const uint32_t b0 = smem_addr(sX + stage * C::kStageX + i * kXBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kBKBytes / 32; ++kk) {
+                            const uint64_t ad = sdesc_k_major_sw128(a0 + kk * 32);
+                            const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
+                            const uint32_t accum = (kb > kb0 || i > 0 || kk > 0) ? 1u : 0u;
+                            if constexpr (kFp16In)
+                                mma_f16(d_tmem, ad, bd, kIdesc, accum);
+                            else
+                                mma_f8f6f4(d_tmem, ad, bd, kIdesc, accum);
+                        }
+                    }
+                }
+                issued_any = true;
+                mma_commit(&empty[stage]);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit(&acc_full[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (issued_any) {
+            mma_commit(drain);
+            wait_bounded(drain, 0, ctl, false);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue
+        // Thread (q, lane) owns row r = 32 q + lane of each tile (its tensor-
+        // memory lane) and that row's 16 accumulator columns, one per row of A.
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const int me = static_cast<int>(blockIdx.x);
+        float ab = 1.0f;
+        if (p.sa != nullptr) ab = p.sa[0] * p.sb[0];
+        const float alpha = p.out_kind == kOutE4M3 ? __fdiv_rn(ab, p.sd[0]) : ab;
+        uint32_t amax_bits = 0u;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int t = t_begin, kb0 = kb_begin;
+        for (int64_t left = n_units; left > 0; ++t, kb0 = 0) {
+            const int kb_end = static_cast<int>(min(static_cast<int64_t>(KB), kb0 + left));
+            left -= kb_end - kb0;
+            // Which CTAs share tile t, and their slots (before the wait).
+            const int64_t tile_u0 = static_cast<int64_t>(t) * KB;
+            const int c_first = cta_of_unit(tile_u0, G, units);
+            const int c_last = cta_of_unit(tile_u0 + KB - 1, G, units);
+            const int first_slot =
+                range_start(c_first, G, units) == tile_u0 ? 2 * c_first : 2 * c_first + 1;
+            // The four warps continue or leave together (named barriers below).
+            const bool got = wait_bounded(&acc_full[acc], acc_phase, ctl);
+            if (!named_bar_and(kEpiBar, kEpiThreads, got)) break;
+            tc_fence_after_sync();
+            uint32_t raw[16];
+            __syncwarp();
+            tmem_load_16cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                 static_cast<uint32_t>(acc * kCols),
+                             raw);
+            tmem_load_wait(raw);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+
+            float v[kCols];
+#pragma unroll
+            for (int m = 0; m < kCols; ++m) v[m] = __uint_as_float(raw[m]);
+            bool finish = true;
+            if (c_last > c_first) {
+                // Split tile: publish this partial, count the arrival.
+                const int my_slot = me == c_first ? first_slot : 2 * me;
+                float* ws = p.partials + static_cast<int64_t>(my_slot) * kCols * kRows;
+#pragma unroll
+                for (int m = 0; m < kCols; ++m)
+                    if (m < p.M) ws[m * kRows + r] = v[m];
+                named_bar_sync(kEpiBar, kEpiThreads);
+                if (threadIdx.x == 4 * 32) {
+                    const uint32_t old = atom_add_acq_rel_gpu(&p.counts[t], 1u);
+                    const bool last = old == static_cast<uint32_t>(c_last - c_first);
+                    if (last) atomicExch(&p.counts[t], 0u);   // zero for the next launch
+                    *last_flag = last ? 1 : 0;
+                }
+                named_bar_sync(kEpiBar, kEpiThreads);
+                finish = *last_flag != 0;
+                if (finish) {
+                    // Sum the segments in order c_first .. c_last, the own
+                    // one from registers, the others from their slots.
+                    float sum[kCols];
+#pragma unroll 1
+                    for (int c = c_first; c <= c_last; ++c) {
+                        float x[kCols];
+                        if (c == me) {
+#pragma unroll
+                            for (int m = 0; m < kCols; ++m) x[m] = v[m];
+                        } else {
+                            const int slot = c == c_first ? first_slot : 2 * c;
+                            const float* w = p.partials + static_cast<int64_t>(slot) * kCols * kRows;
+#pragma unroll
+                            for (int m = 0; m < kCols; ++m)
+                                x[m] = m < p.M ? __ldcg(w + m * kRows + r) : 0.0f;
+                        }
+#pragma unroll
+                        for (int m = 0; m < kCols; ++m) sum[m] = c == c_first ? x[m] : sum[m] + x[m];
+                    }
+#pragma unroll
+                    for (int m = 0; m < kCols; ++m) v[m] = sum[m];
+                }
+            }
+            if (finish) {
+                const int n = t * kRows + r;
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < kCols; ++m) {
+                        if (m < p.M) {
+                            amax_bits = max(amax_bits, __float_as_uint(v[m]) & 0x7FFFFFFFu);
+                            store_one(p, m, n, v[m] * alpha);
+                        }
+                    }
+                }
+            }
+        }
+        // max |sa*sb*acc| of this warp's stored outputs (monotone rounding:
+        // fl(max|acc| * c) is the exact maximum of fl(|acc| * c)).
+        if (p.amax_out != nullptr) {
+            __syncwarp();
+            const uint32_t bits = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+            if (lane == 0 && bits != 0u)
+                atomicMax(p.amax_out, __float_as_uint(__uint_as_float(bits) * ab) & 0x7FFFFFFFu);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 2) tmem_dealloc<kTmemCols>(tmem_base);
+}
+
+// ------------------------------------------------------------- host side
+
+template <bool kFp16In, int KPS>
+cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cudaStream_t s) {
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!attr_done[dev]) {
+            e = cudaFuncSetAttribute(gemm_skinny_kernel<kFp16In, KPS>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSkSmemBytes);
+            if (e != cudaSuccess) return e;
+            attr_done[dev] = true;
+        }
+    }
+    CUtensorMap tw, tx;
+    if (!make_map(&tw, L.B, L.N, L.K, kFp16In, kRows) || !make_map(&tx, L.A, L.M, L.K, kFp16In, kCols))
+        return cudaErrorInvalidValue;
+    SkParams prm;
+    prm.D = L.D;
+    prm.M = L.M;
+    prm.N = L.N;
+    prm.K = L.K;
+    prm.sa = L.sa;
+    prm.sb = L.sb;
+    prm.sd = L.sd;
+    prm.out_kind = L.out_kind;
+    prm.status = L.status;
+    prm.timeout_ns = wait_timeout_ns();
+    prm.skip_first_load = take_skip_first_load() ? 1 : 0;
+    prm.amax_out = L.amax_out;
+    prm.partials = partials;
+    prm.counts = counts;
+    prm.tiles = L.plan->tiles;
+    const int bk = kFp16In ? 64 : 128;
+    prm.kblocks = (L.K + bk - 1) / bk;
+    return launch_kernel(gemm_skinny_kernel<kFp16In, KPS>, dim3(L.plan->grid), dim3(kThreads),
+                         kSkSmemBytes, s, tw, tx, prm);
+}
+
+// K blocks per stage: DG_SPLITK_KPS=1|2|4 (sweeps), default 2.
+int splitk_kps() {
+    if (const char* v = std::getenv("DG_SPLITK_KPS")) {
+        const int k = std::atoi(v);
+        if (k == 1 || k == 2 || k == 4) return k;
+    }
+    return 2;
+}
+
+template <bool kFp16In>
+cudaError_t launch_kps(const TcLaunch& L, float* partials, uint32_t* counts, cudaStream_t s) {
+    switch (kRingKBlocks / L.plan->stages) {
+        case 1: return launch_sk<kFp16In, 1>(L, partials, counts, s);
+        case 4: return launch_sk<kFp16In, 4>(L, partials, counts, s);
+        default: return launch_sk<kFp16In, 2>(L, partials, counts, s);
+    }
+}
+
+}  // namespace
+
+void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p) {
+    const int bk = fp16_in ? 64 : 128;
+    const int64_t tiles = (N + kRows - 1) / kRows;
+    const int64_t units = tiles * ((K + bk - 1) / bk);
+    p->block_m = kCols;
+    p->block_n = kRows;
+    p->block_k = bk;
+    p->stages = kRingKBlocks / splitk_kps();
+    p->tiles = static_cast<int>(tiles);
+    p->grid = static_cast<int>(units < sm_count ? units : sm_count);
+    p->smem_bytes = kSkSmemBytes;
+    (void)M;
+}
+
+cudaError_t launch_gemm_skinny(const TcLaunch& L, float* partials, uint32_t* counts,
+                               cudaStream_t s) {
+    if (L.M < 1 || L.M > kCols || L.plan->tiles > kSkinnyMaxTiles || partials == nullptr ||
+        counts == nullptr)
+        return cudaErrorInvalidValue;
+    return L.fp16_in ? launch_kps<true>(L, partials, counts, s)
+                     : launch_kps<false>(L, partials, counts, s);
+}
+
+}  // namespace dg

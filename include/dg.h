@@ -177,13 +177,17 @@ dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M,
  * JIT.  in is DG_E4M3 or DG_FP16.  sm_count <= 0 queries the current device.
  */
 typedef struct {
-    int path;       /* 0 no-op, 1 zero-fill (K == 0), 2 GEMV, 3 tensor core */
-    int block_m;    /* output rows per tile (tensor-core path)              */
+    int path;       /* 0 no-op, 1 zero-fill (K == 0), 2 GEMV, 3 tensor core,
+                       4 split-K tensor core for M <= 16 (operands swapped:
+                       block_m = 16 padded rows of A, block_n = 128 rows of
+                       B per tile, K blocks of all tiles spread over grid
+                       CTAs)                                                */
+    int block_m;    /* output rows per tile (tensor-core paths)             */
     int block_n;    /* output columns per tile                              */
     int block_k;    /* K elements per pipeline stage                        */
     int stages;     /* shared-memory pipeline depth                         */
     int grid;       /* CTAs launched                                        */
-    int tiles;      /* output tiles (tensor-core path)                      */
+    int tiles;      /* output tiles (tensor-core paths)                     */
     int smem_bytes; /* dynamic shared memory per CTA                        */
 } dg_plan;
 

@@ -145,7 +145,23 @@ def test_plan_paths_and_tiles(L):
         p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
         assert p["path"] == 2 and p["block_n"] == 8 and p["grid"] == 12288 // 8
     for m in (3, 16):
-        assert dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)["path"] == 3
+        # split-K: 96 tiles of 128 rows of B, 96 x 32 K blocks over 152 CTAs
+        p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
+        assert p["path"] == 4 and p["block_m"] == 16 and p["block_n"] == 128
+        assert p["tiles"] == 96 and p["grid"] == sm and p["block_k"] == 128
+        assert p["smem_bytes"] <= 232448
+    # fewer K blocks than SMs: one per CTA
+    p = dg.dg_gemm_plan(5, 200, 256, sm_count=sm)
+    assert p["path"] == 4 and p["tiles"] == 2 and p["grid"] == 4
+    assert dg.dg_gemm_plan(5, 200, 256, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16,
+                           sm_count=sm)["grid"] == 8
+    os.environ["DG_SPLITK"] = "0"
+    try:
+        assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=sm)["path"] == 3
+    finally:
+        del os.environ["DG_SPLITK"]
+    assert dg.dg_gemm_plan(17, 12288, 4096, sm_count=sm)["path"] == 3
+    assert dg.dg_gemm_plan(16, 128 * 8192 + 1, 64, sm_count=sm)["path"] == 3   # too many tiles
     os.environ["DG_GEMV_MAX_M"] = "16"
     try:
         for m, rows in ((4, 8), (5, 4), (16, 4)):
@@ -153,7 +169,7 @@ def test_plan_paths_and_tiles(L):
             assert p["path"] == 2 and p["block_n"] == rows and p["grid"] == 12288 // rows
     finally:
         del os.environ["DG_GEMV_MAX_M"]
-    for m in (3, 17, 63, 65, 129, 256, 4096, 8192):
+    for m in (17, 63, 65, 129, 256, 4096, 8192):
         p = dg.dg_gemm_plan(m, 1000, 1040, sm_count=sm)
         assert p["path"] == 3
         assert p["block_n"] in (64, 128, 160, 192, 224, 256)

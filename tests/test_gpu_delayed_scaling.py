@@ -41,7 +41,8 @@ def _amax_bound(R, S, sa, sb):
 @pytest.mark.parametrize("M,N,K,pairs,path", [
     (1, 1000, 1040, "0", 2),      # GEMV
     (7, 300, 512, "0", 2),        # GEMV, several rows (crossover raised to 16)
-    (7, 300, 512, "0", 3),        # the same shape on the tensor-core kernel
+    (7, 300, 512, "0", 4),        # the same shape on the split-K kernel
+    (16, 1000, 1040, "0", 4),     # split-K, every tile split across CTAs
     (65, 1000, 1040, "0", 3),     # single CTA
     (129, 777, 272, "0", 3),      # single CTA, ragged
     (300, 777, 272, "1", 3),      # CTA pairs, odd CTA partly out of range

@@ -1,0 +1,211 @@
+"""Split-K tensor-core path for skinny GEMMs (plan path 4: M <= 16, operands
+swapped, K blocks spread over every SM, partial tiles added in a fixed
+order by the CTA that finishes a tile last) against the CPU oracle.
+
+Covers ragged N (a partial last tile of 128 rows of B) and ragged K (a
+zero-filled last K block), fewer K blocks than SMs, tiles split over two
+and three CTAs, FP16 inputs, E4M3 output, run-to-run determinism, reuse of
+the arrival counters across shapes and graph replays, and recovery after a
+bounded wait runs out.  [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化
+指南" §3.3 (M/N/K boundary handling)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import fp16_tensor_core_gb300 as dg
+import oracle
+import synth
+from _parity import (bf16_bits_to_f64, check_bf16_like, check_e4m3, check_guards,
+                     check_quantised, dev, fp16_bits_to_f64, gpu_quantize, guarded,
+                     sample_positions, scalar)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from fp16_tensor_core_gb300 import build
+    build.build()
+    dg.dg_init()
+    yield
+    assert dg.dg_sync_status() == dg.DG_OK
+
+
+def _plan(M, N, K, in_dtype=dg.DG_E4M3):
+    p = dg.dg_gemm_plan(M, N, K, in_dtype, dg.DG_BF16)
+    assert p["path"] == 4, p
+    return p
+
+
+def _fp8_case(M, N, K, seed_name="fp8_sweep_m65"):
+    A, B = synth.make_inputs(seed_name, M=M, N=N, K=K)
+    qa, amax_a, sa = gpu_quantize(A)
+    qb, amax_b, sb = gpu_quantize(B)
+    qa_ref, sa_ref = check_quantised(A, qa, amax_a, sa)
+    qb_ref, sb_ref = check_quantised(B, qb, amax_b, sb)
+    return qa, qb, sa, sb, qa_ref, qb_ref, sa_ref, sb_ref
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (3, 1000, 1040),     # ragged N and K; 8 tiles x 9 K blocks < 152 CTAs
+    (16, 1000, 1040),
+    (5, 128, 128),       # one tile, one K block
+    (7, 300, 4096),      # 3 tiles x 32 K blocks over 96 CTAs
+    (9, 2048, 2048),     # 16 x 16 = 256 units: tiles split over 2 CTAs
+    (12, 4000, 1024),    # 32 x 8 = 256 units, ragged N
+    (16, 12288, 512),    # 96 x 4 = 384 units: splits across 3 CTAs
+    (4, 777, 16),        # K = 16: a single zero-filled K block
+])
+def test_splitk_bf16_matches_oracle(M, N, K):
+    _plan(M, N, K)
+    qa, qb, sa, sb, qa_ref, qb_ref, sa_ref, sb_ref = _fp8_case(M, N, K)
+    buf, D = guarded(M * N, torch.int16, 0x7FFF)
+    dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf, M * N, 0x7FFF)
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    d = bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N))
+    check_bf16_like(d, R, S, sa_ref, sb_ref)
+
+
+def test_splitk_m1_when_forced():
+    """M = 1 and 2 on the split-K kernel (the GEMV crossover moved to 0)."""
+    os.environ["DG_GEMV_MAX_M"] = "0"
+    try:
+        for M in (1, 2):
+            N, K = 1000, 1040
+            _plan(M, N, K)
+            qa, qb, sa, sb, qa_ref, qb_ref, sa_ref, sb_ref = _fp8_case(M, N, K)
+            D = torch.empty((M, N), dtype=torch.int16, device="cuda")
+            dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16)
+            assert dg.dg_sync_status() == dg.DG_OK
+            R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+            check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16)), R, S,
+                            sa_ref, sb_ref)
+    finally:
+        os.environ.pop("DG_GEMV_MAX_M", None)
+
+
+def test_splitk_qkv_m16_sampled():
+    """The decode QKV weight shape with 16 activation rows, sampled."""
+    M, N, K = 16, 12288, 4096
+    _plan(M, N, K)
+    A, B = synth.make_inputs("fp8_qkv", M=M)
+    qa, amax_a, sa = gpu_quantize(A)
+    qb, amax_b, sb = gpu_quantize(B)
+    qa_ref, sa_ref = check_quantised(A, qa, amax_a, sa)
+    qb_ref, sb_ref = check_quantised(B, qb, amax_b, sb)
+    D = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16)
+    assert dg.dg_sync_status() == dg.DG_OK
+    ms, ns = sample_positions(M, N, 4000, tile_m=16, tile_n=128)
+    R, S = oracle.gemm_e4m3_at(qa_ref, qb_ref, ms, ns)
+    d = bf16_bits_to_f64(D.cpu().numpy().view(np.uint16)[ms, ns])
+    check_bf16_like(d, R, S, sa_ref, sb_ref)
+
+
+def test_splitk_e4m3_out():
+    M, N, K = 11, 1000, 2080
+    _plan(M, N, K)
+    A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+    qa_ref, sa, _ = oracle.quantize_tensor(A)
+    qb_ref, sb, _ = oracle.quantize_tensor(B)
+    R = oracle.gemm_e4m3(qa_ref, qb_ref, with_abs=False)
+    sd = np.float32(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))) / 448.0)
+    qa, _, sa_d = gpu_quantize(A)
+    qb, _, sb_d = gpu_quantize(B)
+    sdt = scalar()
+    sdt[0] = float(sd)
+    buf, D = guarded(M * N, torch.uint8, 0x7F)
+    dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, sdt, dg.DG_E4M3, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf, M * N, 0x7F)
+    check_e4m3(D.cpu().numpy().reshape(M, N), R, sa, sb, sd)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 520, 1040), (16, 1000, 3000)])
+def test_splitk_fp16_hgemm(M, N, K):
+    _plan(M, N, K, dg.DG_FP16)
+    A, B = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
+    buf, D = guarded(M * N, torch.int16, 0x7FFF)
+    dg.dg_hgemm(dev(A.view(np.int16)), dev(B.view(np.int16)), D, dg.DG_FP16, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf, M * N, 0x7FFF)
+    R, S = oracle.hgemm(A, B)
+    check_bf16_like(fp16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N)), R, S,
+                    1.0, 1.0, "FP16")
+
+
+def test_splitk_deterministic_and_counters_reused_across_shapes():
+    """Partial tiles are added in segment order, so repeated calls give the
+    same bits; interleaving shapes with different tile splits reuses the
+    arrival counters, which every call must leave at zero."""
+    shapes = [(9, 2048, 2048), (16, 12288, 512), (3, 1000, 1040)]
+    cases = [(s, _fp8_case(*s)) for s in shapes]
+    first = {}
+    for rep in range(3):
+        for (M, N, K), (qa, qb, sa, sb, *_rest) in cases:
+            D = torch.empty((M, N), dtype=torch.int16, device="cuda")
+            dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16)
+            assert dg.dg_sync_status() == dg.DG_OK
+            h = D.cpu().numpy()
+            if rep == 0:
+                first[(M, N, K)] = h
+            else:
+                assert np.array_equal(h, first[(M, N, K)]), (M, N, K, rep)
+    M, N, K = shapes[1]
+    _, _, _, _, qa_ref, qb_ref, sa_ref, sb_ref = cases[1][1]
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    check_bf16_like(bf16_bits_to_f64(first[(M, N, K)].view(np.uint16)), R, S, sa_ref, sb_ref)
+
+
+def test_splitk_graph_replay():
+    M, N, K = 16, 12288, 512
+    qa, qb, sa, sb, *_ = _fp8_case(M, N, K)
+    direct = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    dg.dg_fp8_gemm(qa, qb, direct, sa, sb, None, dg.DG_BF16)
+    assert dg.dg_sync_status() == dg.DG_OK
+    D = torch.empty_like(direct)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):   # three launches per replay: counters must be back at zero each time
+            dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, stream=s)
+    for _ in range(2):
+        D.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert dg.dg_sync_status() == dg.DG_OK
+        assert torch.equal(D, direct)
+
+
+def test_splitk_timeout_then_recovers():
+    """One stage left unloaded: the bounded wait runs out, the call reports
+    DG_ERR_TIMEOUT, dg_sync_status clears the arrival counters, and the next
+    split-K GEMM is correct."""
+    M, N, K = 9, 2048, 2048
+    _plan(M, N, K)
+    qa, qb, sa, sb, qa_ref, qb_ref, sa_ref, sb_ref = _fp8_case(M, N, K)
+    D = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    assert dg.dg_sync_status() == dg.DG_OK
+    dg.dg_set_wait_timeout_us(100_000)
+    try:
+        dg.dg_debug_skip_first_load(True)
+        dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16)
+        assert dg.dg_sync_status() == dg.DG_ERR_TIMEOUT
+        assert dg.dg_sync_status() == dg.DG_OK
+    finally:
+        dg.dg_set_wait_timeout_us(2_000_000)
+        dg.dg_debug_skip_first_load(False)
+    D.zero_()
+    dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16)
+    assert dg.dg_sync_status() == dg.DG_OK
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16)), R, S, sa_ref, sb_ref)
