@@ -18,7 +18,7 @@ __all__ = [
     "DG_OK", "DG_ERR_INVALID_VALUE", "DG_ERR_MISALIGNED", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_TIMEOUT", "DG_BF16", "DG_E4M3", "DG_FP16", "DgError",
     "lib", "library_path", "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm",
-    "dg_fp8_gemm_amax", "dg_fp8_gemm_grouped",
+    "dg_fp8_gemm_amax", "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static",
     "dg_hgemm",
     "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
     "dg_debug_skip_first_load", "dg_status_string", "dg_version", "EXPORTED_SYMBOLS",
@@ -30,7 +30,7 @@ DG_BF16, DG_E4M3, DG_FP16 = 0, 1, 2
 #: Every function include/dg.h declares.
 EXPORTED_SYMBOLS = (
     "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax",
-    "dg_fp8_gemm_grouped", "dg_hgemm", "dg_gemm_plan",
+    "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_hgemm", "dg_gemm_plan",
     "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
     "dg_status_string", "dg_version",
 )
@@ -75,6 +75,8 @@ def lib():
                                            vp, vp]
             L.dg_fp8_gemm_grouped.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, vp,
                                               vp, ctypes.c_int, vp]
+            L.dg_fp8_gemm_splitk_static.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp,
+                                                     ctypes.c_int, vp, vp]
             L.dg_hgemm.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]
             L.dg_gemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(_Plan)]
@@ -88,7 +90,8 @@ def lib():
             L.dg_status_string.restype = ctypes.c_char_p
             L.dg_version.argtypes = []
             for name in ("dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm",
-                         "dg_fp8_gemm_grouped", "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_version"):
+                         "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_gemm_plan", "dg_init",
+                         "dg_sync_status", "dg_version"):
                 getattr(L, name).restype = st
             _lib = L
     return _lib
@@ -170,6 +173,19 @@ def dg_fp8_gemm_amax(A, B, D, scale_a, scale_b, scale_d=None, out=DG_BF16, amax_
     _check(lib().dg_fp8_gemm_amax(_ptr(A), _ptr(B), _ptr(D), M, N, K, _ptr(scale_a), _ptr(scale_b),
                                   _ptr(scale_d), int(out), _ptr(amax_d), _stream(stream)),
            "dg_fp8_gemm_amax")
+
+
+def dg_fp8_gemm_splitk_static(A, B, D, scale_a, scale_b, scale_d=None, out=DG_BF16,
+                              status_out=None, stream=None, M=None, N=None, K=None) -> None:
+    """dg_fp8_gemm for M <= 16 on the split-K kernel with the library's static
+    workspace (no allocation); kernel error bits are ORed into status_out."""
+    if M is None:
+        M, K = A.shape
+        N = B.shape[0]
+    _check(lib().dg_fp8_gemm_splitk_static(_ptr(A), _ptr(B), _ptr(D), M, N, K, _ptr(scale_a),
+                                           _ptr(scale_b), _ptr(scale_d), int(out),
+                                           _ptr(status_out), _stream(stream)),
+           "dg_fp8_gemm_splitk_static")
 
 
 def dg_fp8_gemm_grouped(A, B, D, group_offsets, scale_a, scale_b, scale_d=None, out=DG_BF16,

@@ -163,6 +163,33 @@ dg_status dg_fp8_gemm_grouped(const uint8_t* A, const uint8_t* B, void* D,
                               const float* scale_d, dg_dtype out,
                               dg_stream_t stream);
 
+/* dg_fp8_gemm for skinny shapes (1 <= M <= 16) that never allocates: the
+ * split-K tensor-core kernel (plan path 4) runs with its workspace in fixed
+ * static device arrays of the library (2.5 MiB of FP32 partial tiles and
+ * 1025 32-bit words) instead of memory the library allocates.  The pages
+ * have no counterpart; it exists for callers that forbid allocation inside
+ * library calls.  For the same arguments the result is bit-identical to
+ * dg_fp8_gemm on the split-K path.
+ *   A, B, D, M, N, K, scale_a, scale_b, scale_d, out, stream: as
+ *          dg_fp8_gemm, with M <= 16 and N <= 131072 (1024 tiles of 128
+ *          rows of B); larger sizes return DG_ERR_INVALID_VALUE.
+ *   status_out  optional device uint32, 4-byte aligned: the kernel ORs its
+ *          error bits into it (1 = a bounded wait ran out, the output is
+ *          incomplete).  NULL: the bits go to a library word nobody reads.
+ * Each call first zeroes the arrival counters of the static workspace on
+ * `stream` (cudaMemsetAsync), then launches the kernel.  Calls share that one
+ * workspace per device: two calls whose executions overlap (different
+ * streams without ordering between them) race and give wrong results.  The
+ * first call on each device looks the arrays' addresses up and sets the
+ * kernel's shared-memory limit; make that first call before capturing a
+ * stream into a CUDA graph.  No memory is allocated or freed by this call.
+ */
+dg_status dg_fp8_gemm_splitk_static(const uint8_t* A, const uint8_t* B, void* D,
+                                    int64_t M, int64_t N, int64_t K,
+                                    const float* scale_a, const float* scale_b,
+                                    const float* scale_d, dg_dtype out,
+                                    uint32_t* status_out, dg_stream_t stream);
+
 /* FP16 GEMM (HGEMM), FP32 accumulation, no scaling.  [HGEMM-L2] §1.3 (FP16
  * inputs, FP32 accumulator) and §3; same layouts and edge rules as
  * dg_fp8_gemm.  A, B hold IEEE binary16 bit patterns.  K must be a multiple

@@ -114,6 +114,26 @@ def test_grouped_argument_errors(L):
     assert call(N=1 << 30, G=8) == dg.DG_ERR_INVALID_VALUE      # groups * N overflows
 
 
+def test_splitk_static_argument_errors(L):
+    """The no-allocation split-K entry rejects what its fixed workspace cannot
+    hold, and every other bad argument as dg_fp8_gemm does, before any CUDA
+    call."""
+    def call(A=FAKE, B=FAKE, D=FAKE, M=8, N=256, K=64, sa=FAKE, sb=FAKE, sd=None,
+             out=dg.DG_BF16, status=None):
+        return L.dg_fp8_gemm_splitk_static(A, B, D, M, N, K, sa, sb, sd, out, status, None)
+    assert call(M=17) == dg.DG_ERR_INVALID_VALUE                 # more rows than the MMA's 16
+    assert call(N=128 * 1024 + 1) == dg.DG_ERR_INVALID_VALUE     # more than 1024 tiles
+    assert call(M=-1) == dg.DG_ERR_INVALID_VALUE
+    assert call(out=7) == dg.DG_ERR_INVALID_VALUE
+    assert call(out=dg.DG_E4M3) == dg.DG_ERR_INVALID_VALUE       # scale_d missing
+    assert call(sa=None) == dg.DG_ERR_INVALID_VALUE
+    assert call(D=None) == dg.DG_ERR_INVALID_VALUE
+    assert call(K=24) == dg.DG_ERR_MISALIGNED
+    assert call(A=FAKE + 8) == dg.DG_ERR_MISALIGNED
+    assert call(status=FAKE + 2) == dg.DG_ERR_MISALIGNED
+    assert call(M=0) == dg.DG_OK and call(N=0) == dg.DG_OK       # empty: nothing launched
+
+
 def test_moe_group_sizes_recipe():
     import synth
     s = synth.moe_group_sizes(3, 16, 8192, empty=2)
