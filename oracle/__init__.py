@@ -60,6 +60,10 @@ def lib():
             L.dgo_scale_from_amax.restype = ctypes.c_float
             L.dgo_scale_pow2_from_amax.argtypes = [ctypes.c_float]
             L.dgo_scale_pow2_from_amax.restype = ctypes.c_float
+            L.dgo_fp16_range_scale.argtypes = [ctypes.c_float, ctypes.c_float, _f32p]
+            L.dgo_fp16_range_scale.restype = None
+            L.dgo_convert_f16.argtypes = [_f32p, _i64, ctypes.c_float, _u16p]
+            L.dgo_convert_f16.restype = None
             L.dgo_quantize_e4m3.argtypes = [_f32p, _i64, ctypes.c_float, _u8p]
             L.dgo_quantize_e4m3.restype = None
             L.dgo_gemm_e4m3.argtypes = [_u8p, _u8p, _i64, _i64, _i64, _f64p,
@@ -164,6 +168,33 @@ def quantize_tensor_pow2(x):
     a = amax(x)
     s = scale_pow2_from_amax(a)
     return quantize_e4m3(x, s), s, a
+
+
+def fp16_range_scale(amax_a, amax_b) -> np.ndarray:
+    """[scale, sqrt(scale), 1/scale, 1] as float32, scale = min(1,
+    65504 / (amax_a * amax_b)) ([DG-FP16] §3.3)."""
+    out = np.zeros(4, dtype=np.float32)
+    lib().dgo_fp16_range_scale(float(np.float32(amax_a)), float(np.float32(amax_b)), out)
+    return out
+
+
+def convert_f16(x, factor) -> np.ndarray:
+    """fp16_rn(fl32(x * factor)) elementwise, as uint16 bit patterns."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().dgo_convert_f16(x.ravel(), x.size, float(np.float32(factor)), out.reshape(-1))
+    return out
+
+
+def fp16_range_chain(A32, B32):
+    """The whole [DG-FP16] §3.3 path in the oracle: factors, the scaled FP16
+    operands and the exact FP64 product of those operands divided by scale.
+    Returns (factors, A16, B16, D) with D = R / scale (FP64)."""
+    f = fp16_range_scale(amax(A32), amax(B32))
+    A16 = convert_f16(A32, f[1])
+    B16 = convert_f16(B32, f[1])
+    R, S = hgemm(A16, B16)
+    return f, A16, B16, R * float(f[2]), S
 
 
 def quantize_e4m3(x, scale) -> np.ndarray:

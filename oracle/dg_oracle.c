@@ -210,6 +210,35 @@ float dgo_scale_pow2_from_amax(float amax) {
     return (float)ldexp(1.0, e);
 }
 
+/* [DG-FP16] §3.3: before the launch, take the largest magnitudes of A and
+ * B, form scale = min(1, 65504 / (max_abs_A * max_abs_B)), multiply A and B
+ * by sqrt(scale) and divide the result by scale, so that no FP16 value
+ * overflows on the way in.  The scale is formed in binary64 and rounded once
+ * to binary32; sqrt and the reciprocal are taken in binary64 from that
+ * binary32 value and rounded once (for sqrt and division this equals the
+ * correctly rounded binary32 operation). */
+void dgo_fp16_range_scale(float amax_a, float amax_b, float out[4]) {
+    float s;
+    if (isnan(amax_a) || isnan(amax_b)) {
+        s = NAN;
+    } else {
+        const double prod = (double)amax_a * (double)amax_b;
+        const double q = 65504.0 / prod;          /* +Inf when prod == 0 */
+        s = (float)(q < 1.0 ? q : 1.0);
+    }
+    out[0] = s;
+    out[1] = (float)sqrt((double)s);
+    out[2] = (float)(1.0 / (double)s);
+    out[3] = 1.0f;
+}
+
+void dgo_convert_f16(const float* x, int64_t n, float factor, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) {
+        const float y = x[i] * factor;            /* one binary32 rounding */
+        out[i] = dgo_fp16_encode((double)y);
+    }
+}
+
 /* [FP8-guide] §4.3: fp8 = clamp(round(x / scale), -448, 448), read as
  * round-to-nearest-even onto the E4M3 grid after a binary32 division. */
 static void quantize_range(const float* x, int64_t lo, int64_t hi, float scale,

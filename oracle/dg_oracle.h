@@ -53,6 +53,17 @@ float dgo_scale_from_amax(float amax);
  * NaN for NaN, +Inf for +Inf.  [FP8-guide] §2.1: a power of two just above
  * the range, so that scaling and unscaling are exponent shifts. */
 float dgo_scale_pow2_from_amax(float amax);
+/* FP16 dynamic-range scaling, [DG-FP16] §3.3 (mixed-precision pitfalls):
+ * scale = min(1, 65504 / (max|A| * max|B|)); A and B are multiplied by
+ * sqrt(scale) before they become FP16, and the result is divided by scale.
+ * out[0] = scale, with the product and the quotient formed in binary64 (no
+ * binary32 overflow of max|A| * max|B|) and rounded once to binary32; 1 when
+ * the product is 0; NaN when either amax is NaN.
+ * out[1] = fl32(sqrt(scale)), out[2] = fl32(1 / scale), out[3] = 1. */
+void  dgo_fp16_range_scale(float amax_a, float amax_b, float out[4]);
+/* out_i = fp16_rn(fl32(x_i * factor)): binary32 product, then one
+ * round-to-nearest-even to binary16 (overflow to +-Inf, NaN stays NaN). */
+void  dgo_convert_f16(const float* x, int64_t n, float factor, uint16_t* out);
 /* q_i = e4m3(fl32(x_i / scale)), binary32 division.  [FP8-guide] §4.3. */
 void  dgo_quantize_e4m3(const float* x, int64_t n, float scale, uint8_t* q);
 

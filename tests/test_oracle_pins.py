@@ -421,3 +421,104 @@ def test_pow2_scale_accuracy_against_amax_scale():
         errs.append(np.linalg.norm(D - exact) / np.linalg.norm(exact))
     assert all(e < FACTS["quantisation_error_guide"]["wrong_above_rel"] for e in errs)
     assert errs[1] <= 2.5 * errs[0]
+
+
+# ---------------------------------------------------------------------------
+# FP16 dynamic-range scaling ([DG-FP16] §3.3): scale = min(1, 65504 /
+# (max|A| max|B|)); A, B times sqrt(scale) into FP16; result divided by scale.
+
+def _is_correctly_rounded_f32(r, exact):
+    """r (float32) is the binary32 value nearest to the rational `exact`."""
+    from fractions import Fraction
+    r = np.float32(r)
+    lo = np.nextafter(r, np.float32(-np.inf))
+    hi = np.nextafter(r, np.float32(np.inf))
+    fr = Fraction(float(r))
+    return (abs(Fraction(float(lo)) - exact) >= abs(fr - exact) and
+            abs(Fraction(float(hi)) - exact) >= abs(fr - exact))
+
+
+def test_fp16_range_scale_closed_forms():
+    f = oracle.fp16_range_scale
+    assert list(f(1.0, 1.0)) == [1, 1, 1, 1]
+    assert list(f(256.0, 255.875)) == [1, 1, 1, 1]              # product exactly 65504
+    s = f(256.0, 256.0)                                         # 65504 / 65536
+    assert s[0] == np.float32(1 - 2 ** -11)
+    s = f(1024.0, 1024.0)                                       # 65504 / 2^20, exact
+    assert s[0] == np.float32(65504 / 2 ** 20)
+    assert list(f(0.0, 7.0)) == [1, 1, 1, 1]                    # all-zero operand
+    assert np.isnan(f(np.nan, 1.0)[0]) and np.isnan(f(1.0, np.nan)[0])
+    assert f(3e38, 3e38)[0] == np.float32(65504 / 9e76)        # product formed in FP64
+    assert f(1e6, 1e6)[3] == 1.0
+
+
+def test_fp16_range_scale_sqrt_and_reciprocal_correctly_rounded():
+    from fractions import Fraction
+    rng = np.random.default_rng(5)
+    for a, b in zip(10 ** rng.uniform(-3, 12, 300), 10 ** rng.uniform(-3, 12, 300)):
+        s, r, inv, one = oracle.fp16_range_scale(np.float32(a), np.float32(b))
+        exact_s = min(Fraction(1), Fraction(65504) / (Fraction(float(np.float32(a))) *
+                                                      Fraction(float(np.float32(b)))))
+        assert _is_correctly_rounded_f32(s, exact_s)
+        assert 0 < s <= 1 and one == 1
+        # sqrt: r is the float nearest to sqrt(s), i.e. the midpoints around r
+        # bracket s when squared
+        rs = Fraction(float(r))
+        lo = (rs + Fraction(float(np.nextafter(r, np.float32(0))))) / 2
+        hi = (rs + Fraction(float(np.nextafter(r, np.float32(2))))) / 2
+        assert lo * lo <= Fraction(float(s)) <= hi * hi
+        assert _is_correctly_rounded_f32(inv, 1 / Fraction(float(s)))
+
+
+def test_convert_f16_matches_numpy_half_cast():
+    """fp16_rn(fl32(x * factor)) against numpy's binary32 multiply and
+    binary32 -> binary16 cast (round to nearest even, overflow to Inf)."""
+    rng = np.random.default_rng(6)
+    x = np.concatenate([
+        (rng.standard_normal(20000) * 10 ** rng.uniform(-9, 6, 20000)).astype(np.float32),
+        np.float32([0.0, -0.0, 1.0, 65504, 65519.99, 65520, -65520, 1e9, np.inf, -np.inf,
+                    2 ** -24, 2 ** -25, 3 * 2 ** -26, 2 ** -14, 1 + 2 ** -11, 1 + 3 * 2 ** -11]),
+    ])
+    for factor in (1.0, 0.24993895, 3.5, 2 ** -7):
+        got = oracle.convert_f16(x, factor)
+        with np.errstate(over="ignore"):
+            want = (x * np.float32(factor)).astype(np.float16).view(np.uint16)
+        assert np.array_equal(got, want), factor
+    nan = oracle.convert_f16(np.float32([np.nan]), 1.0)
+    assert (nan[0] & 0x7C00) == 0x7C00 and (nan[0] & 0x03FF) != 0
+
+
+def test_fp16_range_chain_recovers_out_of_range_product():
+    """A holds outliers far beyond FP16 (so plain conversion gives Inf); the
+    scaled chain reproduces the FP64 product of the original FP32 operands
+    within the FP16 rounding of each operand: |Delta x| <= |x| (2^-11 + 2^-24)
+    + 2^-25 / sqrt(scale), and the binary32 rounding of sqrt(scale) and 1/scale."""
+    M, N, K = 6, 40, 96
+    A, B = synth.make_inputs("fp8_256", M=M, N=N, K=K)
+    A = A.copy()
+    A[1, 5] = 9.0e4
+    A[4, 17] = -7.5e4
+    A[0, 0] = 7.0e4
+    assert (oracle.convert_f16(A, 1.0) & 0x7FFF).max() == 0x7C00     # plain cast overflows
+    f, A16, B16, D, S = oracle.fp16_range_chain(A, B)
+    assert f[0] < 1
+    assert np.all(np.isfinite(oracle.fp16_decode(A16)))
+    exact = A.astype(np.float64) @ B.astype(np.float64).T
+    r = float(f[1])
+    ea = np.abs(A.astype(np.float64)) * (2 ** -11 + 2 ** -24) + 2 ** -25 / r
+    eb = np.abs(B.astype(np.float64)) * (2 ** -11 + 2 ** -24) + 2 ** -25 / r
+    bound = (ea @ np.abs(B.astype(np.float64)).T + np.abs(A.astype(np.float64)) @ eb.T + ea @ eb.T)
+    bound = bound * (1 + 2 ** -20) + 2 ** -20 * np.abs(exact)
+    assert np.all(np.abs(D - exact) <= bound)
+    # dropping the final division by scale is caught
+    assert not np.all(np.abs(D * float(f[0]) - exact) <= bound)
+
+
+def test_fp16_range_scale_bounds_products_not_operands():
+    """The page's single scale keeps every |a b| scale within 65504; one
+    operand alone still overflows once max|A| / max|B| exceeds 65504."""
+    f = oracle.fp16_range_scale(9.0e5, 4.0)
+    assert np.float64(9.0e5) * 4.0 * float(f[0]) <= 65504 * (1 + 2 ** -23)
+    assert oracle.convert_f16(np.float32([9.0e5]), f[1])[0] == 0x7C00          # +Inf
+    g = oracle.fp16_range_scale(6.0e4, 1.0)                                     # ratio < 65504
+    assert oracle.convert_f16(np.float32([6.0e4]), g[1])[0] != 0x7C00
