@@ -341,6 +341,35 @@ def kernel_cases(torch, dg):
         fn = lambda i, s: dg.dg_quantize_e4m3(x, sc, q, stream=s)  # noqa: E731
         return fn, 0.0, 5 * x.numel(), "hbm", "268 MB input > L2"
 
+    def convert16():
+        x = torch.randn((8192, 8192), device=dev)
+        f = torch.full((4,), 0.25, dtype=torch.float32, device=dev)
+        o = torch.empty((8192, 8192), dtype=torch.int16, device=dev)
+        fn = lambda i, s: dg.dg_convert_f16(x, o, f, stream=s)  # noqa: E731
+        return fn, 0.0, 6 * x.numel(), "hbm", "268 MB input > L2"
+
+    def fp16_range_chain(S):
+        # FP32 operands with values beyond FP16 range: amax of both, the
+        # dynamic-range factors, sqrt(scale) conversion of both, scaled HGEMM
+        g = torch.Generator(device=dev)
+        g.manual_seed(9)
+        A = torch.randn((S, S), device=dev, generator=g)
+        B = torch.randn((S, S), device=dev, generator=g)
+        A[0, 0] = 9.0e4
+        am_a, am_b, f = (torch.zeros(4, dtype=torch.float32, device=dev) for _ in range(3))
+        A16 = torch.empty((S, S), dtype=torch.int16, device=dev)
+        B16 = torch.empty((S, S), dtype=torch.int16, device=dev)
+        D = torch.empty((S, S), dtype=torch.bfloat16, device=dev)
+
+        def fn(i, s):
+            dg.dg_amax(A, am_a, stream=s)
+            dg.dg_amax(B, am_b, stream=s)
+            dg.dg_fp16_range_scale(am_a, am_b, f, stream=s)
+            dg.dg_convert_f16(A, A16, f[1:2], stream=s)
+            dg.dg_convert_f16(B, B16, f[1:2], stream=s)
+            dg.dg_hgemm_scaled(A16, B16, D, f[2:3], f[3:4], dg.DG_BF16, stream=s)
+        return fn, 2.0 * S ** 3, 0.0, "tensor_fp16", "FP32 operands 2 x 67 MB (> L2 together with the FP16 copies)"
+
     def moe(grouped: bool):
         # 16 experts, 8192 routed rows with a skewed load, N = 2048, K = 4096
         import synth
@@ -381,6 +410,8 @@ def kernel_cases(torch, dg):
         "fp16_hgemm_4096": lambda: hgemm(4096),
         "amax_8192sq": amax,
         "quantise_8192sq": quant,
+        "convert_f16_8192sq": convert16,
+        "fp16_range_scaled_hgemm_chain_4096": lambda: fp16_range_chain(4096),
     }
 
 

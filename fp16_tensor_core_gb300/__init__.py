@@ -19,7 +19,7 @@ __all__ = [
     "DG_ERR_CUDA", "DG_ERR_TIMEOUT", "DG_BF16", "DG_E4M3", "DG_FP16", "DgError",
     "lib", "library_path", "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm",
     "dg_fp8_gemm_amax", "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static",
-    "dg_hgemm",
+    "dg_hgemm", "dg_hgemm_scaled", "dg_fp16_range_scale", "dg_convert_f16",
     "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
     "dg_debug_skip_first_load", "dg_status_string", "dg_version", "EXPORTED_SYMBOLS",
 ]
@@ -30,7 +30,8 @@ DG_BF16, DG_E4M3, DG_FP16 = 0, 1, 2
 #: Every function include/dg.h declares.
 EXPORTED_SYMBOLS = (
     "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax",
-    "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_hgemm", "dg_gemm_plan",
+    "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_hgemm", "dg_hgemm_scaled",
+    "dg_fp16_range_scale", "dg_convert_f16", "dg_gemm_plan",
     "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
     "dg_status_string", "dg_version",
 )
@@ -78,6 +79,9 @@ def lib():
             L.dg_fp8_gemm_splitk_static.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp,
                                                      ctypes.c_int, vp, vp]
             L.dg_hgemm.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, vp]
+            L.dg_hgemm_scaled.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, ctypes.c_int, vp]
+            L.dg_fp16_range_scale.argtypes = [vp, vp, vp, vp]
+            L.dg_convert_f16.argtypes = [vp, i64, vp, vp, vp]
             L.dg_gemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(_Plan)]
             L.dg_init.argtypes = []
@@ -91,7 +95,8 @@ def lib():
             L.dg_version.argtypes = []
             for name in ("dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm",
                          "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_gemm_plan", "dg_init",
-                         "dg_sync_status", "dg_version"):
+                         "dg_sync_status", "dg_version", "dg_hgemm_scaled", "dg_fp16_range_scale",
+                         "dg_convert_f16"):
                 getattr(L, name).restype = st
             _lib = L
     return _lib
@@ -209,6 +214,29 @@ def dg_hgemm(A, B, D, out=DG_FP16, stream=None, M=None, N=None, K=None) -> None:
         N = B.shape[0]
     _check(lib().dg_hgemm(_ptr(A), _ptr(B), _ptr(D), M, N, K, int(out), _stream(stream)),
            "dg_hgemm")
+
+
+def dg_hgemm_scaled(A, B, D, scale_a, scale_b, out=DG_BF16, stream=None, M=None, N=None,
+                    K=None) -> None:
+    """D = out(scale_a * scale_b * A @ B^T), FP16 operands, FP32 accumulation."""
+    if M is None:
+        M, K = A.shape
+        N = B.shape[0]
+    _check(lib().dg_hgemm_scaled(_ptr(A), _ptr(B), _ptr(D), M, N, K, _ptr(scale_a),
+                                 _ptr(scale_b), int(out), _stream(stream)), "dg_hgemm_scaled")
+
+
+def dg_fp16_range_scale(amax_a, amax_b, factors, stream=None) -> None:
+    """factors[0..3] = scale, sqrt(scale), 1/scale, 1 with
+    scale = min(1, 65504 / (amax_a * amax_b)) (FP16 dynamic-range scaling)."""
+    _check(lib().dg_fp16_range_scale(_ptr(amax_a), _ptr(amax_b), _ptr(factors),
+                                     _stream(stream)), "dg_fp16_range_scale")
+
+
+def dg_convert_f16(x, out, factor=None, stream=None) -> None:
+    """out = fp16_rn(x * factor[0]) elementwise (binary16 bit patterns)."""
+    _check(lib().dg_convert_f16(_ptr(x), x.numel(), _ptr(factor), _ptr(out), _stream(stream)),
+           "dg_convert_f16")
 
 
 def dg_gemm_plan(M, N, K, in_dtype=DG_E4M3, out_dtype=DG_BF16, sm_count=0) -> dict:

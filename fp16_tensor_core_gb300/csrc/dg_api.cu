@@ -375,6 +375,52 @@ dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M, int
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
+dg_status dg_hgemm_scaled(const uint16_t* A, const uint16_t* B, void* D, int64_t M, int64_t N,
+                          int64_t K, const float* scale_a, const float* scale_b, dg_dtype out,
+                          dg_stream_t stream) {
+    dg_status rc = check_sizes(M, N, K);
+    if (rc != DG_OK) return rc;
+    if (out != DG_FP16 && out != DG_BF16) return DG_ERR_INVALID_VALUE;
+    if (scale_a == nullptr || scale_b == nullptr) return DG_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(scale_a) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(scale_b) & 3u) != 0)
+        return DG_ERR_MISALIGNED;
+    if (M > 0 && N > 0) {
+        if (D == nullptr) return DG_ERR_INVALID_VALUE;
+        if (K > 0 && (A == nullptr || B == nullptr)) return DG_ERR_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0)
+            return DG_ERR_MISALIGNED;
+    }
+    return run_gemm(A, B, D, M, N, K, true, scale_a, scale_b, nullptr, out,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_fp16_range_scale(const float* amax_a, const float* amax_b, float* factors,
+                              dg_stream_t stream) {
+    if (amax_a == nullptr || amax_b == nullptr || factors == nullptr) return DG_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(amax_a) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(amax_b) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(factors) & 15u) != 0)
+        return DG_ERR_MISALIGNED;
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_fp16_range_scale(amax_a, amax_b, factors,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_convert_f16(const float* x, int64_t n, const float* factor, uint16_t* out,
+                         dg_stream_t stream) {
+    if (n < 0 || (n > 0 && (x == nullptr || out == nullptr))) return DG_ERR_INVALID_VALUE;
+    if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(factor) & 3u) != 0)
+        return DG_ERR_MISALIGNED;
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_convert_f16(x, n, factor, out, st->sm_count,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dg_status dg_gemm_plan(int64_t M, int64_t N, int64_t K, dg_dtype in, dg_dtype out,
                        int sm_count, dg_plan* plan) {
     if (plan == nullptr) return DG_ERR_INVALID_VALUE;

@@ -73,6 +73,12 @@ cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N,
                         int K, bool fp16_in, const float* sa, const float* sb,
                         const float* sd, int out_kind, uint32_t* amax_out,
                         cudaStream_t s);
+// FP16 dynamic-range scaling: out[0..3] = scale, sqrt(scale), 1/scale, 1
+// (one-thread kernel), and out_i = fp16_rn(x_i * factor).
+cudaError_t launch_fp16_range_scale(const float* amax_a, const float* amax_b, float* out,
+                                    cudaStream_t s);
+cudaError_t launch_convert_f16(const float* x, int64_t n, const float* factor, uint16_t* out,
+                               int sm_count, cudaStream_t s);
 // Sets *bits = 0 on stream s (one-thread kernel).
 cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s);
 

@@ -1,9 +1,13 @@
-// k_scale.cu -- per-tensor amax, scale and the E4M3 quantiser.
+// k_scale.cu -- per-tensor amax, scale, the E4M3 quantiser, and the FP16
+// dynamic-range scaling factors and conversion.
 //
 // [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南".
 // §3.2: one scale per tensor, scale = max |x| / 448; §4.3: the quantiser
-// fp8 = clamp(round(x / scale), -448, 448).  Both kernels are HBM streams:
-// amax reads 4 B per element, the quantiser reads 4 B and writes 1 B.
+// fp8 = clamp(round(x / scale), -448, 448).  [DG-FP16] = the DeepGEMM
+// FP16/WMMA deep-dive page, §3.3: scale = min(1, 65504 / (max|A| max|B|)),
+// operands times sqrt(scale) into FP16, result divided by scale.  The
+// streaming kernels are bound by HBM: amax reads 4 B per element, the
+// quantiser reads 4 B and writes 1 B, the FP16 conversion 4 B and 2 B.
 #include <cuda_runtime.h>
 
 #include "dg_internal.h"
@@ -143,7 +147,84 @@ quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict_
     }
 }
 
+// [DG-FP16] §3.3 factors: out = {scale, sqrt(scale), 1/scale, 1}.  The
+// product of the two maxima and the quotient are formed in binary64 (no
+// binary32 overflow) and rounded once; sqrt and the reciprocal are taken in
+// binary64 from the binary32 scale and rounded once, which for these two
+// operations is the correctly rounded binary32 result.
+__global__ void fp16_range_scale_kernel(const float* __restrict__ amax_a,
+                                        const float* __restrict__ amax_b,
+                                        float* __restrict__ out) {
+    pdl_wait();
+    const float a = *amax_a, b = *amax_b;
+    float sc;
+    if (isnan(a) || isnan(b)) {
+        sc = __int_as_float(0x7FC00000);
+    } else {
+        const double q = 65504.0 / (static_cast<double>(a) * static_cast<double>(b));
+        sc = __double2float_rn(q < 1.0 ? q : 1.0);
+    }
+    out[0] = sc;
+    out[1] = __double2float_rn(sqrt(static_cast<double>(sc)));
+    out[2] = __double2float_rn(1.0 / static_cast<double>(sc));
+    out[3] = 1.0f;
+}
+
+__device__ __forceinline__ uint2 half4(float4 v, float f) {
+    return make_uint2(f32x2_to_f16x2(__fmul_rn(v.x, f), __fmul_rn(v.y, f)),
+                      f32x2_to_f16x2(__fmul_rn(v.z, f), __fmul_rn(v.w, f)));
+}
+
+// out_i = fp16_rn(fl32(x_i * factor)): each warp converts 512-element slabs
+// (four 512-byte loads, four 256-byte stores per slab); the ragged tail is
+// converted by block 0.
+__global__ void __launch_bounds__(kQuantThreads)
+convert_f16_kernel(const float* __restrict__ x, int64_t n, const float* __restrict__ factor_p,
+                   uint16_t* __restrict__ out) {
+    pdl_wait();
+    const float f = factor_p != nullptr ? *factor_p : 1.0f;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t nslab = n >> 9;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    uint2* o4 = reinterpret_cast<uint2*>(out);
+    for (int64_t slab = warp; slab < nslab; slab += nwarps) {
+        const int64_t b = slab * 128 + lane;
+        const float4 v0 = ld_stream_f4(x4 + b);
+        const float4 v1 = ld_stream_f4(x4 + b + 32);
+        const float4 v2 = ld_stream_f4(x4 + b + 64);
+        const float4 v3 = ld_stream_f4(x4 + b + 96);
+        o4[b] = half4(v0, f);
+        o4[b + 32] = half4(v1, f);
+        o4[b + 64] = half4(v2, f);
+        o4[b + 96] = half4(v3, f);
+    }
+    if (blockIdx.x == 0) {
+        for (int64_t i = (nslab << 9) + threadIdx.x; i < n; i += blockDim.x)
+            out[i] = static_cast<uint16_t>(f32x2_to_f16x2(__fmul_rn(x[i], f), 0.0f) & 0xFFFFu);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_fp16_range_scale(const float* amax_a, const float* amax_b, float* out,
+                                    cudaStream_t s) {
+    return launch_kernel(fp16_range_scale_kernel, dim3(1), dim3(1), 0, s, amax_a, amax_b, out);
+}
+
+cudaError_t launch_convert_f16(const float* x, int64_t n, const float* factor, uint16_t* out,
+                               int sm_count, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t slabs = n >> 9;
+    const int warps_per_block = kQuantThreads / 32;
+    int64_t blocks = (slabs + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return launch_kernel(convert_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads),
+                         0, s, x, n, factor, out);
+}
 
 cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
                         int sm_count, cudaStream_t s, bool pow2) {

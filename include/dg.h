@@ -197,6 +197,38 @@ dg_status dg_fp8_gemm_splitk_static(const uint8_t* A, const uint8_t* B, void* D,
 dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M,
                    int64_t N, int64_t K, dg_dtype out, dg_stream_t stream);
 
+/* HGEMM with per-tensor scales in the epilogue: D = out(scale_a * scale_b *
+ * A * B^T), FP32 accumulation.  As dg_hgemm otherwise; scale_a, scale_b are
+ * FP32 device scalars (both required, 4-byte aligned).  With the factors of
+ * dg_fp16_range_scale (scale_a = &factors[2], scale_b = &factors[3]) this is
+ * the last step of [DG-FP16] §3.3's dynamic-range scaling: the result is
+ * divided by the scale the operands were multiplied with (as 1/scale). */
+dg_status dg_hgemm_scaled(const uint16_t* A, const uint16_t* B, void* D,
+                          int64_t M, int64_t N, int64_t K,
+                          const float* scale_a, const float* scale_b,
+                          dg_dtype out, dg_stream_t stream);
+
+/* [DG-FP16] §3.3 dynamic-range-aware scaling for FP16 operands: from the
+ * two maxima (e.g. dg_amax of A and of B, FP32 device scalars) it writes
+ * factors[0..3] = { scale, sqrt(scale), 1/scale, 1 } with
+ * scale = min(1, 65504 / (amax_a * amax_b)): the product and quotient are
+ * formed in binary64 and rounded once to binary32; sqrt and the reciprocal
+ * are correctly rounded binary32 values of that scale.  1 when a maximum is
+ * 0; NaN when one is NaN.  factors: device, 4 floats, 16-byte aligned,
+ * caller-owned.  The scale bounds every |a * b| * scale by 65504; a single
+ * operand value still overflows FP16 after the sqrt(scale) multiply if
+ * max|A| / max|B| (or its inverse) exceeds 65504. */
+dg_status dg_fp16_range_scale(const float* amax_a, const float* amax_b,
+                              float* factors, dg_stream_t stream);
+
+/* out[i] = fp16_rn(fl32(x[i] * factor[0])), IEEE round-to-nearest-even,
+ * overflow to +-Inf, NaN stays NaN.  x: n FP32, out: n binary16 bit
+ * patterns, both device, 16-byte aligned, caller-owned; factor: FP32 device
+ * scalar (NULL = 1), e.g. &factors[1] of dg_fp16_range_scale.  An HBM
+ * stream (6 B per element). */
+dg_status dg_convert_f16(const float* x, int64_t n, const float* factor,
+                         uint16_t* out, dg_stream_t stream);
+
 /* Tile / path selection for a GEMM shape, host only (launches nothing).
  * [FP8-guide] §2.2, §3.1, §3.3 (per-shape tile choice, smaller tiles where
  * edge waste is high) and [HGEMM-L2] §3.1-§3.3 (tile and stage count chosen

@@ -134,6 +134,24 @@ def test_splitk_static_argument_errors(L):
     assert call(M=0) == dg.DG_OK and call(N=0) == dg.DG_OK       # empty: nothing launched
 
 
+def test_fp16_range_argument_errors(L):
+    assert L.dg_fp16_range_scale(None, FAKE, FAKE, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_fp16_range_scale(FAKE, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_fp16_range_scale(FAKE + 2, FAKE, FAKE, None) == dg.DG_ERR_MISALIGNED
+    assert L.dg_fp16_range_scale(FAKE, FAKE, FAKE + 4, None) == dg.DG_ERR_MISALIGNED  # 16 B
+    assert L.dg_convert_f16(FAKE, -1, None, FAKE, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_convert_f16(None, 8, None, FAKE, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_convert_f16(FAKE + 4, 8, None, FAKE, None) == dg.DG_ERR_MISALIGNED
+    assert L.dg_convert_f16(FAKE, 8, None, FAKE + 8, None) == dg.DG_ERR_MISALIGNED
+    assert L.dg_convert_f16(FAKE, 8, FAKE + 1, FAKE, None) == dg.DG_ERR_MISALIGNED
+    h = (FAKE, FAKE, FAKE, 8, 8, 16)
+    assert L.dg_hgemm_scaled(*h, None, FAKE, dg.DG_BF16, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_hgemm_scaled(*h, FAKE, FAKE, dg.DG_E4M3, None) == dg.DG_ERR_INVALID_VALUE
+    assert L.dg_hgemm_scaled(*h, FAKE + 2, FAKE, dg.DG_BF16, None) == dg.DG_ERR_MISALIGNED
+    assert L.dg_hgemm_scaled(FAKE, FAKE, FAKE, 8, 8, 12, FAKE, FAKE, dg.DG_BF16,
+                             None) == dg.DG_ERR_MISALIGNED
+
+
 def test_moe_group_sizes_recipe():
     import synth
     s = synth.moe_group_sizes(3, 16, 8192, empty=2)

@@ -1,0 +1,100 @@
+"""FP16 dynamic-range scaling on the GPU ([DG-FP16] = the DeepGEMM FP16/WMMA
+deep-dive page, §3.3): dg_amax of A and B, dg_fp16_range_scale, dg_convert_f16
+of both operands with sqrt(scale), dg_hgemm_scaled with 1/scale.  The
+factors and the FP16 operands are bit-exact against the oracle; the GEMM is
+within the parity bound of the oracle's exact product of those operands."""
+import numpy as np
+import pytest
+import torch
+
+import fp16_tensor_core_gb300 as dg
+import oracle
+import synth
+from _parity import bf16_bits_to_f64, check_bf16_like, dev, scalar
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from fp16_tensor_core_gb300 import build
+    build.build()
+    dg.dg_init()
+    yield
+    assert dg.dg_sync_status() == dg.DG_OK
+
+
+def gpu_factors(a, b):
+    da, db = dev(np.float32([a, 0, 0, 0])), dev(np.float32([b, 0, 0, 0]))
+    f = scalar()
+    dg.dg_fp16_range_scale(da, db, f)
+    assert dg.dg_sync_status() == dg.DG_OK
+    return f.cpu().numpy()
+
+
+def test_factors_bit_exact():
+    rng = np.random.default_rng(8)
+    pairs = [(1.0, 1.0), (256.0, 255.875), (256.0, 256.0), (1024.0, 1024.0), (0.0, 3.0),
+             (3e38, 3e38), (9.0e5, 4.0), (7.0e4, 3.9)]
+    pairs += list(zip(10 ** rng.uniform(-4, 14, 200), 10 ** rng.uniform(-4, 14, 200)))
+    for a, b in pairs:
+        got = gpu_factors(np.float32(a), np.float32(b))
+        want = oracle.fp16_range_scale(np.float32(a), np.float32(b))
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (a, b, got, want)
+    got = gpu_factors(np.nan, 1.0)
+    assert np.isnan(got[0]) and np.isnan(got[1]) and np.isnan(got[2]) and got[3] == 1
+
+
+@pytest.mark.parametrize("n", [1, 511, 512, 513, 4096 * 3 + 17, 1 << 20])
+def test_convert_bit_exact(n):
+    x = (synth.normal_f32(11, (n,)) * np.float32(3e3)).astype(np.float32)
+    for factor in (1.0, 0.24993895, 37.0):
+        f = dev(np.float32([factor, 0, 0, 0]))
+        out = torch.empty(n, dtype=torch.int16, device="cuda")
+        dg.dg_convert_f16(dev(x), out, f)
+        assert dg.dg_sync_status() == dg.DG_OK
+        got = out.cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, oracle.convert_f16(x, factor)), (n, factor)
+
+
+def test_convert_special_values():
+    x = np.float32([0.0, -0.0, 65504, 65519.99, 65520, -65520, 1e30, -np.inf, np.inf,
+                    2 ** -24, 2 ** -25, 3 * 2 ** -26, 1 + 2 ** -11, 1 + 3 * 2 ** -11, np.nan, 7])
+    out = torch.empty(x.size, dtype=torch.int16, device="cuda")
+    dg.dg_convert_f16(dev(x), out)       # factor NULL = 1
+    assert dg.dg_sync_status() == dg.DG_OK
+    got = out.cpu().numpy().view(np.uint16)
+    want = oracle.convert_f16(x, 1.0)
+    is_nan = lambda h: ((h & 0x7C00) == 0x7C00) & ((h & 0x03FF) != 0)  # noqa: E731
+    assert np.array_equal(is_nan(got), is_nan(want))
+    assert np.array_equal(got[~is_nan(want)], want[~is_nan(want)])
+
+
+@pytest.mark.parametrize("M,N,K", [(2, 300, 512), (9, 1000, 1040), (129, 520, 1040), (384, 1000, 2048)])
+def test_range_scaled_hgemm_chain(M, N, K):
+    """Operands with FP16-overflowing outliers: the whole chain on the GPU
+    against the oracle's chain (GEMV, split-K, single-CTA and pair paths)."""
+    A, B = synth.make_inputs("fp8_256", M=M, N=N, K=K)
+    A = A.copy()
+    A[0, 3] = 9.0e4
+    A[M - 1, K - 1] = -7.0e4
+    dA, dB = dev(A), dev(B)
+    am_a, am_b, f = scalar(), scalar(), scalar()
+    dg.dg_amax(dA, am_a)
+    dg.dg_amax(dB, am_b)
+    dg.dg_fp16_range_scale(am_a, am_b, f)
+    A16 = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    B16 = torch.empty((N, K), dtype=torch.int16, device="cuda")
+    dg.dg_convert_f16(dA, A16, f[1:2])
+    dg.dg_convert_f16(dB, B16, f[1:2])
+    D = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    dg.dg_hgemm_scaled(A16, B16, D, f[2:3], f[3:4], dg.DG_BF16)
+    assert dg.dg_sync_status() == dg.DG_OK
+    fr, A16r, B16r, Dr, S = oracle.fp16_range_chain(A, B)
+    assert np.array_equal(f.cpu().numpy().view(np.uint32), fr.view(np.uint32))
+    assert np.array_equal(A16.cpu().numpy().view(np.uint16), A16r)
+    assert np.array_equal(B16.cpu().numpy().view(np.uint16), B16r)
+    R, _ = oracle.hgemm(A16r, B16r)
+    check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16)), R, S,
+                    float(fr[2]), 1.0, "range-scaled HGEMM")
+    assert np.all(np.isfinite(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16))))
