@@ -341,6 +341,15 @@ def kernel_cases(torch, dg):
         fn = lambda i, s: dg.dg_quantize_e4m3(x, sc, q, stream=s)  # noqa: E731
         return fn, 0.0, 5 * x.numel(), "hbm", "268 MB input > L2"
 
+    def quant_amax():
+        x = torch.randn((8192, 8192), device=dev)
+        sc = torch.full((4,), 0.01, dtype=torch.float32, device=dev)
+        am = torch.zeros(4, dtype=torch.float32, device=dev)
+        nx = torch.zeros(4, dtype=torch.float32, device=dev)
+        q = torch.empty((8192, 8192), dtype=torch.uint8, device=dev)
+        fn = lambda i, s: dg.dg_quantize_e4m3_amax(x, sc, q, am, nx, stream=s)  # noqa: E731
+        return fn, 0.0, 5 * x.numel(), "hbm", "268 MB input > L2"
+
     def convert16():
         x = torch.randn((8192, 8192), device=dev)
         f = torch.full((4,), 0.25, dtype=torch.float32, device=dev)
@@ -410,6 +419,7 @@ def kernel_cases(torch, dg):
         "fp16_hgemm_4096": lambda: hgemm(4096),
         "amax_8192sq": amax,
         "quantise_8192sq": quant,
+        "quantise_with_amax_8192sq": quant_amax,
         "convert_f16_8192sq": convert16,
         "fp16_range_scaled_hgemm_chain_4096": lambda: fp16_range_chain(4096),
     }

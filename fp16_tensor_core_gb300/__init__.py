@@ -17,7 +17,8 @@ import torch
 __all__ = [
     "DG_OK", "DG_ERR_INVALID_VALUE", "DG_ERR_MISALIGNED", "DG_ERR_UNSUPPORTED",
     "DG_ERR_CUDA", "DG_ERR_TIMEOUT", "DG_BF16", "DG_E4M3", "DG_FP16", "DgError",
-    "lib", "library_path", "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm",
+    "lib", "library_path", "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3",
+    "dg_quantize_e4m3_amax", "dg_fp8_gemm",
     "dg_fp8_gemm_amax", "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static",
     "dg_hgemm", "dg_hgemm_scaled", "dg_fp16_range_scale", "dg_convert_f16",
     "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
@@ -29,7 +30,8 @@ DG_BF16, DG_E4M3, DG_FP16 = 0, 1, 2
 
 #: Every function include/dg.h declares.
 EXPORTED_SYMBOLS = (
-    "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax",
+    "dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_quantize_e4m3_amax", "dg_fp8_gemm",
+    "dg_fp8_gemm_amax",
     "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_hgemm", "dg_hgemm_scaled",
     "dg_fp16_range_scale", "dg_convert_f16", "dg_gemm_plan",
     "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
@@ -71,6 +73,7 @@ def lib():
             L.dg_amax.argtypes = [vp, i64, vp, vp, vp]
             L.dg_amax_pow2.argtypes = [vp, i64, vp, vp, vp]
             L.dg_quantize_e4m3.argtypes = [vp, i64, vp, vp, vp]
+            L.dg_quantize_e4m3_amax.argtypes = [vp, i64, vp, vp, vp, vp, vp]
             L.dg_fp8_gemm.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, ctypes.c_int, vp]
             L.dg_fp8_gemm_amax.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, ctypes.c_int,
                                            vp, vp]
@@ -96,7 +99,7 @@ def lib():
             for name in ("dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm",
                          "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_gemm_plan", "dg_init",
                          "dg_sync_status", "dg_version", "dg_hgemm_scaled", "dg_fp16_range_scale",
-                         "dg_convert_f16"):
+                         "dg_convert_f16", "dg_quantize_e4m3_amax"):
                 getattr(L, name).restype = st
             _lib = L
     return _lib
@@ -157,6 +160,14 @@ def dg_quantize_e4m3(x, scale, q, stream=None) -> None:
         raise ValueError("q must have as many elements as x")
     _check(lib().dg_quantize_e4m3(_ptr(x), x.numel(), _ptr(scale), _ptr(q), _stream(stream)),
            "dg_quantize_e4m3")
+
+
+def dg_quantize_e4m3_amax(x, scale, q, amax_out, next_scale_out=None, stream=None) -> None:
+    """q = E4M3(x / scale[0]) and amax_out[0] = max |x| in one pass; optionally
+    next_scale_out[0] = amax / 448 (delayed scaling)."""
+    _check(lib().dg_quantize_e4m3_amax(_ptr(x), x.numel(), _ptr(scale), _ptr(q), _ptr(amax_out),
+                                       _ptr(next_scale_out), _stream(stream)),
+           "dg_quantize_e4m3_amax")
 
 
 def dg_fp8_gemm(A, B, D, scale_a, scale_b, scale_d=None, out=DG_BF16, stream=None,

@@ -266,6 +266,24 @@ dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dg_status dg_quantize_e4m3_amax(const float* x, int64_t n, const float* scale, uint8_t* q,
+                                float* amax_out, float* next_scale_out, dg_stream_t stream) {
+    if (n < 0 || scale == nullptr || amax_out == nullptr ||
+        (n > 0 && (x == nullptr || q == nullptr)))
+        return DG_ERR_INVALID_VALUE;
+    if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(amax_out) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(next_scale_out) & 3u) != 0)
+        return DG_ERR_MISALIGNED;
+    if (amax_out == scale) return DG_ERR_INVALID_VALUE;   // zeroed before the scale is read
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_quantize_e4m3_amax(x, n, scale, q, amax_out, next_scale_out,
+                                               st->sm_count,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M, int64_t N,
                       int64_t K, const float* scale_a, const float* scale_b,
                       const float* scale_d, dg_dtype out, dg_stream_t stream) {

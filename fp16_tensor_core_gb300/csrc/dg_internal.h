@@ -73,6 +73,11 @@ cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N,
                         int K, bool fp16_in, const float* sa, const float* sb,
                         const float* sd, int out_kind, uint32_t* amax_out,
                         cudaStream_t s);
+// Quantise with a given scale and record max |x| (and optionally the next
+// scale = amax / 448) in the same pass over x.
+cudaError_t launch_quantize_e4m3_amax(const float* x, int64_t n, const float* scale, uint8_t* q,
+                                      float* amax_out, float* next_scale_out, int sm_count,
+                                      cudaStream_t s);
 // FP16 dynamic-range scaling: out[0..3] = scale, sqrt(scale), 1/scale, 1
 // (one-thread kernel), and out_i = fp16_rn(x_i * factor).
 cudaError_t launch_fp16_range_scale(const float* amax_a, const float* amax_b, float* out,

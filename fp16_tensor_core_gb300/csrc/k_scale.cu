@@ -118,9 +118,12 @@ __device__ __forceinline__ uint32_t quant4(float4 v, float s) {
 // Each warp iteration handles 512 consecutive elements: four fully coalesced
 // 512-byte loads (lane j reads float4 j, j+32, j+64, j+96 of the slab) and
 // four 128-byte stores of packed codes.
+// kAmax: also the running max |x| (ordered bits, NaN above every number)
+// into *amax_bits, for the scale of the next call (delayed scaling).
+template <bool kAmax>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict__ scale_p,
-                uint8_t* __restrict__ q) {
+                uint8_t* __restrict__ q, uint32_t* __restrict__ amax_bits) {
     pdl_wait();
     const float s = *scale_p;
     const int lane = threadIdx.x & 31;
@@ -129,6 +132,7 @@ quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict_
     const int64_t nslab = n >> 9;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     uint32_t* q4 = reinterpret_cast<uint32_t*>(q);
+    uint32_t m = 0u;
     for (int64_t slab = warp; slab < nslab; slab += nwarps) {
         const int64_t b = slab * 128 + lane;
         const float4 v0 = ld_stream_f4(x4 + b);
@@ -139,11 +143,28 @@ quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict_
         q4[b + 32] = quant4(v1, s);
         q4[b + 64] = quant4(v2, s);
         q4[b + 96] = quant4(v3, s);
+        if constexpr (kAmax)
+            m = max(m, max(max(abs_bits4(v0), abs_bits4(v1)), max(abs_bits4(v2), abs_bits4(v3))));
     }
     // Ragged tail (< 512 elements): one element per thread of block 0.
     if (blockIdx.x == 0) {
-        for (int64_t i = (nslab << 9) + threadIdx.x; i < n; i += blockDim.x)
-            q[i] = static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(x[i], s), 0.0f) & 0xFFu);
+        for (int64_t i = (nslab << 9) + threadIdx.x; i < n; i += blockDim.x) {
+            const float v = x[i];
+            q[i] = static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(v, s), 0.0f) & 0xFFu);
+            if constexpr (kAmax) m = max(m, abs_bits(v));
+        }
+    }
+    if constexpr (kAmax) {
+        __shared__ uint32_t partial[kQuantThreads / 32];
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        const int w = threadIdx.x >> 5;
+        if (lane == 0) partial[w] = m;
+        __syncthreads();
+        if (w == 0) {
+            m = lane < kQuantThreads / 32 ? partial[lane] : 0u;
+            m = __reduce_max_sync(0xFFFFFFFFu, m);
+            if (lane == 0 && m != 0u) atomicMax(amax_bits, m);
+        }
     }
 }
 
@@ -259,8 +280,31 @@ cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale, 
     const int64_t cap = static_cast<int64_t>(sm_count) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    return launch_kernel(quantize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads), 0,
-                         s, x, n, scale, q);
+    return launch_kernel(quantize_kernel<false>, dim3(static_cast<unsigned>(blocks)),
+                         dim3(kQuantThreads), 0, s, x, n, scale, q, static_cast<uint32_t*>(nullptr));
+}
+
+cudaError_t launch_quantize_e4m3_amax(const float* x, int64_t n, const float* scale, uint8_t* q,
+                                      float* amax_out, float* next_scale_out, int sm_count,
+                                      cudaStream_t s) {
+    uint32_t* bits = reinterpret_cast<uint32_t*>(amax_out);
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
+    if (e != cudaSuccess) return e;
+    if (n > 0) {
+        const int64_t slabs = n >> 9;
+        const int warps_per_block = kQuantThreads / 32;
+        int64_t blocks = (slabs + warps_per_block - 1) / warps_per_block;
+        const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        e = launch_kernel(quantize_kernel<true>, dim3(static_cast<unsigned>(blocks)),
+                          dim3(kQuantThreads), 0, s, x, n, scale, q, bits);
+        if (e != cudaSuccess) return e;
+    }
+    if (next_scale_out != nullptr)
+        e = launch_kernel(scale_kernel, dim3(1), dim3(1), 0, s,
+                          static_cast<const float*>(amax_out), next_scale_out);
+    return e;
 }
 
 }  // namespace dg

@@ -163,6 +163,21 @@ dg_status dg_fp8_gemm_grouped(const uint8_t* A, const uint8_t* B, void* D,
                               const float* scale_d, dg_dtype out,
                               dg_stream_t stream);
 
+/* dg_quantize_e4m3 with a scale recorded earlier (delayed scaling), fused
+ * with the amax of this tensor for the next call: one pass over x writes
+ * q[i] = e4m3(fl32(x[i] / scale[0])) and amax_out[0] = max |x| (NaN
+ * propagates), then, if next_scale_out is not NULL, next_scale_out[0] =
+ * amax / 448 (1 when amax == 0) — the same rules as dg_amax and
+ * dg_quantize_e4m3.  [FP8-guide] §3.2: the calibration run records each
+ * tensor's largest magnitude and the scale comes from it; here the record
+ * of one call scales the next, so amax and quantisation share one read.
+ * next_scale_out may be the same buffer as scale (it is written after the
+ * quantiser has finished); amax_out must not be scale.  Pointers as
+ * dg_quantize_e4m3 and dg_amax. */
+dg_status dg_quantize_e4m3_amax(const float* x, int64_t n, const float* scale,
+                                uint8_t* q, float* amax_out,
+                                float* next_scale_out, dg_stream_t stream);
+
 /* dg_fp8_gemm for skinny shapes (1 <= M <= 16) that never allocates: the
  * split-K tensor-core kernel (plan path 4) runs with its workspace in fixed
  * static device arrays of the library (2.5 MiB of FP32 partial tiles and

@@ -152,6 +152,17 @@ def test_fp16_range_argument_errors(L):
                              None) == dg.DG_ERR_MISALIGNED
 
 
+def test_quantize_amax_argument_errors(L):
+    q = L.dg_quantize_e4m3_amax
+    assert q(FAKE, 10, None, FAKE, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE    # no scale
+    assert q(FAKE, 10, FAKE, FAKE, None, None, None) == dg.DG_ERR_INVALID_VALUE    # no amax
+    assert q(FAKE, -1, FAKE, FAKE, FAKE + 64, None, None) == dg.DG_ERR_INVALID_VALUE
+    assert q(FAKE, 10, FAKE, FAKE, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE    # amax is scale
+    assert q(FAKE + 4, 10, FAKE, FAKE, FAKE + 64, None, None) == dg.DG_ERR_MISALIGNED
+    assert q(FAKE, 10, FAKE, FAKE, FAKE + 66, None, None) == dg.DG_ERR_MISALIGNED
+    assert q(FAKE, 10, FAKE, FAKE, FAKE + 64, FAKE + 1, None) == dg.DG_ERR_MISALIGNED
+
+
 def test_moe_group_sizes_recipe():
     import synth
     s = synth.moe_group_sizes(3, 16, 8192, empty=2)

@@ -110,3 +110,40 @@ def test_empty_and_k_zero_give_zero_amax():
     dg.dg_fp8_gemm_amax(A, B, D, s, s, None, dg.DG_BF16, am, M=5, N=7, K=0)
     assert dg.dg_sync_status() == dg.DG_OK
     assert am[0].item() == 0.0 and torch.all(D == 0)
+
+
+@pytest.mark.parametrize("n", [0, 1, 511, 512, 513, 4096 * 5 + 3, 1 << 21])
+def test_quantise_with_recorded_scale_and_amax_in_one_pass(n):
+    """dg_quantize_e4m3_amax: codes with the given (earlier) scale, this
+    tensor's amax and the next scale, all bit-exact against the oracle."""
+    x = synth.make_inputs("fp8_sweep_m65", M=1, N=1, K=max(n, 1))[0].reshape(-1)[:n].copy()
+    dx = torch.from_numpy(x).cuda() if n else torch.empty(0, dtype=torch.float32, device="cuda")
+    scale = scalar()
+    scale[0] = 0.0123
+    amax, nxt = scalar(), scalar()
+    amax[0] = 99.0     # stale: the call must reset it
+    q = torch.empty(n, dtype=torch.uint8, device="cuda")
+    dg.dg_quantize_e4m3_amax(dx, scale, q, amax, nxt)
+    assert dg.dg_sync_status() == dg.DG_OK
+    assert np.array_equal(q.cpu().numpy(), oracle.quantize_e4m3(x, np.float32(0.0123)))
+    a_ref = oracle.amax(x) if n else np.float32(0.0)
+    assert np.float32(amax[0].item()).view(np.uint32) == np.float32(a_ref).view(np.uint32)
+    s_ref = oracle.scale_from_amax(a_ref)
+    assert np.float32(nxt[0].item()).view(np.uint32) == np.float32(s_ref).view(np.uint32)
+
+
+def test_quantise_amax_updates_scale_in_place_and_propagates_nan():
+    x = synth.normal_f32(21, (100000,))
+    scale = scalar()
+    scale[0] = 0.01
+    amax = scalar()
+    q1 = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+    dg.dg_quantize_e4m3_amax(torch.from_numpy(x).cuda(), scale, q1, amax, scale)   # next scale in place
+    assert dg.dg_sync_status() == dg.DG_OK
+    assert np.array_equal(q1.cpu().numpy(), oracle.quantize_e4m3(x, np.float32(0.01)))
+    assert scale[0].item() == float(oracle.scale_from_amax(oracle.amax(x)))
+    y = x.copy()
+    y[777] = np.nan
+    dg.dg_quantize_e4m3_amax(torch.from_numpy(y).cuda(), scale, q1, amax)
+    assert dg.dg_sync_status() == dg.DG_OK
+    assert np.isnan(amax[0].item())
