@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <climits>
+#include <unordered_map>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -20,6 +21,22 @@ constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 DeviceState g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {};
+
+// Split-K workspaces per device, one per stream that has run a split-K GEMM
+// (calls on different streams may execute concurrently, so they must not
+// share partial slots and arrival counters).  The first such stream uses
+// the workspace allocated with the device state.
+struct SplitkWs {
+    float* partials;
+    uint32_t* counts;
+};
+std::mutex g_ws_mu[kMaxDevices];
+std::unordered_map<cudaStream_t, SplitkWs> g_ws[kMaxDevices];
+
+size_t splitk_partial_bytes(int sm_count) {
+    return sizeof(float) * 2 * static_cast<size_t>(sm_count) * kSkinnyMaxM * kSkinnyTileRows;
+}
+constexpr size_t kSplitkCountBytes = sizeof(uint32_t) * kSkinnyMaxTiles;
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_skip_first_load{0};
@@ -66,9 +83,8 @@ dg_status current_device_state(DeviceState** out) {
         st.status = static_cast<uint32_t*>(p);
         // Split-K workspace (fixed size, so that nothing is allocated later,
         // e.g. while a stream is being captured into a graph).
-        const size_t part_bytes = sizeof(float) * 2 * static_cast<size_t>(st.sm_count) *
-                                  kSkinnyMaxM * kSkinnyTileRows;
-        const size_t count_bytes = sizeof(uint32_t) * kSkinnyMaxTiles;
+        const size_t part_bytes = splitk_partial_bytes(st.sm_count);
+        const size_t count_bytes = kSplitkCountBytes;
         void* w = nullptr;
         if (cudaMalloc(&w, part_bytes + count_bytes) != cudaSuccess) {
             cudaFree(p);
@@ -164,6 +180,42 @@ dg_status check_sizes(int64_t M, int64_t N, int64_t K) {
     return DG_OK;
 }
 
+// The split-K workspace of `s` on the device of `st` (created on the first
+// split-K call on a stream other than the first one; never while the stream
+// is being captured into a graph).
+dg_status splitk_workspace(const DeviceState* st, cudaStream_t s, SplitkWs* out) {
+    std::lock_guard<std::mutex> lk(g_ws_mu[st->device]);
+    auto& map = g_ws[st->device];
+    auto it = map.find(s);
+    if (it != map.end()) {
+        *out = it->second;
+        return DG_OK;
+    }
+    if (map.empty()) {
+        map[s] = SplitkWs{st->splitk_partials, st->splitk_counts};
+        *out = map[s];
+        return DG_OK;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return DG_ERR_UNSUPPORTED;
+    const size_t part_bytes = splitk_partial_bytes(st->sm_count);
+    void* w = nullptr;
+    if (cudaMalloc(&w, part_bytes + kSplitkCountBytes) != cudaSuccess) return DG_ERR_CUDA;
+    if (cudaMemset(w, 0, part_bytes + kSplitkCountBytes) != cudaSuccess) {
+        cudaFree(w);
+        return DG_ERR_CUDA;
+    }
+    SplitkWs ws{static_cast<float*>(w),
+                reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(w) + part_bytes)};
+    map[s] = ws;
+    *out = ws;
+    return DG_OK;
+}
+
 dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                    bool fp16_in, const float* sa, const float* sb, const float* sd,
                    dg_dtype out, cudaStream_t s, float* amax_d = nullptr) {
@@ -210,8 +262,12 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             L.amax_out = amax_bits;
             L.group_off = nullptr;
             L.groups = 0;
-            if (plan.path == 4)
-                return from_cuda(launch_gemm_skinny(L, st->splitk_partials, st->splitk_counts, s));
+            if (plan.path == 4) {
+                SplitkWs ws;
+                rc = splitk_workspace(st, s, &ws);
+                if (rc != DG_OK) return rc;
+                return from_cuda(launch_gemm_skinny(L, ws.partials, ws.counts, s));
+            }
             return from_cuda(launch_gemm_tc(L, s));
         }
     }
@@ -475,8 +531,12 @@ dg_status dg_sync_status(dg_stream_t stream) {
             // A CTA that gave up may have left split-K arrival counters
             // part-way: clear them (every launch expects zeros).
             if (cudaDeviceSynchronize() != cudaSuccess ||
-                cudaMemset(st->splitk_counts, 0, sizeof(uint32_t) * kSkinnyMaxTiles) != cudaSuccess)
+                cudaMemset(st->splitk_counts, 0, kSplitkCountBytes) != cudaSuccess)
                 return DG_ERR_CUDA;
+            std::lock_guard<std::mutex> lk(g_ws_mu[st->device]);
+            for (auto& kv : g_ws[st->device])
+                if (cudaMemset(kv.second.counts, 0, kSplitkCountBytes) != cudaSuccess)
+                    return DG_ERR_CUDA;
             return DG_ERR_TIMEOUT;
         }
         if (word & kStatusBadArgument) return DG_ERR_INVALID_VALUE;

@@ -13,8 +13,15 @@
  * ---------------------------------------
  * Memory.    Every data pointer is DEVICE memory on the current CUDA device,
  *            owned by the caller.  The library allocates nothing per call and
- *            takes no workspace.  The first call on a device (or dg_init)
- *            allocates a 16-byte device status word that lives until exit.
+ *            takes no workspace argument.  The first call on a device (or
+ *            dg_init) allocates a 16-byte device status word and a split-K
+ *            workspace (two 16 x 128 FP32 partial tiles per SM and 8192
+ *            counters, 2.4 MB on 152 SMs) that live until exit.  Split-K
+ *            GEMMs (plan path 4) issued on a second, third, ... stream get a
+ *            workspace of their own on that stream's first such call, so
+ *            calls on different streams may run concurrently; that first
+ *            call must not happen while the stream is being captured into a
+ *            graph (it returns DG_ERR_UNSUPPORTED then).
  * Layout.    Dense, row-major, no leading-dimension arguments: A is M x K,
  *            B is N x K (both K contiguous, the "TN" form), D is M x N.
  * Alignment. Every data pointer must be 16-byte aligned and K * element
@@ -106,9 +113,11 @@ dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale,
  *   M, N, K  >= 0 and < 2^31.  M == 0 or N == 0 is a no-op; K == 0 writes
  *            zeros.  K must be a multiple of 16 (row pitch alignment).
  * M <= 2 runs a bandwidth-bound GEMV with the K sum split across a warp
- * ([DG-FP16] §2.1 and §4.1, the decode QKV projection); larger M runs the
- * tensor-core kernel with a tile chosen per shape (dg_gemm_plan).  K tails are zero-filled by the
- * tensor-memory loads and M/N edges are predicated stores ([FP8-guide] §3.3).
+ * ([DG-FP16] §2.1 and §4.1, the decode QKV projection); 3 <= M <= 16 a
+ * split-K tensor-core kernel (operands swapped, K spread over every SM);
+ * larger M the tiled tensor-core kernel with a tile chosen per shape
+ * (dg_gemm_plan).  K tails are zero-filled by the tensor-memory loads and M/N
+ * edges are predicated stores ([FP8-guide] §3.3).
  */
 dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M,
                       int64_t N, int64_t K, const float* scale_a,
