@@ -227,6 +227,17 @@ convert_f16_kernel(const float* __restrict__ x, int64_t n, const float* __restri
     }
 }
 
+// Grid of the slab kernels (quantiser, FP16 conversion): one 512-element
+// slab per warp, at most 8 CTAs of kQuantThreads per SM, at least one CTA.
+int64_t slab_grid(int64_t n, int sm_count) {
+    const int64_t slabs = n >> 9;
+    const int warps_per_block = kQuantThreads / 32;
+    int64_t blocks = (slabs + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    return blocks < 1 ? 1 : blocks;
+}
+
 }  // namespace
 
 cudaError_t launch_fp16_range_scale(const float* amax_a, const float* amax_b, float* out,
@@ -237,12 +248,7 @@ cudaError_t launch_fp16_range_scale(const float* amax_a, const float* amax_b, fl
 cudaError_t launch_convert_f16(const float* x, int64_t n, const float* factor, uint16_t* out,
                                int sm_count, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    const int64_t slabs = n >> 9;
-    const int warps_per_block = kQuantThreads / 32;
-    int64_t blocks = (slabs + warps_per_block - 1) / warps_per_block;
-    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    const int64_t blocks = slab_grid(n, sm_count);
     return launch_kernel(convert_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads),
                          0, s, x, n, factor, out);
 }
@@ -274,12 +280,7 @@ cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s) {
 cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_t* q,
                                  int sm_count, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    const int64_t slabs = n >> 9;
-    const int warps_per_block = kQuantThreads / 32;
-    int64_t blocks = (slabs + warps_per_block - 1) / warps_per_block;
-    const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    const int64_t blocks = slab_grid(n, sm_count);
     return launch_kernel(quantize_kernel<false>, dim3(static_cast<unsigned>(blocks)),
                          dim3(kQuantThreads), 0, s, x, n, scale, q, static_cast<uint32_t*>(nullptr));
 }
@@ -291,12 +292,7 @@ cudaError_t launch_quantize_e4m3_amax(const float* x, int64_t n, const float* sc
     cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
     if (e != cudaSuccess) return e;
     if (n > 0) {
-        const int64_t slabs = n >> 9;
-        const int warps_per_block = kQuantThreads / 32;
-        int64_t blocks = (slabs + warps_per_block - 1) / warps_per_block;
-        const int64_t cap = static_cast<int64_t>(sm_count) * 8;
-        if (blocks > cap) blocks = cap;
-        if (blocks < 1) blocks = 1;
+        const int64_t blocks = slab_grid(n, sm_count);
         e = launch_kernel(quantize_kernel<true>, dim3(static_cast<unsigned>(blocks)),
                           dim3(kQuantThreads), 0, s, x, n, scale, q, bits);
         if (e != cudaSuccess) return e;
