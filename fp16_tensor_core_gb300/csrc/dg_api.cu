@@ -180,6 +180,40 @@ dg_status check_sizes(int64_t M, int64_t N, int64_t K) {
     return DG_OK;
 }
 
+// Arguments of the E4M3 GEMM entry points (everything checked before any
+// device work; a no-op shape needs no pointers).
+dg_status check_fp8_gemm_args(const void* A, const void* B, const void* D, int64_t M,
+                              int64_t N, int64_t K, const float* scale_a, const float* scale_b,
+                              const float* scale_d, dg_dtype out) {
+    const dg_status rc = check_sizes(M, N, K);
+    if (rc != DG_OK) return rc;
+    if (out != DG_BF16 && out != DG_E4M3 && out != DG_FP16) return DG_ERR_INVALID_VALUE;
+    if (M > 0 && N > 0) {
+        if (D == nullptr) return DG_ERR_INVALID_VALUE;
+        if (K > 0 && (A == nullptr || B == nullptr || scale_a == nullptr || scale_b == nullptr))
+            return DG_ERR_INVALID_VALUE;
+        if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0)
+            return DG_ERR_MISALIGNED;
+    }
+    return DG_OK;
+}
+
+// Arguments of the FP16 GEMM entry points.
+dg_status check_hgemm_args(const void* A, const void* B, const void* D, int64_t M, int64_t N,
+                           int64_t K, dg_dtype out) {
+    const dg_status rc = check_sizes(M, N, K);
+    if (rc != DG_OK) return rc;
+    if (out != DG_FP16 && out != DG_BF16) return DG_ERR_INVALID_VALUE;
+    if (M > 0 && N > 0) {
+        if (D == nullptr) return DG_ERR_INVALID_VALUE;
+        if (K > 0 && (A == nullptr || B == nullptr)) return DG_ERR_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0)
+            return DG_ERR_MISALIGNED;
+    }
+    return DG_OK;
+}
+
 // The split-K workspace of `s` on the device of `st` (created on the first
 // split-K call on a stream other than the first one; never while the stream
 // is being captured into a graph).
@@ -343,17 +377,8 @@ dg_status dg_quantize_e4m3_amax(const float* x, int64_t n, const float* scale, u
 dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M, int64_t N,
                       int64_t K, const float* scale_a, const float* scale_b,
                       const float* scale_d, dg_dtype out, dg_stream_t stream) {
-    dg_status rc = check_sizes(M, N, K);
+    const dg_status rc = check_fp8_gemm_args(A, B, D, M, N, K, scale_a, scale_b, scale_d, out);
     if (rc != DG_OK) return rc;
-    if (out != DG_BF16 && out != DG_E4M3 && out != DG_FP16) return DG_ERR_INVALID_VALUE;
-    if (M > 0 && N > 0) {
-        if (D == nullptr) return DG_ERR_INVALID_VALUE;
-        if (K > 0 && (A == nullptr || B == nullptr || scale_a == nullptr || scale_b == nullptr))
-            return DG_ERR_INVALID_VALUE;
-        if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
-        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0)
-            return DG_ERR_MISALIGNED;
-    }
     return run_gemm(A, B, D, M, N, K, false, scale_a, scale_b, scale_d, out,
                     reinterpret_cast<cudaStream_t>(stream));
 }
@@ -364,17 +389,8 @@ dg_status dg_fp8_gemm_amax(const uint8_t* A, const uint8_t* B, void* D, int64_t 
                            dg_stream_t stream) {
     if (amax_d == nullptr) return DG_ERR_INVALID_VALUE;
     if ((reinterpret_cast<uintptr_t>(amax_d) & 3u) != 0) return DG_ERR_MISALIGNED;
-    dg_status rc = check_sizes(M, N, K);
+    const dg_status rc = check_fp8_gemm_args(A, B, D, M, N, K, scale_a, scale_b, scale_d, out);
     if (rc != DG_OK) return rc;
-    if (out != DG_BF16 && out != DG_E4M3 && out != DG_FP16) return DG_ERR_INVALID_VALUE;
-    if (M > 0 && N > 0) {
-        if (D == nullptr) return DG_ERR_INVALID_VALUE;
-        if (K > 0 && (A == nullptr || B == nullptr || scale_a == nullptr || scale_b == nullptr))
-            return DG_ERR_INVALID_VALUE;
-        if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
-        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0)
-            return DG_ERR_MISALIGNED;
-    }
     return run_gemm(A, B, D, M, N, K, false, scale_a, scale_b, scale_d, out,
                     reinterpret_cast<cudaStream_t>(stream), amax_d);
 }
@@ -436,15 +452,8 @@ dg_status dg_fp8_gemm_grouped(const uint8_t* A, const uint8_t* B, void* D, int64
 
 dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M, int64_t N,
                    int64_t K, dg_dtype out, dg_stream_t stream) {
-    dg_status rc = check_sizes(M, N, K);
+    const dg_status rc = check_hgemm_args(A, B, D, M, N, K, out);
     if (rc != DG_OK) return rc;
-    if (out != DG_FP16 && out != DG_BF16) return DG_ERR_INVALID_VALUE;
-    if (M > 0 && N > 0) {
-        if (D == nullptr) return DG_ERR_INVALID_VALUE;
-        if (K > 0 && (A == nullptr || B == nullptr)) return DG_ERR_INVALID_VALUE;
-        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0)
-            return DG_ERR_MISALIGNED;
-    }
     return run_gemm(A, B, D, M, N, K, true, nullptr, nullptr, nullptr, out,
                     reinterpret_cast<cudaStream_t>(stream));
 }
@@ -452,19 +461,12 @@ dg_status dg_hgemm(const uint16_t* A, const uint16_t* B, void* D, int64_t M, int
 dg_status dg_hgemm_scaled(const uint16_t* A, const uint16_t* B, void* D, int64_t M, int64_t N,
                           int64_t K, const float* scale_a, const float* scale_b, dg_dtype out,
                           dg_stream_t stream) {
-    dg_status rc = check_sizes(M, N, K);
-    if (rc != DG_OK) return rc;
-    if (out != DG_FP16 && out != DG_BF16) return DG_ERR_INVALID_VALUE;
     if (scale_a == nullptr || scale_b == nullptr) return DG_ERR_INVALID_VALUE;
     if ((reinterpret_cast<uintptr_t>(scale_a) & 3u) != 0 ||
         (reinterpret_cast<uintptr_t>(scale_b) & 3u) != 0)
         return DG_ERR_MISALIGNED;
-    if (M > 0 && N > 0) {
-        if (D == nullptr) return DG_ERR_INVALID_VALUE;
-        if (K > 0 && (A == nullptr || B == nullptr)) return DG_ERR_INVALID_VALUE;
-        if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0)
-            return DG_ERR_MISALIGNED;
-    }
+    const dg_status rc = check_hgemm_args(A, B, D, M, N, K, out);
+    if (rc != DG_OK) return rc;
     return run_gemm(A, B, D, M, N, K, true, scale_a, scale_b, nullptr, out,
                     reinterpret_cast<cudaStream_t>(stream));
 }
