@@ -307,6 +307,16 @@ def kernel_cases(torch, dg):
                                          dg.DG_BF16, stream=s)
         return fn, 2.0 * m * Nq * Kq, Nq * Kq + m * Kq + m * Nq * 2, "hbm", f"{nb} rotating copies"
 
+    def small_fp8(M, N, K):
+        # latency-bound parity configurations (256^3, the 1000 x 1040 sweep)
+        nb = ncopies(M * K + N * K)
+        As = [codes((M, K), 90 + i) for i in range(nb)]
+        Bs = [codes((N, K), 95 + i) for i in range(nb)]
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda i, s: dg.dg_fp8_gemm(As[i % nb], Bs[i % nb], D, one, one, None,  # noqa: E731
+                                         dg.DG_BF16, stream=s)
+        return fn, 2.0 * M * N * K, M * K + N * K + 2 * M * N, "latency", f"{nb} rotating copies"
+
     def fp8_sq(S, out):
         nb = ncopies(2 * S * S)
         As = [codes((S, S), 30 + i) for i in range(nb)]
@@ -410,6 +420,11 @@ def kernel_cases(torch, dg):
     return {
         "moe_grouped_16x8192x2048x4096": lambda: moe(True),
         "moe_per_group_calls_16x8192x2048x4096": lambda: moe(False),
+        "fp8_gemm_256": lambda: small_fp8(256, 256, 256),
+        "fp8_sweep_m1_1x1000x1040": lambda: small_fp8(1, 1000, 1040),
+        "fp8_sweep_m63_63x1000x1040": lambda: small_fp8(63, 1000, 1040),
+        "fp8_sweep_m65_65x1000x1040": lambda: small_fp8(65, 1000, 1040),
+        "fp8_sweep_m129_129x1000x1040": lambda: small_fp8(129, 1000, 1040),
         "qkv_gemv_1x12288x4096": qkv,
         "qkv_m4_4x12288x4096": lambda: gemv_m(4),
         "qkv_m8_8x12288x4096": lambda: gemv_m(8),
