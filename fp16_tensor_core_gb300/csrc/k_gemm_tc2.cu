@@ -23,7 +23,12 @@
 //    the even CTA's `acc_empty` (count 8: four warps per CTA);
 //  * a final multicast commit to `drain` tells both CTAs that no pair MMA
 //    still reads their shared memory or writes their tensor memory; only
-//    then is tensor memory freed (collectively) and the CTAs exit.
+//    then is tensor memory freed (collectively) and the CTAs exit;
+//  * the last tile's epilogue, which nothing overlaps, stages each warp's
+//    32 x 32 output boxes in the idle A stages (TMA's 64- or 32-byte swizzle)
+//    and writes them with bulk tensor stores (whole lines, edges clipped by
+//    the tensor map) instead of one scattered row per lane; earlier tiles'
+//    epilogues overlap the next tile's main loop and store directly.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -65,7 +70,8 @@ struct PairCfg {
 template <int BN, int STAGES, bool kFp16In>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                    const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_d, const Params p) {
     using C = PairCfg<BN, STAGES, kFp16In>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -217,15 +223,76 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             if (!__all_sync(0xFFFFFFFFu, got)) break;
             tc_fence_after_sync();
             const int row = mt * kPairBM + static_cast<int>(rank) * kHalfBM + q * 32 + lane;
+            const int row0 = row - lane;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
+            if (p.vec_ok && t + npairs >= num_tiles) {
+                // Last tile: the pipeline stages are idle, so each warp stages
+                // its 32 x 32 output boxes in shared memory (TMA swizzled
+                // layout) and writes them with bulk tensor stores, which
+                // clip rows >= M and columns >= N.
+                const bool e4 = p.out_kind == kOutE4M3;
+                uint8_t* stg = sA + q * (BN * 64);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_load_32cols(tbase + c * 32, r);
+                    tmem_load_wait(r);
+                    const int col0 = nt * BN + c * 32;
+                    const int ncols = min(32, p.N - col0);
+                    if (p.amax_out != nullptr && row < p.M) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < ncols) amax_bits = max(amax_bits, r[i] & 0x7FFFFFFFu);
+                    }
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
+                    uint8_t* box = stg + c * 2048;
+                    if (e4) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            w[j] = static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j], v[4 * j + 1])) |
+                                   (static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j + 2], v[4 * j + 3])) << 16);
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int ph = k ^ ((lane >> 2) & 1);
+                            st_shared_v4(smem_addr(box + lane * 32 + ph * 16), w[4 * k], w[4 * k + 1],
+                                         w[4 * k + 2], w[4 * k + 3]);
+                        }
+                    } else {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            w[j] = p.out_kind == kOutFP16 ? f32x2_to_f16x2(v[2 * j], v[2 * j + 1])
+                                                          : f32x2_to_bf16x2(v[2 * j], v[2 * j + 1]);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int ph = k ^ ((lane >> 1) & 3);
+                            st_shared_v4(smem_addr(box + lane * 64 + ph * 16), w[4 * k], w[4 * k + 1],
+                                         w[4 * k + 2], w[4 * k + 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.M && col0 < p.N) {
+                        tma_store_2d(&tmap_d, box, col0, row0);
+                        bulk_commit();
+                    }
+                }
+                if (lane == 0) bulk_wait_all();
                 __syncwarp();
-                tmem_load_32cols(tbase + c * 32, r);
-                tmem_load_wait(r);
-                amax_bits = max(amax_bits, store_chunk(p, row, p.M, nt * BN + c * 32, r, alpha));
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_load_32cols(tbase + c * 32, r);
+                    tmem_load_wait(r);
+                    amax_bits = max(amax_bits, store_chunk(p, row, p.M, nt * BN + c * 32, r, alpha));
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -253,7 +320,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
 template <typename Kern>
 cudaError_t launch_pair(Kern kern, dim3 grid, size_t smem, cudaStream_t s,
-                        const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm) {
+                        const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                        const Params& prm) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
@@ -268,7 +336,7 @@ cudaError_t launch_pair(Kern kern, dim3 grid, size_t smem, cudaStream_t s,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, prm);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, td, prm);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -307,12 +375,33 @@ cudaError_t launch_pair_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s
         }
         clusters = max_clusters[dev];
     }
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kHalfBM) ||
         !make_map(&tb, L.B, L.N, L.K, kFp16In, C::kBRows))
         return cudaErrorInvalidValue;
+    Params prm2 = prm;
+    if (prm2.vec_ok) {
+        // Output map for the last tile's bulk stores: 32 x 32 boxes, swizzled
+        // to the width of one box row (64 B for 2-byte outputs, 32 B for E4M3).
+        auto encode = get_encode_fn();
+        const bool e4 = L.out_kind == kOutE4M3;
+        const CUtensorMapDataType dt = e4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                      : (L.out_kind == kOutFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.N), static_cast<cuuint64_t>(L.M)};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.N) * L.out_elem};
+        cuuint32_t box[2] = {32, 32};
+        cuuint32_t estr[2] = {1, 1};
+        if (!encode || encode(&td, dt, 2, L.D, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              e4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            prm2.vec_ok = 0;
+    }
+    if (!prm2.vec_ok) td = ta;
+    static_assert(STAGES * C::kABytes >= 4 * BN * 64, "staging for the last tile");
     const int pairs = L.plan->tiles < clusters ? L.plan->tiles : clusters;
-    return launch_pair(kern, dim3(2 * pairs), C::kSmemBytes, s, ta, tb, prm);
+    return launch_pair(kern, dim3(2 * pairs), C::kSmemBytes, s, ta, tb, td, prm2);
 }
 
 template <bool kFp16In>
