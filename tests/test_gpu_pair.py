@@ -137,3 +137,34 @@ def test_bounded_wait_timeout(kernel):
         dg.dg_set_wait_timeout_us(2_000_000)
         dg.dg_debug_skip_first_load(False)
     test_fp8_bf16_out(kernel, 256, 256, 256)
+
+
+@pytest.mark.parametrize("out", [dg.DG_BF16, dg.DG_FP16, dg.DG_E4M3])
+@pytest.mark.parametrize("M,N,K", [(300, 1024, 272), (512, 2048, 128)])
+def test_last_tile_bulk_store_epilogue(kernel, M, N, K, out):
+    """Rows of D a multiple of 16 bytes: each pair's last tile is written by
+    bulk tensor stores (swizzled staging, rows past M clipped); every element
+    is checked, and nothing outside D is written."""
+    A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+    qa_ref, sa, _ = oracle.quantize_tensor(A)
+    qb_ref, sb, _ = oracle.quantize_tensor(B)
+    qa, _, sa_d = gpu_quantize(A)
+    qb, _, sb_d = gpu_quantize(B)
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    if out == dg.DG_E4M3:
+        sd = np.float32(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))) / 448.0)
+        sdt = scalar()
+        sdt[0] = float(sd)
+        buf, D = guarded(M * N, torch.uint8, 0x7F)
+        dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, sdt, out, M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        check_guards(buf, M * N, 0x7F)
+        check_e4m3(D.cpu().numpy().reshape(M, N), R, sa, sb, sd)
+    else:
+        buf, D = guarded(M * N, torch.int16, 0x7FFF)
+        dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, None, out, M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        check_guards(buf, M * N, 0x7FFF)
+        h = D.cpu().numpy().view(np.uint16).reshape(M, N)
+        d = fp16_bits_to_f64(h) if out == dg.DG_FP16 else bf16_bits_to_f64(h)
+        check_bf16_like(d, R, S, sa, sb, "FP16" if out == dg.DG_FP16 else "BF16")
