@@ -18,10 +18,11 @@
  *            workspace (two 16 x 128 FP32 partial tiles per SM and 8192
  *            counters, 2.4 MB on 152 SMs) that live until exit.  Split-K
  *            GEMMs (plan path 4) issued on a second, third, ... stream get a
- *            workspace of their own on that stream's first such call, so
- *            calls on different streams may run concurrently; that first
- *            call must not happen while the stream is being captured into a
- *            graph (it returns DG_ERR_UNSUPPORTED then).
+ *            workspace of their own (same size, kept until exit) on that
+ *            stream's first such call, so calls on different streams may run
+ *            concurrently; that first call must not happen while the stream
+ *            is being captured into a graph (it returns DG_ERR_UNSUPPORTED
+ *            then).
  * Layout.    Dense, row-major, no leading-dimension arguments: A is M x K,
  *            B is N x K (both K contiguous, the "TN" form), D is M x N.
  * Alignment. Every data pointer must be 16-byte aligned and K * element
