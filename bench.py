@@ -429,6 +429,10 @@ def kernel_cases(torch, dg):
         "qkv_m4_4x12288x4096": lambda: gemv_m(4),
         "qkv_m8_8x12288x4096": lambda: gemv_m(8),
         "qkv_m16_16x12288x4096": lambda: gemv_m(16),
+        "qkv_m32_32x12288x4096": lambda: gemv_m(32),
+        "qkv_m64_64x12288x4096": lambda: gemv_m(64),
+        "qkv_m128_128x12288x4096": lambda: gemv_m(128),
+        "qkv_m256_256x12288x4096": lambda: gemv_m(256),
         "fp8_gemm_4096": lambda: fp8_sq(4096, dg.DG_BF16),
         "fp8_gemm_8192_e4m3out": lambda: fp8_sq(8192, dg.DG_E4M3),
         "fp16_hgemm_4096": lambda: hgemm(4096),
