@@ -2,6 +2,7 @@
 // per-device state, path/tile selection and launch.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <unordered_map>
@@ -34,7 +35,7 @@ std::mutex g_ws_mu[kMaxDevices];
 std::unordered_map<cudaStream_t, SplitkWs> g_ws[kMaxDevices];
 
 size_t splitk_partial_bytes(int sm_count) {
-    return sizeof(float) * 2 * static_cast<size_t>(sm_count) * kSkinnyMaxM * kSkinnyTileRows;
+    return sizeof(float) * 2 * static_cast<size_t>(sm_count) * kSplitkMaxCols * kSkinnyTileRows;
 }
 constexpr size_t kSplitkCountBytes = sizeof(uint32_t) * kSkinnyMaxTiles;
 
@@ -126,6 +127,35 @@ void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& 
                  p.block_m, p.block_n, p.stages, p.tiles, p.grid);
 }
 
+// Launch-time estimates (microseconds) for choosing between the tiled and
+// the split-K kernels at 17 <= M <= 128, fitted to graph-replayed GB300
+// timings with B read from HBM (M = 16..128 against N = 1024..28672,
+// K = 4096..14336).
+//  * Tiled: a fixed ~3 us plus the larger of one CTA's operand stream at its
+//    single-SM rate (~115 GB/s) and all bytes at ~6 TB/s.
+//  * Split-K: ~5.3 us fixed, B at ~6.5 TB/s, and for each 16 columns of A
+//    past the first, the last-arriving CTA's extra fixup pass: ~1.2 us plus
+//    ~0.6 us per four partial tiles it reads (ceil(grid / tiles) of them).
+double tiled_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const dg_plan& p) {
+    const double elem = fp16_in ? 2.0 : 1.0;
+    const int64_t kblocks = (K + p.block_k - 1) / p.block_k;
+    const int64_t tiles_per_cta = (p.tiles + p.grid - 1) / p.grid;
+    const double cta_bytes = static_cast<double>(tiles_per_cta) * static_cast<double>(kblocks) *
+                             static_cast<double>(p.block_m + p.block_n) * 128.0;
+    const double all_bytes = static_cast<double>(M + N) * static_cast<double>(K) * elem;
+    return 3.0 + std::max(cta_bytes / 1.15e5, all_bytes / 6.0e6);
+}
+
+double splitk_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const dg_plan& p) {
+    const double elem = fp16_in ? 2.0 : 1.0;
+    const int64_t chunks = (M + 15) / 16;
+    const int64_t others = (p.grid + p.tiles - 1) / p.tiles;
+    const int64_t groups = (others + 3) / 4;
+    const double b_bytes = static_cast<double>(N) * static_cast<double>(K) * elem;
+    return 5.3 + b_bytes / 6.5e6 +
+           static_cast<double>(chunks - 1) * (1.2 + 0.6 * static_cast<double>(groups));
+}
+
 // Shared path selection for dg_gemm_plan and the GEMM entry points.
 dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p) {
     *p = dg_plan{};
@@ -157,12 +187,16 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
         p->stages = 1;
         return DG_OK;
     }
-    // Split-K with swapped operands for the remaining skinny shapes (every
-    // SM streams an equal share of B; DG_SPLITK=0 turns it off).
+    // Split-K with swapped operands (every SM streams an equal share of B)
+    // for the remaining skinny shapes, and for 17 <= M <= 128 when the tiled
+    // plan would keep fewer than 3/4 of the SMs busy and the time estimate
+    // below favours it.  DG_SPLITK=0 turns it off, DG_SPLITK=1 uses it for
+    // every M <= 128.
     const char* sk = std::getenv("DG_SPLITK");
     const bool splitk_off = sk != nullptr && sk[0] == '0';
-    if (!splitk_off && M <= kSkinnyMaxM &&
-        (N + kSkinnyTileRows - 1) / kSkinnyTileRows <= kSkinnyMaxTiles) {
+    const bool splitk_forced = sk != nullptr && sk[0] == '1';
+    const bool splitk_fits = (N + kSkinnyTileRows - 1) / kSkinnyTileRows <= kSkinnyMaxTiles;
+    if (!splitk_off && splitk_fits && M <= kSkinnyMaxM) {
         p->path = 4;
         plan_skinny(M, N, K, fp16_in, sm_count, p);
         return DG_OK;
@@ -171,6 +205,15 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     if (tiles > INT_MAX) return DG_ERR_UNSUPPORTED;
     p->path = 3;
     plan_tc(M, N, K, fp16_in, sm_count, p);
+    if (!splitk_off && splitk_fits && M <= kSplitkMaxCols &&
+        (splitk_forced || 4 * static_cast<int64_t>(p->grid) < 3 * static_cast<int64_t>(sm_count))) {
+        dg_plan sk{};
+        sk.path = 4;
+        plan_skinny(M, N, K, fp16_in, sm_count, &sk);
+        if (splitk_forced || splitk_estimate_us(M, N, K, fp16_in, sk) <
+                                 0.9 * tiled_estimate_us(M, N, K, fp16_in, *p))
+            *p = sk;
+    }
     return DG_OK;
 }
 
@@ -300,7 +343,8 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
                 SplitkWs ws;
                 rc = splitk_workspace(st, s, &ws);
                 if (rc != DG_OK) return rc;
-                return from_cuda(launch_gemm_skinny(L, ws.partials, ws.counts, s));
+                return from_cuda(
+                    launch_gemm_skinny(L, ws.partials, ws.counts, kSplitkMaxCols, s));
             }
             return from_cuda(launch_gemm_tc(L, s));
         }

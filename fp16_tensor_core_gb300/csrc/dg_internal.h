@@ -15,9 +15,12 @@ inline int out_kind_of(dg_dtype t) {
 }
 inline int elem_bytes(dg_dtype t) { return t == DG_E4M3 ? 1 : 2; }
 
-// Split-K path for skinny GEMMs (M <= 16): 128 rows of B per tile, the M
-// rows of A padded to 16, K blocks of every tile spread evenly over the SMs.
+// Split-K path for skinny GEMMs: 128 rows of B per tile, the M rows of A
+// padded to MMA N = 16, 32, 64 or 128, K blocks of every tile spread evenly
+// over the SMs.  Always used for M <= 16 (past the GEMV); for M <= 128 when
+// the tiled kernels would leave SMs idle.
 constexpr int kSkinnyMaxM = 16;
+constexpr int kSplitkMaxCols = 128;
 constexpr int kSkinnyTileRows = 128;
 constexpr int kSkinnyMaxTiles = 8192;   // N <= 1,048,576
 
@@ -26,7 +29,7 @@ struct DeviceState {
     int device = -1;
     int sm_count = 0;
     uint32_t* status = nullptr;  // device status word (kStatus* bits)
-    // Split-K workspace: two FP32 partial-tile slots of 16 x 128 per SM and
+    // Split-K workspace: two FP32 partial-tile slots of 128 x 128 per SM and
     // one arrival counter per tile (all zero between launches).
     float* splitk_partials = nullptr;
     uint32_t* splitk_counts = nullptr;
@@ -110,7 +113,9 @@ cudaError_t launch_gemm_tc_grouped(const TcLaunch& L, cudaStream_t s);
 constexpr int kMaxGemmGroups = 1024;
 
 // Skinny split-K tensor-core GEMM (plan path 4).
-cudaError_t launch_gemm_skinny(const TcLaunch& L, float* partials, uint32_t* counts,
+// partials must hold 2 * grid slots of nc_for(M) x 128 floats, with
+// nc_for(M) <= max_cols.
+cudaError_t launch_gemm_skinny(const TcLaunch& L, float* partials, uint32_t* counts, int max_cols,
                                cudaStream_t s);
 void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p);
 

@@ -127,5 +127,7 @@ extern "C" dg_status dg_fp8_gemm_splitk_static(const uint8_t* A, const uint8_t* 
     L.amax_out = nullptr;
     L.group_off = nullptr;
     L.groups = 0;
-    return launch_gemm_skinny(L, a.partials, a.counts, s) == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+    return launch_gemm_skinny(L, a.partials, a.counts, kSkinnyMaxM, s) == cudaSuccess
+               ? DG_OK
+               : DG_ERR_CUDA;
 }

@@ -1,6 +1,6 @@
-// k_gemm_skinny.cu -- the tensor-core path for skinny GEMMs (M <= 16):
-// split-K over every SM, with the operands swapped so that the long side
-// fills the 128-row MMA.
+// k_gemm_skinny.cu -- the tensor-core path for skinny GEMMs (M <= 128 with
+// few output tiles): split-K over every SM, with the operands swapped so that
+// the long side fills the 128-row MMA.
 //
 // Page shorthands: [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南";
 // [DG-FP16] = the DeepGEMM FP16/WMMA deep-dive page.
@@ -11,8 +11,9 @@
 // M <= 16 would leave 7/8 of each MMA empty and give N/BN tiles -- too few
 // to occupy 152 SMs.  Here instead:
 //  * operands are swapped: the MMA computes D^T = B * A^T, its M side (128)
-//    is 128 rows of B and its N side (16) the M rows of A, zero-filled by TMA
-//    past M ([FP8-guide] §3.3's edge handling);
+//    is 128 rows of B and its N side (NC = 16, 32, 64 or 128) the M rows of
+//    A rounded up, zero-filled by TMA past M ([FP8-guide] §3.3's edge
+//    handling);
 //  * the K blocks of all tiles form one sequence of `units` (tile, k block)
 //    that is cut into gridDim.x equal contiguous ranges, one per CTA, so every
 //    SM streams the same number of bytes (split-K, balanced);
@@ -24,8 +25,11 @@
 //    scale_A * scale_B (/ scale_D for E4M3 out, [FP8-guide] §3.2), stores D
 //    and resets the counter to zero.  No CTA waits for another.
 // Pipeline: one TMA thread, one MMA thread, four epilogue warps, a ring of
-// 12 K blocks (16 KB of B + 2 KB of A each, 1 / 2 / 4 blocks per stage) and
-// two 16-column accumulators in tensor memory.  Launch overlap: before its
+// K blocks (16 KB of B + NC x 128 bytes of A each; 12 of them for NC = 16,
+// 6 for NC = 128; 1 or 2 blocks per stage) and two NC-column accumulators in
+// tensor memory.  Partial tiles are kept as FP32 column quads (16 bytes per
+// row and 4 columns) and the finishing CTA requests four segments' quads at a
+// time before adding them in segment order.  Launch overlap: before its
 // dependency wait a CTA prefetches its first ring of B into L2, and right
 // after it the grid lets the next kernel take over SMs as CTAs exit, so the
 // start-up of one launch hides in the straggling tail of the one before.
@@ -45,28 +49,37 @@ namespace dg {
 namespace {
 
 constexpr int kRows = kSkinnyTileRows;            // MMA M: rows of B per tile
-constexpr int kCols = kSkinnyMaxM;                // MMA N: rows of A (padded)
 constexpr int kWBytes = kRows * kBKBytes;         // 16 KB of B per K block
-constexpr int kXBytes = kCols * kBKBytes;         // 2 KB of A per K block
-constexpr int kKBBytes = kWBytes + kXBytes;       // 18 KB per K block
-constexpr int kRingKBlocks = 12;                  // K blocks in flight per CTA
 constexpr int kBarBytes = 256;
-constexpr int kSkSmemBytes = 1024 + kRingKBlocks * kKBBytes + kBarBytes;
-constexpr uint32_t kTmemCols = 32;                // two 16-column accumulators
-constexpr uint32_t kIdesc = idesc_f32acc(kRows, kCols, 0, 0);
 constexpr uint32_t kEpiBar = 1;                   // named barrier of the epilogue warps
 constexpr uint32_t kEpiThreads = 128;
-static_assert(kSkSmemBytes <= kSmemLimit, "shared memory");
-static_assert(kXBytes % 1024 == 0, "1024-byte aligned A blocks (128-byte swizzle atoms)");
 
-// A stage holds up to KPS consecutive K blocks of one tile, loaded together
-// so that each row of B is requested KPS x 128 contiguous bytes at a time.
-template <int KPS>
+// K blocks in flight per CTA for MMA N = nc (the rows of A, padded): as many
+// as fit in 227 KB of shared memory, rounded down to an even number.
+constexpr int ring_kblocks(int nc) {
+    const int r = (kSmemLimit - 1024 - kBarBytes) / (kWBytes + nc * kBKBytes);
+    const int even = r & ~1;
+    return even > 12 ? 12 : even;
+}
+
+// Configuration for MMA N = NC (16, 32, 64 or 128 rows of A) with KPS
+// consecutive K blocks per stage, loaded together so that each row of B is
+// requested KPS x 128 contiguous bytes at a time.
+template <int NC, int KPS>
 struct SkCfg {
-    static_assert(kRingKBlocks % KPS == 0, "ring");
-    static constexpr int kStages = kRingKBlocks / KPS;
+    static constexpr int kXBytes = NC * kBKBytes;           // A rows per K block
+    static constexpr int kKBBytes = kWBytes + kXBytes;
+    static constexpr int kRing = ring_kblocks(NC);
+    static constexpr int kStages = kRing / KPS;
     static constexpr int kStageW = KPS * kWBytes;
     static constexpr int kStageX = KPS * kXBytes;
+    static constexpr int kSmemBytes = 1024 + kRing * kKBBytes + kBarBytes;
+    static constexpr uint32_t kTmemCols = pow2_at_least(2 * NC);   // two accumulators
+    static constexpr uint32_t kIdesc = idesc_f32acc(kRows, NC, 0, 0);
+    static_assert(NC % 16 == 0 && NC >= 16 && NC <= kSplitkMaxCols, "MMA N");
+    static_assert(kRing % KPS == 0 && kStages <= 12, "ring");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+    static_assert(kXBytes % 1024 == 0, "1024-byte aligned A blocks (128-byte swizzle atoms)");
 };
 
 struct SkParams {
@@ -80,7 +93,7 @@ struct SkParams {
     uint64_t timeout_ns;
     int skip_first_load;
     uint32_t* amax_out;
-    float* partials;       // [2 * gridDim.x][16][128]
+    float* partials;       // [2 * gridDim.x][NC / 4][128] float4: column quads
     uint32_t* counts;      // [tiles]
     int tiles;             // ceil(N / 128)
     int kblocks;           // ceil(K / BK)
@@ -114,13 +127,16 @@ __device__ __forceinline__ void store_one(const SkParams& p, int m, int n, float
     }
 }
 
-template <bool kFp16In, int KPS>
+template <bool kFp16In, int KPS, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_x, const SkParams p) {
     constexpr int kBK = kFp16In ? 64 : 128;   // K elements per K block
-    using C = SkCfg<KPS>;
+    using C = SkCfg<NC, KPS>;
     constexpr int kStages = C::kStages;
+    constexpr int kRingKBlocks = C::kRing;
+    constexpr int kKBBytes = C::kKBBytes;
+    constexpr int kXBytes = C::kXBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -155,7 +171,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
         tma_prefetch_desc(&tmap_x);
     }
     if (warp == 2) {
-        tmem_alloc<kTmemCols>(tmem_slot);
+        tmem_alloc<C::kTmemCols>(tmem_slot);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -240,7 +256,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
             left -= kb_end - kb0;
             if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, ctl)) break;
             tc_fence_after_sync();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kCols);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NC);
             for (int kb = kb0; kb < kb_end; kb += KPS) {
                 const int nk = min(KPS, kb_end - kb);
                 if (!wait_bounded(&full[stage], phase, ctl)) { ok = false; break; }
@@ -256,9 +272,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                             const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
                             const uint32_t accum = (kb > kb0 || i > 0 || kk > 0) ? 1u : 0u;
                             if constexpr (kFp16In)
-                                mma_f16(d_tmem, ad, bd, kIdesc, accum);
+                                mma_f16(d_tmem, ad, bd, C::kIdesc, accum);
                             else
-                                mma_f8f6f4(d_tmem, ad, bd, kIdesc, accum);
+                                mma_f8f6f4(d_tmem, ad, bd, C::kIdesc, accum);
                         }
                     }
                 }
@@ -301,28 +317,38 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
             const bool got = wait_bounded(&acc_full[acc], acc_phase, ctl);
             if (!named_bar_and(kEpiBar, kEpiThreads, got)) break;
             tc_fence_after_sync();
-            uint32_t raw[16];
-            __syncwarp();
-            tmem_load_16cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                 static_cast<uint32_t>(acc * kCols),
-                             raw);
-            tmem_load_wait(raw);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-
-            float v[kCols];
-#pragma unroll
-            for (int m = 0; m < kCols; ++m) v[m] = __uint_as_float(raw[m]);
+            // Columns [c0, c0 + 16) of this row's accumulator, 16 at a time;
+            // only chunks that hold rows of A (c0 < M) are read.
+            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                  static_cast<uint32_t>(acc * NC);
+            const int n = t * kRows + r;
+            float first[16];   // chunk 0, kept from the partial pass
             bool finish = true;
+            int my_slot = 0;
             if (c_last > c_first) {
                 // Split tile: publish this partial, count the arrival.
-                const int my_slot = me == c_first ? first_slot : 2 * me;
-                float* ws = p.partials + static_cast<int64_t>(my_slot) * kCols * kRows;
+                my_slot = me == c_first ? first_slot : 2 * me;
+                float4* ws = reinterpret_cast<float4*>(p.partials) +
+                             static_cast<int64_t>(my_slot) * (NC / 4) * kRows;
+#pragma unroll 1
+                for (int c0 = 0; c0 < NC && c0 < p.M; c0 += 16) {
+                    uint32_t raw[16];
+                    __syncwarp();
+                    tmem_load_16cols(tacc + static_cast<uint32_t>(c0), raw);
+                    tmem_load_wait(raw);
 #pragma unroll
-                for (int m = 0; m < kCols; ++m)
-                    if (m < p.M) ws[m * kRows + r] = v[m];
+                    for (int j = 0; j < 16; ++j) {
+                        if (c0 == 0) first[j] = __uint_as_float(raw[j]);
+                    }
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (c0 + 4 * g < p.M)
+                            __stcg(ws + ((c0 >> 2) + g) * kRows + r,
+                                   make_float4(__uint_as_float(raw[4 * g]), __uint_as_float(raw[4 * g + 1]),
+                                               __uint_as_float(raw[4 * g + 2]),
+                                               __uint_as_float(raw[4 * g + 3])));
+                    }
+                }
                 named_bar_sync(kEpiBar, kEpiThreads);
                 if (threadIdx.x == 4 * 32) {
                     const uint32_t old = atom_add_acq_rel_gpu(&p.counts[t], 1u);
@@ -332,42 +358,81 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 }
                 named_bar_sync(kEpiBar, kEpiThreads);
                 finish = *last_flag != 0;
-                if (finish) {
-                    // Sum the segments in order c_first .. c_last, the own
-                    // one from registers, the others from their slots.
-                    float sum[kCols];
-#pragma unroll 1
-                    for (int c = c_first; c <= c_last; ++c) {
-                        float x[kCols];
-                        if (c == me) {
-#pragma unroll
-                            for (int m = 0; m < kCols; ++m) x[m] = v[m];
-                        } else {
-                            const int slot = c == c_first ? first_slot : 2 * c;
-                            const float* w = p.partials + static_cast<int64_t>(slot) * kCols * kRows;
-#pragma unroll
-                            for (int m = 0; m < kCols; ++m)
-                                x[m] = m < p.M ? __ldcg(w + m * kRows + r) : 0.0f;
-                        }
-#pragma unroll
-                        for (int m = 0; m < kCols; ++m) sum[m] = c == c_first ? x[m] : sum[m] + x[m];
-                    }
-#pragma unroll
-                    for (int m = 0; m < kCols; ++m) v[m] = sum[m];
-                }
             }
             if (finish) {
-                const int n = t * kRows + r;
-                if (n < p.N) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < NC && c0 < p.M; c0 += 16) {
+                    float v[16];
+                    if (c_last > c_first && c0 == 0) {
 #pragma unroll
-                    for (int m = 0; m < kCols; ++m) {
-                        if (m < p.M) {
-                            amax_bits = max(amax_bits, __float_as_uint(v[m]) & 0x7FFFFFFFu);
-                            store_one(p, m, n, v[m] * alpha);
+                        for (int j = 0; j < 16; ++j) v[j] = first[j];
+                    } else {
+                        uint32_t raw[16];
+                        __syncwarp();
+                        tmem_load_16cols(tacc + static_cast<uint32_t>(c0), raw);
+                        tmem_load_wait(raw);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+                    }
+                    if (c_last > c_first) {
+                        // Sum the segments in order c_first .. c_last, the own
+                        // one from tensor memory, the others from their slots.
+                        // The slots of four segments are requested together
+                        // and then added in order, so the order (and the
+                        // result) is fixed while four loads are in flight.
+                        float sum[16];
+#pragma unroll 1
+                        for (int cb = c_first; cb <= c_last; cb += 4) {
+                            float4 x[4][4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int c = cb + i;
+                                const int slot = c == c_first ? first_slot : 2 * c;
+                                const float4* w = reinterpret_cast<const float4*>(p.partials) +
+                                                  static_cast<int64_t>(slot) * (NC / 4) * kRows;
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) {
+                                    x[i][g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                                    if (c <= c_last && c != me && c0 + 4 * g < p.M)
+                                        x[i][g] = __ldcg(w + ((c0 >> 2) + g) * kRows + r);
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int c = cb + i;
+                                if (c > c_last) break;
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) {
+                                    float y[4] = {x[i][g].x, x[i][g].y, x[i][g].z, x[i][g].w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int j = 4 * g + e;
+                                        const float val = c == me ? v[j] : y[e];
+                                        sum[j] = c == c_first ? val : sum[j] + val;
+                                    }
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = sum[j];
+                    }
+                    if (n < p.N) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (c0 + j < p.M) {
+                                amax_bits = max(amax_bits, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+                                store_one(p, c0 + j, n, v[j] * alpha);
+                            }
                         }
                     }
                 }
             }
+            // The accumulator is free once every chunk has been read.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            (void)my_slot;
         }
         // max |sa*sb*acc| of this warp's stored outputs (monotone rounding:
         // fl(max|acc| * c) is the exact maximum of fl(|acc| * c)).
@@ -382,13 +447,14 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    if (warp == 2) tmem_dealloc<kTmemCols>(tmem_base);
+    if (warp == 2) tmem_dealloc<C::kTmemCols>(tmem_base);
 }
 
 // ------------------------------------------------------------- host side
 
-template <bool kFp16In, int KPS>
+template <bool kFp16In, int KPS, int NC>
 cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cudaStream_t s) {
+    using C = SkCfg<NC, KPS>;
     static std::mutex mu;
     static bool attr_done[64] = {};
     int dev = 0;
@@ -398,14 +464,14 @@ cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cuda
         std::lock_guard<std::mutex> lk(mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!attr_done[dev]) {
-            e = cudaFuncSetAttribute(gemm_skinny_kernel<kFp16In, KPS>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSkSmemBytes);
+            e = cudaFuncSetAttribute(gemm_skinny_kernel<kFp16In, KPS, NC>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
             if (e != cudaSuccess) return e;
             attr_done[dev] = true;
         }
     }
     CUtensorMap tw, tx;
-    if (!make_map(&tw, L.B, L.N, L.K, kFp16In, kRows) || !make_map(&tx, L.A, L.M, L.K, kFp16In, kCols))
+    if (!make_map(&tw, L.B, L.N, L.K, kFp16In, kRows) || !make_map(&tx, L.A, L.M, L.K, kFp16In, NC))
         return cudaErrorInvalidValue;
     SkParams prm;
     prm.D = L.D;
@@ -425,25 +491,45 @@ cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cuda
     prm.tiles = L.plan->tiles;
     const int bk = kFp16In ? 64 : 128;
     prm.kblocks = (L.K + bk - 1) / bk;
-    return launch_kernel(gemm_skinny_kernel<kFp16In, KPS>, dim3(L.plan->grid), dim3(kThreads),
-                         kSkSmemBytes, s, tw, tx, prm);
+    return launch_kernel(gemm_skinny_kernel<kFp16In, KPS, NC>, dim3(L.plan->grid), dim3(kThreads),
+                         C::kSmemBytes, s, tw, tx, prm);
 }
 
-// K blocks per stage: DG_SPLITK_KPS=1|2|4 (sweeps), default 2.
+// K blocks per stage: DG_SPLITK_KPS=1|2 (sweeps), default 2.
 int splitk_kps() {
     if (const char* v = std::getenv("DG_SPLITK_KPS")) {
         const int k = std::atoi(v);
-        if (k == 1 || k == 2 || k == 4) return k;
+        if (k == 1 || k == 2) return k;
     }
     return 2;
 }
 
+// MMA N for M rows of A: M rounded up to 16, 32, 64 or 128.
+int nc_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+int smem_for_nc(int nc) {
+    switch (nc) {
+        case 16: return SkCfg<16, 2>::kSmemBytes;
+        case 32: return SkCfg<32, 2>::kSmemBytes;
+        case 64: return SkCfg<64, 2>::kSmemBytes;
+        default: return SkCfg<128, 2>::kSmemBytes;
+    }
+}
+
+template <bool kFp16In, int NC>
+cudaError_t launch_nc(const TcLaunch& L, float* partials, uint32_t* counts, cudaStream_t s) {
+    if (SkCfg<NC, 1>::kRing == L.plan->stages)
+        return launch_sk<kFp16In, 1, NC>(L, partials, counts, s);
+    return launch_sk<kFp16In, 2, NC>(L, partials, counts, s);
+}
+
 template <bool kFp16In>
-cudaError_t launch_kps(const TcLaunch& L, float* partials, uint32_t* counts, cudaStream_t s) {
-    switch (kRingKBlocks / L.plan->stages) {
-        case 1: return launch_sk<kFp16In, 1>(L, partials, counts, s);
-        case 4: return launch_sk<kFp16In, 4>(L, partials, counts, s);
-        default: return launch_sk<kFp16In, 2>(L, partials, counts, s);
+cudaError_t launch_in(const TcLaunch& L, float* partials, uint32_t* counts, cudaStream_t s) {
+    switch (nc_for(L.M)) {
+        case 16: return launch_nc<kFp16In, 16>(L, partials, counts, s);
+        case 32: return launch_nc<kFp16In, 32>(L, partials, counts, s);
+        case 64: return launch_nc<kFp16In, 64>(L, partials, counts, s);
+        default: return launch_nc<kFp16In, 128>(L, partials, counts, s);
     }
 }
 
@@ -451,25 +537,25 @@ cudaError_t launch_kps(const TcLaunch& L, float* partials, uint32_t* counts, cud
 
 void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p) {
     const int bk = fp16_in ? 64 : 128;
+    const int nc = nc_for(M);
     const int64_t tiles = (N + kRows - 1) / kRows;
     const int64_t units = tiles * ((K + bk - 1) / bk);
-    p->block_m = kCols;
+    p->block_m = nc;
     p->block_n = kRows;
     p->block_k = bk;
-    p->stages = kRingKBlocks / splitk_kps();
+    p->stages = ring_kblocks(nc) / splitk_kps();
     p->tiles = static_cast<int>(tiles);
     p->grid = static_cast<int>(units < sm_count ? units : sm_count);
-    p->smem_bytes = kSkSmemBytes;
-    (void)M;
+    p->smem_bytes = smem_for_nc(nc);
 }
 
-cudaError_t launch_gemm_skinny(const TcLaunch& L, float* partials, uint32_t* counts,
+cudaError_t launch_gemm_skinny(const TcLaunch& L, float* partials, uint32_t* counts, int max_cols,
                                cudaStream_t s) {
-    if (L.M < 1 || L.M > kCols || L.plan->tiles > kSkinnyMaxTiles || partials == nullptr ||
-        counts == nullptr)
+    if (L.M < 1 || L.M > kSplitkMaxCols || nc_for(L.M) > max_cols ||
+        L.plan->tiles > kSkinnyMaxTiles || partials == nullptr || counts == nullptr)
         return cudaErrorInvalidValue;
-    return L.fp16_in ? launch_kps<true>(L, partials, counts, s)
-                     : launch_kps<false>(L, partials, counts, s);
+    return L.fp16_in ? launch_in<true>(L, partials, counts, s)
+                     : launch_in<false>(L, partials, counts, s);
 }
 
 }  // namespace dg

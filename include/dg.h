@@ -15,8 +15,8 @@
  *            owned by the caller.  The library allocates nothing per call and
  *            takes no workspace argument.  The first call on a device (or
  *            dg_init) allocates a 16-byte device status word and a split-K
- *            workspace (two 16 x 128 FP32 partial tiles per SM and 8192
- *            counters, 2.4 MB on 152 SMs) that live until exit.  Split-K
+ *            workspace (two 128 x 128 FP32 partial tiles per SM and 8192
+ *            counters, 20 MB on 152 SMs) that live until exit.  Split-K
  *            GEMMs (plan path 4) issued on a second, third, ... stream get a
  *            workspace of their own (same size, kept until exit) on that
  *            stream's first such call, so calls on different streams may run
@@ -117,7 +117,9 @@ dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale,
  * ([DG-FP16] §2.1 and §4.1, the decode QKV projection); 3 <= M <= 16 a
  * split-K tensor-core kernel (operands swapped, K spread over every SM);
  * larger M the tiled tensor-core kernel with a tile chosen per shape
- * (dg_gemm_plan).  K tails are zero-filled by the tensor-memory loads and M/N
+ * (dg_gemm_plan), or for 17 <= M <= 128 the split-K kernel where the tiled
+ * one would leave SMs idle and a time estimate favours split-K (few rows of
+ * A against a long K).  K tails are zero-filled by the tensor-memory loads and M/N
  * edges are predicated stores ([FP8-guide] §3.3).
  */
 dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M,
@@ -262,10 +264,11 @@ dg_status dg_convert_f16(const float* x, int64_t n, const float* factor,
  */
 typedef struct {
     int path;       /* 0 no-op, 1 zero-fill (K == 0), 2 GEMV, 3 tensor core,
-                       4 split-K tensor core for M <= 16 (operands swapped:
-                       block_m = 16 padded rows of A, block_n = 128 rows of
-                       B per tile, K blocks of all tiles spread over grid
-                       CTAs)                                                */
+                       4 split-K tensor core for M <= 16, and for
+                       M <= 128 where it is estimated faster (operands
+                       swapped: block_m = 16, 32, 64 or 128 padded rows of
+                       A, block_n = 128 rows of B per tile, K blocks of all
+                       tiles spread over grid CTAs)                         */
     int block_m;    /* output rows per tile (tensor-core paths)             */
     int block_n;    /* output columns per tile                              */
     int block_k;    /* K elements per pipeline stage                        */

@@ -209,7 +209,27 @@ def test_plan_paths_and_tiles(L):
         assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=sm)["path"] == 3
     finally:
         del os.environ["DG_SPLITK"]
-    assert dg.dg_gemm_plan(17, 12288, 4096, sm_count=sm)["path"] == 3
+    # 17 <= M <= 128: split-K only where the tiled plan leaves SMs idle and the
+    # time estimate favours it (few columns of A, or a long K per tile)
+    for m in (17, 32):
+        p = dg.dg_gemm_plan(m, 4096, 4096, sm_count=sm)
+        assert p["path"] == 4 and p["block_m"] == 32 and p["stages"] == 5
+    p = dg.dg_gemm_plan(64, 4096, 11008, sm_count=sm)
+    assert p["path"] == 4 and p["block_m"] == 64 and p["stages"] == 4
+    p = dg.dg_gemm_plan(64, 4096, 11008, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16, sm_count=sm)
+    assert p["path"] == 4 and p["block_k"] == 64
+    for m, n, k in ((17, 12288, 4096), (33, 4096, 4096), (64, 4096, 4096), (128, 4096, 4096),
+                    (64, 1024, 4096), (128, 32768, 4096), (129, 4096, 4096)):
+        assert dg.dg_gemm_plan(m, n, k, sm_count=sm)["path"] == 3, (m, n, k)
+    os.environ["DG_SPLITK"] = "1"
+    try:
+        for m, nc in ((33, 64), (64, 64), (65, 128), (128, 128)):
+            p = dg.dg_gemm_plan(m, 4096, 4096, sm_count=sm)
+            assert p["path"] == 4 and p["block_m"] == nc and p["smem_bytes"] <= 232448
+        assert dg.dg_gemm_plan(128, 32768, 4096, sm_count=sm)["path"] == 4
+        assert dg.dg_gemm_plan(129, 4096, 4096, sm_count=sm)["path"] == 3
+    finally:
+        del os.environ["DG_SPLITK"]
     assert dg.dg_gemm_plan(16, 128 * 8192 + 1, 64, sm_count=sm)["path"] == 3   # too many tiles
     os.environ["DG_GEMV_MAX_M"] = "16"
     try:

@@ -43,6 +43,7 @@ def _amax_bound(R, S, sa, sb):
     (7, 300, 512, "0", 2),        # GEMV, several rows (crossover raised to 16)
     (7, 300, 512, "0", 4),        # the same shape on the split-K kernel
     (16, 1000, 1040, "0", 4),     # split-K, every tile split across CTAs
+    (65, 1000, 1040, "0", 4),     # split-K (forced), MMA N = 128
     (65, 1000, 1040, "0", 3),     # single CTA
     (129, 777, 272, "0", 3),      # single CTA, ragged
     (300, 777, 272, "1", 3),      # CTA pairs, odd CTA partly out of range
@@ -52,6 +53,8 @@ def test_output_amax_matches_oracle(M, N, K, pairs, path):
     os.environ["DG_2CTA"] = pairs
     if path == 2:
         os.environ["DG_GEMV_MAX_M"] = "16"
+    if path == 4 and M > 16:
+        os.environ["DG_SPLITK"] = "1"
     try:
         assert dg.dg_gemm_plan(M, N, K, dg.DG_E4M3, dg.DG_BF16)["path"] == path
         A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
@@ -73,6 +76,7 @@ def test_output_amax_matches_oracle(M, N, K, pairs, path):
     finally:
         os.environ.pop("DG_2CTA", None)
         os.environ.pop("DG_GEMV_MAX_M", None)
+        os.environ.pop("DG_SPLITK", None)
 
 
 def test_delayed_scaling_round_trip():

@@ -1,5 +1,5 @@
-"""Split-K tensor-core path for skinny GEMMs (plan path 4: M <= 16, operands
-swapped, K blocks spread over every SM, partial tiles added in a fixed
+"""Split-K tensor-core path for skinny GEMMs (plan path 4: M <= 16, and
+M <= 128 where the tiled kernels would leave SMs idle; operands swapped, K blocks spread over every SM, partial tiles added in a fixed
 order by the CTA that finishes a tile last) against the CPU oracle.
 
 Covers ragged N (a partial last tile of 128 rows of B) and ragged K (a
@@ -68,6 +68,67 @@ def test_splitk_bf16_matches_oracle(M, N, K):
     R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
     d = bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N))
     check_bf16_like(d, R, S, sa_ref, sb_ref)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (17, 1000, 1040),    # MMA N = 32
+    (32, 4096, 1024),
+    (33, 2000, 2048),    # MMA N = 64, ragged M
+    (64, 4096, 4096),
+    (65, 1000, 1040),    # MMA N = 128, ragged M; 8 tiles x 9 K blocks
+    (100, 777, 3008),    # ragged N, 23.5 K blocks
+    (128, 4096, 2048),
+])
+def test_splitk_wide_bf16_matches_oracle(M, N, K):
+    """17 <= M <= 128: MMA N = 32 / 64 / 128 columns of A per CTA, the
+    partial slots and the fixup walked 16 columns at a time."""
+    os.environ["DG_SPLITK"] = "1"
+    try:
+        p = _plan(M, N, K)
+        assert p["block_m"] == (32 if M <= 32 else 64 if M <= 64 else 128), p
+        qa, qb, sa, sb, qa_ref, qb_ref, sa_ref, sb_ref = _fp8_case(M, N, K)
+        buf, D = guarded(M * N, torch.int16, 0x7FFF)
+        dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        check_guards(buf, M * N, 0x7FFF)
+        R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+        d = bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N))
+        check_bf16_like(d, R, S, sa_ref, sb_ref)
+    finally:
+        os.environ.pop("DG_SPLITK", None)
+
+
+@pytest.mark.parametrize("M,N,K", [(48, 1000, 2080), (120, 640, 1040)])
+def test_splitk_wide_e4m3_out_and_fp16(M, N, K):
+    os.environ["DG_SPLITK"] = "1"
+    try:
+        _plan(M, N, K)
+        A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+        qa_ref, sa, _ = oracle.quantize_tensor(A)
+        qb_ref, sb, _ = oracle.quantize_tensor(B)
+        R = oracle.gemm_e4m3(qa_ref, qb_ref, with_abs=False)
+        sd = np.float32(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))) / 448.0)
+        qa, _, sa_d = gpu_quantize(A)
+        qb, _, sb_d = gpu_quantize(B)
+        sdt = scalar()
+        sdt[0] = float(sd)
+        buf, D = guarded(M * N, torch.uint8, 0x7F)
+        dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, sdt, dg.DG_E4M3, M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        check_guards(buf, M * N, 0x7F)
+        check_e4m3(D.cpu().numpy().reshape(M, N), R, sa, sb, sd)
+        _plan(M, N, K, dg.DG_FP16)
+        A16, B16 = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
+        buf16, D16 = guarded(M * N, torch.int16, 0x7FFF)
+        dg.dg_hgemm(dev(A16.view(np.int16)), dev(B16.view(np.int16)), D16, dg.DG_FP16,
+                    M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        check_guards(buf16, M * N, 0x7FFF)
+        R16, S16 = oracle.hgemm(A16, B16)
+        check_bf16_like(fp16_bits_to_f64(D16.cpu().numpy().view(np.uint16).reshape(M, N)),
+                        R16, S16, 1.0, 1.0, "FP16")
+    finally:
+        os.environ.pop("DG_SPLITK", None)
 
 
 def test_splitk_m1_when_forced():
