@@ -97,6 +97,7 @@ struct SkParams {
     uint32_t* counts;      // [tiles]
     int tiles;             // ceil(N / 128)
     int kblocks;           // ceil(K / BK)
+    int prefetch_kblocks;  // B boxes of its range a CTA moves into L2 up front
 };
 
 // CTA i's range of units is [range_start(i), range_start(i + 1)).
@@ -189,10 +190,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const int kb_begin = static_cast<int>(u_begin - static_cast<int64_t>(t_begin) * KB);
 
     if (warp == 0 && lane == 0) {
-        // Warm L2 with this CTA's first ring of B blocks while the preceding
+        // Warm L2 with the start of this CTA's range of B while the preceding
         // kernel finishes (a prefetch only moves lines into L2).
         int t = t_begin, kb = kb_begin;
-        for (int i = 0; i < kRingKBlocks && i < n_units; ++i) {
+        for (int i = 0; i < p.prefetch_kblocks && i < n_units; ++i) {
             tma_prefetch_l2_2d(&tmap_w, kb * kBK, t * kRows);
             if (++kb == KB) { kb = 0; ++t; }
         }
@@ -452,6 +453,16 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
 // ------------------------------------------------------------- host side
 
+// B boxes each CTA prefetches into L2 before its dependency wait:
+// DG_SPLITK_PREFETCH=n (sweeps, 0..256), default one ring.
+int splitk_prefetch_kblocks(int ring) {
+    if (const char* v = std::getenv("DG_SPLITK_PREFETCH")) {
+        const int n = std::atoi(v);
+        if (n >= 0 && n <= 256) return n;
+    }
+    return ring;
+}
+
 template <bool kFp16In, int KPS, int NC>
 cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cudaStream_t s) {
     using C = SkCfg<NC, KPS>;
@@ -491,6 +502,7 @@ cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cuda
     prm.tiles = L.plan->tiles;
     const int bk = kFp16In ? 64 : 128;
     prm.kblocks = (L.K + bk - 1) / bk;
+    prm.prefetch_kblocks = splitk_prefetch_kblocks(C::kRing);
     return launch_kernel(gemm_skinny_kernel<kFp16In, KPS, NC>, dim3(L.plan->grid), dim3(kThreads),
                          C::kSmemBytes, s, tw, tx, prm);
 }
