@@ -297,8 +297,7 @@ def kernel_cases(torch, dg):
                                          dg.DG_BF16, stream=s)
         return fn, 2.0 * Mq * Nq * Kq, Nq * Kq + Mq * Kq + Mq * Nq * 2, "hbm", f"{nb} rotating copies"
 
-    def gemv_m(m):
-        Nq, Kq = 12288, 4096
+    def gemv_m(m, Nq=12288, Kq=4096):
         nb = ncopies(Nq * Kq)
         As = [codes((m, Kq), 70 + i) for i in range(nb)]
         Bs = [codes((Nq, Kq), 80 + i) for i in range(nb)]
@@ -433,6 +432,10 @@ def kernel_cases(torch, dg):
         "qkv_m64_64x12288x4096": lambda: gemv_m(64),
         "qkv_m128_128x12288x4096": lambda: gemv_m(128),
         "qkv_m256_256x12288x4096": lambda: gemv_m(256),
+        # a decode-batch FFN down projection (long K): split-K up to M = 64
+        "ffn_down_m16_16x4096x11008": lambda: gemv_m(16, 4096, 11008),
+        "ffn_down_m64_64x4096x11008": lambda: gemv_m(64, 4096, 11008),
+        "ffn_down_m128_128x4096x11008": lambda: gemv_m(128, 4096, 11008),
         "fp8_gemm_4096": lambda: fp8_sq(4096, dg.DG_BF16),
         "fp8_gemm_8192_e4m3out": lambda: fp8_sq(8192, dg.DG_E4M3),
         "fp16_hgemm_4096": lambda: hgemm(4096),
