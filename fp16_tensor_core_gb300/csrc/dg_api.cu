@@ -129,13 +129,14 @@ void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& 
 
 // Launch-time estimates (microseconds) for choosing between the tiled and
 // the split-K kernels at 17 <= M <= 128, fitted to graph-replayed GB300
-// timings with B read from HBM (M = 16..128 against N = 1024..28672,
-// K = 4096..14336).
+// timings with B read from HBM (M = 16..128 against N = 1000..28672,
+// K = 1040..14336; 45 shapes, the faster kernel chosen on 43).
 //  * Tiled: a fixed ~3 us plus the larger of one CTA's operand stream at its
 //    single-SM rate (~115 GB/s) and all bytes at ~6 TB/s.
-//  * Split-K: ~5.3 us fixed, B at ~6.5 TB/s, and for each 16 columns of A
-//    past the first, the last-arriving CTA's extra fixup pass: ~1.2 us plus
-//    ~0.6 us per four partial tiles it reads (ceil(grid / tiles) of them).
+//  * Split-K: ~4.6 us fixed, B at ~6.9 TB/s (0.145 us per MB), and for each
+//    16 columns of A past the first, the finishing CTAs' extra pass over the
+//    partial tiles: ~1.1 us plus ~0.16 us per other segment of a tile
+//    (ceil(grid / tiles) of them).
 double tiled_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const dg_plan& p) {
     const double elem = fp16_in ? 2.0 : 1.0;
     const int64_t kblocks = (K + p.block_k - 1) / p.block_k;
@@ -150,10 +151,9 @@ double splitk_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const d
     const double elem = fp16_in ? 2.0 : 1.0;
     const int64_t chunks = (M + 15) / 16;
     const int64_t others = (p.grid + p.tiles - 1) / p.tiles;
-    const int64_t groups = (others + 3) / 4;
-    const double b_bytes = static_cast<double>(N) * static_cast<double>(K) * elem;
-    return 5.3 + b_bytes / 6.5e6 +
-           static_cast<double>(chunks - 1) * (1.2 + 0.6 * static_cast<double>(groups));
+    const double b_mb = static_cast<double>(N) * static_cast<double>(K) * elem / 1e6;
+    return 4.6 + 0.145 * b_mb +
+           static_cast<double>(chunks - 1) * (1.1 + 0.16 * static_cast<double>(others));
 }
 
 // Shared path selection for dg_gemm_plan and the GEMM entry points.

@@ -80,6 +80,9 @@ struct SkCfg {
     static_assert(kRing % KPS == 0 && kStages <= 12, "ring");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
     static_assert(kXBytes % 1024 == 0, "1024-byte aligned A blocks (128-byte swizzle atoms)");
+    // barriers: full/empty per stage, 2 + 2 accumulator, drain, fix-up;
+    // then the TMEM address, the abort flag and the last-arrival flag
+    static_assert((2 * kStages + 6) * 8 + 3 * 4 <= kBarBytes, "barrier block");
 };
 
 struct SkParams {
@@ -116,15 +119,27 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int G, int64_t units) {
 // (slot 2c); c_first's segment is its first only if its range starts exactly
 // at the tile.
 
-// Scale, convert and store one output element.
-__device__ __forceinline__ void store_one(const SkParams& p, int m, int n, float v) {
-    const int64_t off = static_cast<int64_t>(m) * p.N + n;
+// Scale, convert and store rows c0 .. c0 + jn - 1 of A's side (m) at column
+// n: one branch on the output type, then one strided store per row.
+__device__ __forceinline__ void store_chunk16(const SkParams& p, int c0, int n, int jn,
+                                              const float (&v)[16], float alpha) {
+    const int64_t ld = p.N;
+    const int64_t off = static_cast<int64_t>(c0) * ld + n;
     if (p.out_kind == kOutE4M3) {
-        static_cast<uint8_t*>(p.D)[off] = static_cast<uint8_t>(f32x2_to_e4m3x2(v, 0.0f) & 0xFFu);
+        uint8_t* d = static_cast<uint8_t*>(p.D) + off;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < jn) d[j * ld] = static_cast<uint8_t>(f32x2_to_e4m3x2(v[j] * alpha, 0.0f) & 0xFFu);
     } else if (p.out_kind == kOutFP16) {
-        static_cast<uint16_t*>(p.D)[off] = static_cast<uint16_t>(f32x2_to_f16x2(v, 0.0f) & 0xFFFFu);
+        uint16_t* d = static_cast<uint16_t*>(p.D) + off;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < jn) d[j * ld] = static_cast<uint16_t>(f32x2_to_f16x2(v[j] * alpha, 0.0f) & 0xFFFFu);
     } else {
-        static_cast<uint16_t*>(p.D)[off] = static_cast<uint16_t>(f32x2_to_bf16x2(v, 0.0f) & 0xFFFFu);
+        uint16_t* d = static_cast<uint16_t*>(p.D) + off;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < jn) d[j * ld] = static_cast<uint16_t>(f32x2_to_bf16x2(v[j] * alpha, 0.0f) & 0xFFFFu);
     }
 }
 
@@ -148,7 +163,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
     uint64_t* acc_full = empty + kStages;   // [2]
     uint64_t* acc_empty = acc_full + 2;     // [2]
     uint64_t* drain = acc_empty + 2;        // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* fix_bar = drain + 1;          // [1] partial tiles staged for the fix-up
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fix_bar + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     volatile int* last_flag = abort_flag + 1;
 
@@ -163,6 +179,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(&acc_empty[b], 4);
         }
         mbar_init(drain, 1);
+        mbar_init(fix_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_mbar_init();
@@ -360,6 +377,42 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 named_bar_sync(kEpiBar, kEpiThreads);
                 finish = *last_flag != 0;
             }
+            // When this is the CTA's last segment its ring of K blocks is idle:
+            // one thread bulk-copies every other segment's partial tile into
+            // it on one barrier, and the sum below reads shared memory instead
+            // of making L2 round trips for each 16 columns and each four
+            // segments.  At NC = 16 with at most three other segments (one
+            // chunk, one group of direct loads) the loads measured as fast.
+            const int others = c_last - c_first;
+            const int quads = (min(p.M, NC) + 3) >> 2;   // column quads that hold rows of A
+            const uint32_t slot_bytes = static_cast<uint32_t>(quads) * kRows * 16u;
+            const bool staged = (NC >= 32 || others >= 4) && finish && others > 0 && left == 0 &&
+                                static_cast<int64_t>(others + 1) * slot_bytes <=
+                                    static_cast<int64_t>(kRingKBlocks) * kKBBytes;
+            if (staged) {
+                if (threadIdx.x == 4 * 32) {
+                    // the partials were published through the generic proxy
+                    // and acquired by this thread's arrival atomic
+                    fence_proxy_async_global();
+                    mbar_arrive_expect_tx(fix_bar, static_cast<uint32_t>(others) * slot_bytes);
+                    // segment c goes to position c - c_first; the own position
+                    // is filled from tensor memory below
+                    for (int c = c_first; c <= c_last; ++c) {
+                        if (c == me) continue;
+                        const int slot = c == c_first ? first_slot : 2 * c;
+                        bulk_load_g2s(smem + static_cast<uint32_t>(c - c_first) * slot_bytes,
+                                      reinterpret_cast<const float4*>(p.partials) +
+                                          static_cast<int64_t>(slot) * (NC / 4) * kRows,
+                                      slot_bytes, fix_bar);
+                    }
+                }
+                const bool landed = wait_bounded(fix_bar, 0, ctl);
+                if (!named_bar_and(kEpiBar, kEpiThreads, landed)) {
+                    // let the copies land before the CTA's shared memory is released
+                    if (threadIdx.x == 4 * 32) wait_bounded(fix_bar, 0, ctl, false);
+                    break;
+                }
+            }
             if (finish) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < NC && c0 < p.M; c0 += 16) {
@@ -375,7 +428,45 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
 #pragma unroll
                         for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
                     }
-                    if (c_last > c_first) {
+                    if (staged) {
+                        // Segments in order c_first .. c_last from the staged
+                        // copies, the own one written into its position first
+                        // (this thread reads back only what it wrote itself).
+                        float4* stage = reinterpret_cast<float4*>(smem) + (c0 >> 2) * kRows + r;
+                        const int seg_stride = quads * kRows;   // float4s per position
+                        float4* own = stage + (me - c_first) * seg_stride;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            if (c0 + 4 * g < p.M)
+                                own[g * kRows] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2],
+                                                             v[4 * g + 3]);
+                        float4 sum[4];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            sum[g] = c0 + 4 * g < p.M ? stage[g * kRows]
+                                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
+                        for (int i = 1; i <= others; ++i) {
+                            const float4* w = stage + i * seg_stride;
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                if (c0 + 4 * g < p.M) {
+                                    const float4 x = w[g * kRows];
+                                    sum[g].x += x.x;
+                                    sum[g].y += x.y;
+                                    sum[g].z += x.z;
+                                    sum[g].w += x.w;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            v[4 * g] = sum[g].x;
+                            v[4 * g + 1] = sum[g].y;
+                            v[4 * g + 2] = sum[g].z;
+                            v[4 * g + 3] = sum[g].w;
+                        }
+                    } else if (c_last > c_first) {
                         // Sum the segments in order c_first .. c_last, the own
                         // one from tensor memory, the others from their slots.
                         // The slots of four segments are requested together
@@ -418,13 +509,11 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         for (int j = 0; j < 16; ++j) v[j] = sum[j];
                     }
                     if (n < p.N) {
+                        const int jn = min(16, p.M - c0);   // rows of A in this chunk
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (c0 + j < p.M) {
-                                amax_bits = max(amax_bits, __float_as_uint(v[j]) & 0x7FFFFFFFu);
-                                store_one(p, c0 + j, n, v[j] * alpha);
-                            }
-                        }
+                        for (int j = 0; j < 16; ++j)
+                            if (j < jn) amax_bits = max(amax_bits, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+                        store_chunk16(p, c0, n, jn, v, alpha);
                     }
                 }
             }

@@ -214,11 +214,13 @@ def test_plan_paths_and_tiles(L):
     for m in (17, 32):
         p = dg.dg_gemm_plan(m, 4096, 4096, sm_count=sm)
         assert p["path"] == 4 and p["block_m"] == 32 and p["stages"] == 5
+    p = dg.dg_gemm_plan(48, 4096, 4096, sm_count=sm)
+    assert p["path"] == 4 and p["block_m"] == 64
     p = dg.dg_gemm_plan(64, 4096, 11008, sm_count=sm)
     assert p["path"] == 4 and p["block_m"] == 64 and p["stages"] == 4
     p = dg.dg_gemm_plan(64, 4096, 11008, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16, sm_count=sm)
     assert p["path"] == 4 and p["block_k"] == 64
-    for m, n, k in ((17, 12288, 4096), (33, 4096, 4096), (64, 4096, 4096), (128, 4096, 4096),
+    for m, n, k in ((17, 12288, 4096), (64, 4096, 4096), (128, 4096, 4096),
                     (64, 1024, 4096), (128, 32768, 4096), (129, 4096, 4096)):
         assert dg.dg_gemm_plan(m, n, k, sm_count=sm)["path"] == 3, (m, n, k)
     os.environ["DG_SPLITK"] = "1"
