@@ -170,7 +170,7 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     // GEMV for M <= 2, split-K tensor cores up to M = 16.  Measured on GB300
     // for N = 12288 (B read from HBM, graph-replayed launches): at K = 4096
     // the GEMV takes 10.2 us at M = 1 and grows with M (its FMA count), the
-    // split-K kernel a flat 11.3-11.7 us for M = 1..16; at K = 1024 4.4
+    // split-K kernel a flat 11.1-11.5 us for M = 1..16; at K = 1024 4.4
     // against 6.9 us.  DG_GEMV_MAX_M (0..16) moves the crossover.
     int gemv_max_m = 2;
     if (const char* v = std::getenv("DG_GEMV_MAX_M")) {
