@@ -130,13 +130,13 @@ void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& 
 // Launch-time estimates (microseconds) for choosing between the tiled and
 // the split-K kernels at 17 <= M <= 128, fitted to graph-replayed GB300
 // timings with B read from HBM (M = 16..128 against N = 1000..28672,
-// K = 1040..14336; 45 shapes, the faster kernel chosen on 43).
+// K = 1040..14336; 45 shapes, the faster kernel chosen on 44).
 //  * Tiled: a fixed ~3 us plus the larger of one CTA's operand stream at its
 //    single-SM rate (~115 GB/s) and all bytes at ~6 TB/s.
-//  * Split-K: ~4.6 us fixed, B at ~6.9 TB/s (0.145 us per MB), and for each
-//    16 columns of A past the first, the finishing CTAs' extra pass over the
-//    partial tiles: ~1.1 us plus ~0.16 us per other segment of a tile
-//    (ceil(grid / tiles) of them).
+//  * Split-K: ~2.1 us fixed, B at ~5.8 TB/s (0.173 us per MB), ~0.24 us per
+//    segment a tile is cut into (s = ceil(grid / tiles)), and for each 16
+//    columns of A past the first, the finishing CTAs' extra pass over the
+//    partial tiles: ~1 us plus ~0.145 us per segment.
 double tiled_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const dg_plan& p) {
     const double elem = fp16_in ? 2.0 : 1.0;
     const int64_t kblocks = (K + p.block_k - 1) / p.block_k;
@@ -152,8 +152,8 @@ double splitk_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const d
     const int64_t chunks = (M + 15) / 16;
     const int64_t others = (p.grid + p.tiles - 1) / p.tiles;
     const double b_mb = static_cast<double>(N) * static_cast<double>(K) * elem / 1e6;
-    return 4.6 + 0.145 * b_mb +
-           static_cast<double>(chunks - 1) * (1.1 + 0.16 * static_cast<double>(others));
+    return 2.1 + 0.173 * b_mb + 0.24 * static_cast<double>(others) +
+           static_cast<double>(chunks - 1) * (0.98 + 0.145 * static_cast<double>(others));
 }
 
 // Shared path selection for dg_gemm_plan and the GEMM entry points.
@@ -211,7 +211,7 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
         sk.path = 4;
         plan_skinny(M, N, K, fp16_in, sm_count, &sk);
         if (splitk_forced || splitk_estimate_us(M, N, K, fp16_in, sk) <
-                                 0.9 * tiled_estimate_us(M, N, K, fp16_in, *p))
+                                 tiled_estimate_us(M, N, K, fp16_in, *p))
             *p = sk;
     }
     return DG_OK;

@@ -646,7 +646,17 @@ void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg
     p->block_k = bk;
     p->stages = ring_kblocks(nc) / splitk_kps();
     p->tiles = static_cast<int>(tiles);
-    p->grid = static_cast<int>(units < sm_count ? units : sm_count);
+    // With room for at least two CTAs per tile, launch a whole multiple of
+    // the tile count, so every CTA covers the same fraction of one tile (one
+    // segment each, the same number of segments in every tile); otherwise
+    // every SM, with ranges that cross tile edges.
+    const int64_t per_tile = sm_count / tiles;
+    const int64_t g = per_tile >= 2 ? per_tile * tiles : sm_count;
+    p->grid = static_cast<int>(units < g ? units : g);
+    if (const char* v = std::getenv("DG_SPLITK_GRID")) {   // sweeps: CTAs per launch
+        const int64_t g = std::atoll(v);
+        if (g >= 1 && g <= sm_count && g <= units) p->grid = static_cast<int>(g);
+    }
     p->smem_bytes = smem_for_nc(nc);
 }
 

@@ -199,6 +199,10 @@ def test_plan_paths_and_tiles(L):
         assert p["path"] == 4 and p["block_m"] == 16 and p["block_n"] == 128
         assert p["tiles"] == 96 and p["grid"] == sm and p["block_k"] == 128
         assert p["smem_bytes"] <= 232448
+    # few tiles: a whole multiple of the tile count (every CTA one segment)
+    assert dg.dg_gemm_plan(16, 4096, 4096, sm_count=sm)["grid"] == 128    # 4 x 32 tiles
+    assert dg.dg_gemm_plan(16, 2048, 4096, sm_count=sm)["grid"] == 144    # 9 x 16 tiles
+    assert dg.dg_gemm_plan(16, 11008, 4096, sm_count=sm)["grid"] == sm    # 86 tiles: every SM
     # fewer K blocks than SMs: one per CTA
     p = dg.dg_gemm_plan(5, 200, 256, sm_count=sm)
     assert p["path"] == 4 and p["tiles"] == 2 and p["grid"] == 4
@@ -214,13 +218,15 @@ def test_plan_paths_and_tiles(L):
     for m in (17, 32):
         p = dg.dg_gemm_plan(m, 4096, 4096, sm_count=sm)
         assert p["path"] == 4 and p["block_m"] == 32 and p["stages"] == 5
-    p = dg.dg_gemm_plan(48, 4096, 4096, sm_count=sm)
-    assert p["path"] == 4 and p["block_m"] == 64
+    for m in (48, 64):
+        p = dg.dg_gemm_plan(m, 4096, 4096, sm_count=sm)
+        assert p["path"] == 4 and p["block_m"] == 64
+        assert p["grid"] == 128   # 4 CTAs for each of the 32 tiles
     p = dg.dg_gemm_plan(64, 4096, 11008, sm_count=sm)
     assert p["path"] == 4 and p["block_m"] == 64 and p["stages"] == 4
     p = dg.dg_gemm_plan(64, 4096, 11008, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16, sm_count=sm)
     assert p["path"] == 4 and p["block_k"] == 64
-    for m, n, k in ((17, 12288, 4096), (64, 4096, 4096), (128, 4096, 4096),
+    for m, n, k in ((17, 12288, 4096), (128, 4096, 4096),
                     (64, 1024, 4096), (128, 32768, 4096), (129, 4096, 4096)):
         assert dg.dg_gemm_plan(m, n, k, sm_count=sm)["path"] == 3, (m, n, k)
     os.environ["DG_SPLITK"] = "1"
