@@ -131,6 +131,49 @@ def test_splitk_wide_e4m3_out_and_fp16(M, N, K):
         os.environ.pop("DG_SPLITK", None)
 
 
+@pytest.mark.parametrize("M,N,K", [(48, 4096, 2048), (24, 2048, 1040)])
+def test_splitk_staged_fixup_all_outputs(M, N, K):
+    """Shapes whose finishing CTAs stage the other segments' partial tiles in
+    shared memory (32 or 16 tiles, a whole multiple of CTAs per tile, every
+    partial tile fits in the ring): BF16 and E4M3 out from E4M3 inputs and
+    FP16 out from FP16 inputs."""
+    os.environ["DG_SPLITK"] = "1"
+    try:
+        p = _plan(M, N, K)
+        assert p["grid"] % p["tiles"] == 0 and p["grid"] // p["tiles"] >= 2, p
+        A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+        qa_ref, sa, _ = oracle.quantize_tensor(A)
+        qb_ref, sb, _ = oracle.quantize_tensor(B)
+        qa, _, sa_d = gpu_quantize(A)
+        qb, _, sb_d = gpu_quantize(B)
+        R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+        buf, D = guarded(M * N, torch.int16, 0x7FFF)
+        dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, None, dg.DG_BF16, M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        check_guards(buf, M * N, 0x7FFF)
+        check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N)), R, S, sa, sb)
+        sd = np.float32(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))) / 448.0)
+        sdt = scalar()
+        sdt[0] = float(sd)
+        buf8, D8 = guarded(M * N, torch.uint8, 0x7F)
+        dg.dg_fp8_gemm(qa, qb, D8, sa_d, sb_d, sdt, dg.DG_E4M3, M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        check_guards(buf8, M * N, 0x7F)
+        check_e4m3(D8.cpu().numpy().reshape(M, N), R, sa, sb, sd)
+        p16 = _plan(M, N, K, dg.DG_FP16)
+        assert p16["grid"] % p16["tiles"] == 0, p16
+        A16, B16 = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
+        buf16, D16 = guarded(M * N, torch.int16, 0x7FFF)
+        dg.dg_hgemm(dev(A16.view(np.int16)), dev(B16.view(np.int16)), D16, dg.DG_FP16, M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        check_guards(buf16, M * N, 0x7FFF)
+        R16, S16 = oracle.hgemm(A16, B16)
+        check_bf16_like(fp16_bits_to_f64(D16.cpu().numpy().view(np.uint16).reshape(M, N)), R16, S16,
+                        1.0, 1.0, "FP16")
+    finally:
+        os.environ.pop("DG_SPLITK", None)
+
+
 def test_splitk_m1_when_forced():
     """M = 1 and 2 on the split-K kernel (the GEMV crossover moved to 0)."""
     os.environ["DG_GEMV_MAX_M"] = "0"
