@@ -130,9 +130,12 @@ void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& 
 // Launch-time estimates (microseconds) for choosing between the tiled and
 // the split-K kernels at 17 <= M <= 128, fitted to graph-replayed GB300
 // timings with B read from HBM (M = 16..128 against N = 1000..28672,
-// K = 1040..14336; 45 shapes, the faster kernel chosen on 44).
-//  * Tiled: a fixed ~3 us plus the larger of one CTA's operand stream at its
-//    single-SM rate (~115 GB/s) and all bytes at ~6 TB/s.
+// K = 1040..14336; 45 shapes, the faster kernel chosen on 42, the three
+// misses within 0.9 us).
+//  * Tiled: ~3.4 us fixed, plus the larger of ~0.26 us per K block for
+//    each wave of tiles (a CTA's pipeline refills at that rate whatever the
+//    tile width) and all bytes at ~6.5 TB/s, plus ~0.12 us per 1000 output
+//    elements of a tile (the epilogue's row-per-lane stores).
 //  * Split-K: ~2.1 us fixed, B at ~5.8 TB/s (0.173 us per MB), ~0.24 us per
 //    segment a tile is cut into (s = ceil(grid / tiles)), and for each 16
 //    columns of A past the first, the finishing CTAs' extra pass over the
@@ -140,11 +143,11 @@ void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& 
 double tiled_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const dg_plan& p) {
     const double elem = fp16_in ? 2.0 : 1.0;
     const int64_t kblocks = (K + p.block_k - 1) / p.block_k;
-    const int64_t tiles_per_cta = (p.tiles + p.grid - 1) / p.grid;
-    const double cta_bytes = static_cast<double>(tiles_per_cta) * static_cast<double>(kblocks) *
-                             static_cast<double>(p.block_m + p.block_n) * 128.0;
-    const double all_bytes = static_cast<double>(M + N) * static_cast<double>(K) * elem;
-    return 3.0 + std::max(cta_bytes / 1.15e5, all_bytes / 6.0e6);
+    const int64_t waves = (p.tiles + p.grid - 1) / p.grid;
+    const double all_mb = static_cast<double>(M + N) * static_cast<double>(K) * elem / 1e6;
+    const double tile_rows = static_cast<double>(std::min<int64_t>(M, p.block_m));
+    return 3.4 + std::max(0.26 * static_cast<double>(kblocks * waves), all_mb / 6.5) +
+           0.121 * tile_rows * static_cast<double>(p.block_n) / 1000.0;
 }
 
 double splitk_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const dg_plan& p) {
