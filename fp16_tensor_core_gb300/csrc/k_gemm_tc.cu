@@ -394,16 +394,17 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
         const double cost = static_cast<double>(waves) * bn / eff[i];
         if (i == 0 || cost < best_cost) { best = bn; best_cost = cost; }
     }
-    // A width that puts every tile in one wave (K up to 64 K blocks): the
-    // launch is bound by latency and each SM's own operand stream rather
-    // than by MMA efficiency, so the narrowest such tile (most CTAs, fewest
-    // bytes per CTA) wins, and CTA pairs only add cluster start-up.
-    // Measured on GB300 (BF16 out, graph-replayed), against the estimate
-    // below: 256^3 3.2 us (128 x 64) vs 5.2 (pairs 256 x 128); 1024^3 5.9
-    // vs 8.1; 129 x 1000 x 1040 6.8 vs 7.7; 1024 x 1024 x 8192 20.9 vs
-    // 24.0; FP16 1024^3 8.1 vs 10.3 -- faster on all 23 shapes tried, equal
-    // at 256 x 12288 x 4096.  DG_ONE_WAVE=0 turns the rule off and
-    // DG_ONE_WAVE_KB sets its K-block limit (sweeps).
+    // A width that puts every tile in one wave (K up to 64 K blocks, up to
+    // 32 for widths above 128): the launch is bound by latency and each
+    // SM's own operand stream rather than by MMA efficiency, so the
+    // narrowest such tile (most CTAs, fewest bytes per CTA) wins, and CTA
+    // pairs only add cluster start-up.  Measured on GB300 (BF16 out,
+    // graph-replayed), against the estimate below: 256^3 3.2 us (128 x 64)
+    // vs 5.2 (pairs 256 x 128); 1024^3 5.9 vs 8.1; 129 x 1000 x 1040 6.8 vs
+    // 7.7; 1024 x 1024 x 8192 20.9 vs 24.0; FP16 1024^3 8.1 vs 10.3;
+    // 1024 x 4096 x 4096 15.5 vs 17.2 (128 x 224); equal at 256 x 12288 x
+    // 4096.  DG_ONE_WAVE=0 turns the rule off and DG_ONE_WAVE_KB sets its
+    // K-block limit (sweeps).
     const int64_t kblocks = (K + (fp16_in ? 64 : 128) - 1) / (fp16_in ? 64 : 128);
     const char* ow = std::getenv("DG_ONE_WAVE");
     bool one_wave = false;
@@ -412,8 +413,13 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     if (!(ow != nullptr && ow[0] == '0') && kblocks <= max_kb) {
         for (int i = 5; i >= 0; --i) {   // narrowest first
             if (num_m * ((N + cand[i] - 1) / cand[i]) <= sm_count) {
-                best = cand[i];
-                one_wave = true;
+                // past 32 K blocks a wide tile is MMA-bound enough for the
+                // pairs' efficiency to win (2048^2 x 8192: 26.1 us as pairs
+                // vs 27.6 as 128 x 256 single tiles)
+                if (kblocks <= 32 || cand[i] <= 128) {
+                    best = cand[i];
+                    one_wave = true;
+                }
                 break;
             }
         }
