@@ -290,6 +290,45 @@ def test_splitk_graph_replay():
         assert torch.equal(D, direct)
 
 
+@pytest.mark.parametrize("M,N,K", [(64, 4096, 4096), (16, 1024, 4096), (24, 2048, 1040)])
+def test_splitk_staged_fixup_repeatable_back_to_back(M, N, K):
+    """Eight launches per graph replay, 50 replays: every output equals the
+    first launch's bit for bit.  The finishing CTAs copy the other segments'
+    partial tiles into shared memory with bulk copies after their acquiring
+    arrival atomic; a missing ordering would show as an occasional stale
+    partial, so a different sum."""
+    os.environ["DG_SPLITK"] = "1"
+    try:
+        p = _plan(M, N, K)
+        assert p["grid"] % p["tiles"] == 0
+        qa, qb, sa, sb, *_ = _fp8_case(M, N, K)
+        ref = torch.empty((M, N), dtype=torch.int16, device="cuda")
+        dg.dg_fp8_gemm(qa, qb, ref, sa, sb, None, dg.DG_BF16)
+        assert dg.dg_sync_status() == dg.DG_OK
+        outs = [torch.empty_like(ref) for _ in range(8)]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for D in outs:
+                dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for D in outs:
+                dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, stream=s)
+        for r in range(50):
+            g.replay()
+            if r % 10 == 9:
+                torch.cuda.synchronize()
+                for D in outs:
+                    assert torch.equal(D, ref)
+        torch.cuda.synchronize()
+        assert dg.dg_sync_status() == dg.DG_OK
+    finally:
+        os.environ.pop("DG_SPLITK", None)
+
+
 def test_splitk_timeout_then_recovers():
     """One stage left unloaded: the bounded wait runs out, the call reports
     DG_ERR_TIMEOUT, dg_sync_status clears the arrival counters, and the next
