@@ -130,16 +130,16 @@ void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& 
 // Launch-time estimates (microseconds) for choosing between the tiled and
 // the split-K kernels at 17 <= M <= 128, fitted to graph-replayed GB300
 // timings with B read from HBM (M = 16..128 against N = 1000..28672,
-// K = 1040..14336; 45 shapes, the faster kernel chosen on 42, the three
+// K = 1040..14336; 45 shapes, the faster kernel chosen on 41, the four
 // misses within 0.9 us).
 //  * Tiled: ~3.4 us fixed, plus the larger of ~0.26 us per K block for
 //    each wave of tiles (a CTA's pipeline refills at that rate whatever the
 //    tile width) and all bytes at ~6.5 TB/s, plus ~0.12 us per 1000 output
 //    elements of a tile (the epilogue's row-per-lane stores).
-//  * Split-K: ~2.1 us fixed, B at ~5.8 TB/s (0.173 us per MB), ~0.24 us per
-//    segment a tile is cut into (s = ceil(grid / tiles)), and for each 16
-//    columns of A past the first, the finishing CTAs' extra pass over the
-//    partial tiles: ~1 us plus ~0.145 us per segment.
+//  * Split-K: ~2.2 us fixed, B at ~5.8 TB/s (0.172 us per MB), ~0.235 us
+//    per segment a tile is cut into (s = ceil(grid / tiles)), and for each
+//    16 columns of A past the first, the finishing CTAs' extra pass over
+//    the partial tiles: ~0.86 us plus ~0.058 us per segment.
 double tiled_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const dg_plan& p) {
     const double elem = fp16_in ? 2.0 : 1.0;
     const int64_t kblocks = (K + p.block_k - 1) / p.block_k;
@@ -155,8 +155,8 @@ double splitk_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const d
     const int64_t chunks = (M + 15) / 16;
     const int64_t others = (p.grid + p.tiles - 1) / p.tiles;
     const double b_mb = static_cast<double>(N) * static_cast<double>(K) * elem / 1e6;
-    return 2.1 + 0.173 * b_mb + 0.24 * static_cast<double>(others) +
-           static_cast<double>(chunks - 1) * (0.98 + 0.145 * static_cast<double>(others));
+    return 2.2 + 0.172 * b_mb + 0.235 * static_cast<double>(others) +
+           static_cast<double>(chunks - 1) * (0.86 + 0.058 * static_cast<double>(others));
 }
 
 // Shared path selection for dg_gemm_plan and the GEMM entry points.

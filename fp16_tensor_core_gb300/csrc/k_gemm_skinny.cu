@@ -50,9 +50,12 @@ namespace {
 
 constexpr int kRows = kSkinnyTileRows;            // MMA M: rows of B per tile
 constexpr int kWBytes = kRows * kBKBytes;         // 16 KB of B per K block
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
 constexpr uint32_t kEpiBar = 1;                   // named barrier of the epilogue warps
 constexpr uint32_t kEpiThreads = 128;
+// Hand-off to warps 0-3 for a CTA's last tile: valid, tile, accumulator,
+// first and last CTA of the tile, the first CTA's slot, staged.
+constexpr int kHelpInts = 7;
 
 // K blocks in flight per CTA for MMA N = nc (the rows of A, padded): as many
 // as fit in 227 KB of shared memory, rounded down to an even number.
@@ -80,9 +83,10 @@ struct SkCfg {
     static_assert(kRing % KPS == 0 && kStages <= 12, "ring");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
     static_assert(kXBytes % 1024 == 0, "1024-byte aligned A blocks (128-byte swizzle atoms)");
-    // barriers: full/empty per stage, 2 + 2 accumulator, drain, fix-up;
-    // then the TMEM address, the abort flag and the last-arrival flag
-    static_assert((2 * kStages + 6) * 8 + 3 * 4 <= kBarBytes, "barrier block");
+    // barriers: full/empty per stage, 2 + 2 accumulator, drain, fix-up,
+    // helpers; then the TMEM address, the abort flag, the last-arrival flag
+    // and the helpers' hand-off block
+    static_assert((2 * kStages + 7) * 8 + 3 * 4 + kHelpInts * 4 <= kBarBytes, "barrier block");
 };
 
 struct SkParams {
@@ -143,6 +147,123 @@ __device__ __forceinline__ void store_chunk16(const SkParams& p, int c0, int n, 
     }
 }
 
+// Adds up, scales and stores the 16-column chunks c0 = c0_begin,
+// c0_begin + c0_step, ... (c0 < NC, c0 < M) of a finished tile for the
+// calling thread's row r (its tensor-memory lane): the segments c_first ..
+// c_last in that order, the own one (CTA me) from tensor memory, the others
+// from the staged copies in shared memory or from their workspace slots.
+// `first` holds chunk 0 when the CTA published its own partial.
+template <int NC>
+__device__ __forceinline__ void finish_chunks(const SkParams& p, uint8_t* smem, uint32_t tacc,
+                                              int r, int n, int c0_begin, int c0_step, int me,
+                                              int c_first, int c_last, int first_slot,
+                                              bool staged, int quads, const float (&first)[16],
+                                              float alpha, uint32_t& amax_bits) {
+    const int others = c_last - c_first;
+#pragma unroll 1
+    for (int c0 = c0_begin; c0 < NC && c0 < p.M; c0 += c0_step) {
+        float v[16];
+        if (c_last > c_first && c0 == 0) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = first[j];
+        } else {
+            uint32_t raw[16];
+            __syncwarp();
+            tmem_load_16cols(tacc + static_cast<uint32_t>(c0), raw);
+            tmem_load_wait(raw);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
+        }
+        if (staged) {
+            // Segments in order c_first .. c_last from the staged
+            // copies, the own one written into its position first
+            // (this thread reads back only what it wrote itself).
+            float4* stage = reinterpret_cast<float4*>(smem) + (c0 >> 2) * kRows + r;
+            const int seg_stride = quads * kRows;   // float4s per position
+            float4* own = stage + (me - c_first) * seg_stride;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                if (c0 + 4 * g < p.M)
+                    own[g * kRows] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2],
+                                                 v[4 * g + 3]);
+            float4 sum[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                sum[g] = c0 + 4 * g < p.M ? stage[g * kRows]
+                                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
+            for (int i = 1; i <= others; ++i) {
+                const float4* w = stage + i * seg_stride;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (c0 + 4 * g < p.M) {
+                        const float4 x = w[g * kRows];
+                        sum[g].x += x.x;
+                        sum[g].y += x.y;
+                        sum[g].z += x.z;
+                        sum[g].w += x.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                v[4 * g] = sum[g].x;
+                v[4 * g + 1] = sum[g].y;
+                v[4 * g + 2] = sum[g].z;
+                v[4 * g + 3] = sum[g].w;
+            }
+        } else if (c_last > c_first) {
+            // Sum the segments in order c_first .. c_last, the own
+            // one from tensor memory, the others from their slots.
+            // The slots of four segments are requested together
+            // and then added in order, so the order (and the
+            // result) is fixed while four loads are in flight.
+            float sum[16];
+#pragma unroll 1
+            for (int cb = c_first; cb <= c_last; cb += 4) {
+                float4 x[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = cb + i;
+                    const int slot = c == c_first ? first_slot : 2 * c;
+                    const float4* w = reinterpret_cast<const float4*>(p.partials) +
+                                      static_cast<int64_t>(slot) * (NC / 4) * kRows;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        x[i][g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        if (c <= c_last && c != me && c0 + 4 * g < p.M)
+                            x[i][g] = __ldcg(w + ((c0 >> 2) + g) * kRows + r);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = cb + i;
+                    if (c > c_last) break;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float y[4] = {x[i][g].x, x[i][g].y, x[i][g].z, x[i][g].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 4 * g + e;
+                            const float val = c == me ? v[j] : y[e];
+                            sum[j] = c == c_first ? val : sum[j] + val;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = sum[j];
+        }
+        if (n < p.N) {
+            const int jn = min(16, p.M - c0);   // rows of A in this chunk
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (j < jn) amax_bits = max(amax_bits, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+            store_chunk16(p, c0, n, jn, v, alpha);
+        }
+    }
+}
+
 template <bool kFp16In, int KPS, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
@@ -164,9 +285,11 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
     uint64_t* acc_empty = acc_full + 2;     // [2]
     uint64_t* drain = acc_empty + 2;        // [1]
     uint64_t* fix_bar = drain + 1;          // [1] partial tiles staged for the fix-up
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fix_bar + 1);
+    uint64_t* help_bar = fix_bar + 1;       // [1] last tile handed to warps 0-3
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(help_bar + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     volatile int* last_flag = abort_flag + 1;
+    volatile int* help = last_flag + 1;     // [kHelpInts]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -180,6 +303,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
         mbar_init(drain, 1);
         mbar_init(fix_bar, 1);
+        mbar_init(help_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_mbar_init();
@@ -319,6 +443,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
         if (p.sa != nullptr) ab = p.sa[0] * p.sb[0];
         const float alpha = p.out_kind == kOutE4M3 ? __fdiv_rn(ab, p.sd[0]) : ab;
         uint32_t amax_bits = 0u;
+        bool released = false;   // the last tile handed to warps 0-3 (thread 128)
         int acc = 0;
         uint32_t acc_phase = 0;
         int t = t_begin, kb0 = kb_begin;
@@ -413,116 +538,36 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     break;
                 }
             }
-            if (finish) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < NC && c0 < p.M; c0 += 16) {
-                    float v[16];
-                    if (c_last > c_first && c0 == 0) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = first[j];
-                    } else {
-                        uint32_t raw[16];
-                        __syncwarp();
-                        tmem_load_16cols(tacc + static_cast<uint32_t>(c0), raw);
-                        tmem_load_wait(raw);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(raw[j]);
-                    }
-                    if (staged) {
-                        // Segments in order c_first .. c_last from the staged
-                        // copies, the own one written into its position first
-                        // (this thread reads back only what it wrote itself).
-                        float4* stage = reinterpret_cast<float4*>(smem) + (c0 >> 2) * kRows + r;
-                        const int seg_stride = quads * kRows;   // float4s per position
-                        float4* own = stage + (me - c_first) * seg_stride;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-                            if (c0 + 4 * g < p.M)
-                                own[g * kRows] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2],
-                                                             v[4 * g + 3]);
-                        float4 sum[4];
-#pragma unroll
-                        for (int g = 0; g < 4; ++g)
-                            sum[g] = c0 + 4 * g < p.M ? stage[g * kRows]
-                                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll 1
-                        for (int i = 1; i <= others; ++i) {
-                            const float4* w = stage + i * seg_stride;
-#pragma unroll
-                            for (int g = 0; g < 4; ++g) {
-                                if (c0 + 4 * g < p.M) {
-                                    const float4 x = w[g * kRows];
-                                    sum[g].x += x.x;
-                                    sum[g].y += x.y;
-                                    sum[g].z += x.z;
-                                    sum[g].w += x.w;
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            v[4 * g] = sum[g].x;
-                            v[4 * g + 1] = sum[g].y;
-                            v[4 * g + 2] = sum[g].z;
-                            v[4 * g + 3] = sum[g].w;
-                        }
-                    } else if (c_last > c_first) {
-                        // Sum the segments in order c_first .. c_last, the own
-                        // one from tensor memory, the others from their slots.
-                        // The slots of four segments are requested together
-                        // and then added in order, so the order (and the
-                        // result) is fixed while four loads are in flight.
-                        float sum[16];
-#pragma unroll 1
-                        for (int cb = c_first; cb <= c_last; cb += 4) {
-                            float4 x[4][4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int c = cb + i;
-                                const int slot = c == c_first ? first_slot : 2 * c;
-                                const float4* w = reinterpret_cast<const float4*>(p.partials) +
-                                                  static_cast<int64_t>(slot) * (NC / 4) * kRows;
-#pragma unroll
-                                for (int g = 0; g < 4; ++g) {
-                                    x[i][g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                                    if (c <= c_last && c != me && c0 + 4 * g < p.M)
-                                        x[i][g] = __ldcg(w + ((c0 >> 2) + g) * kRows + r);
-                                }
-                            }
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int c = cb + i;
-                                if (c > c_last) break;
-#pragma unroll
-                                for (int g = 0; g < 4; ++g) {
-                                    float y[4] = {x[i][g].x, x[i][g].y, x[i][g].z, x[i][g].w};
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const int j = 4 * g + e;
-                                        const float val = c == me ? v[j] : y[e];
-                                        sum[j] = c == c_first ? val : sum[j] + val;
-                                    }
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = sum[j];
-                    }
-                    if (n < p.N) {
-                        const int jn = min(16, p.M - c0);   // rows of A in this chunk
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (j < jn) amax_bits = max(amax_bits, __float_as_uint(v[j]) & 0x7FFFFFFFu);
-                        store_chunk16(p, c0, n, jn, v, alpha);
-                    }
-                }
+            // The CTA's last tile: with more than one chunk, warps 0-3 (idle
+            // by now, each reading the same tensor-memory lanes as its twin
+            // among warps 4-7) take the odd chunks.  The hand-off is an
+            // mbarrier with bounded waits, released on every exit path.
+            const bool helped = NC >= 32 && finish && left == 0;
+            if (left == 0 && threadIdx.x == 4 * 32) {
+                help[1] = t;
+                help[2] = acc;
+                help[3] = c_first;
+                help[4] = c_last;
+                help[5] = first_slot;
+                help[6] = staged ? 1 : 0;
+                help[0] = helped ? 1 : 0;
+                mbar_arrive(help_bar);
+                released = true;
             }
+            if (finish)
+                finish_chunks<NC>(p, smem, tacc, r, n, 0, helped ? 32 : 16, me, c_first, c_last,
+                                  first_slot, staged, quads, first, alpha, amax_bits);
             // The accumulator is free once every chunk has been read.
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             (void)my_slot;
+        }
+        // Every exit (including a timed-out wait) releases warps 0-3.
+        if (threadIdx.x == 4 * 32 && !released) {
+            help[0] = 0;
+            mbar_arrive(help_bar);
         }
         // max |sa*sb*acc| of this warp's stored outputs (monotone rounding:
         // fl(max|acc| * c) is the exact maximum of fl(|acc| * c)).
@@ -531,6 +576,44 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
             const uint32_t bits = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
             if (lane == 0 && bits != 0u)
                 atomicMax(p.amax_out, __float_as_uint(__uint_as_float(bits) * ab) & 0x7FFFFFFFu);
+        }
+    }
+    if constexpr (NC >= 32) {
+        if (warp < 4) {
+            // ------------------------------------------------ helpers
+            // Warps 0-3, once their own roles are done, take the odd
+            // 16-column chunks of the CTA's last tile when it finishes one.
+            __syncwarp();
+            const bool go = wait_bounded(help_bar, 0, ctl) && help[0] != 0;
+            if (__all_sync(0xFFFFFFFFu, go)) {
+                const int t = help[1], acc = help[2], c_first = help[3], c_last = help[4];
+                const int first_slot = help[5];
+                const bool staged = help[6] != 0;
+                tc_fence_after_sync();
+                const bool landed = !staged || wait_bounded(fix_bar, 0, ctl);
+                if (__all_sync(0xFFFFFFFFu, landed)) {
+                    const int q = warp;   // the same tensor-memory lanes as warp q + 4
+                    const int r = q * 32 + lane;
+                    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                          static_cast<uint32_t>(acc * NC);
+                    float ab = 1.0f;
+                    if (p.sa != nullptr) ab = p.sa[0] * p.sb[0];
+                    const float alpha = p.out_kind == kOutE4M3 ? __fdiv_rn(ab, p.sd[0]) : ab;
+                    const int quads = (min(p.M, NC) + 3) >> 2;
+                    const float none[16] = {};   // chunk 0 is not among the odd ones
+                    uint32_t amax_bits = 0u;
+                    finish_chunks<NC>(p, smem, tacc, r, t * kRows + r, 16, 32,
+                                      static_cast<int>(blockIdx.x), c_first, c_last, first_slot,
+                                      staged, quads, none, alpha, amax_bits);
+                    if (p.amax_out != nullptr) {
+                        __syncwarp();
+                        const uint32_t bits = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+                        if (lane == 0 && bits != 0u)
+                            atomicMax(p.amax_out,
+                                      __float_as_uint(__uint_as_float(bits) * ab) & 0x7FFFFFFFu);
+                    }
+                }
+            }
         }
     }
 
