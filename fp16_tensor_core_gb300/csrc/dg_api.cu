@@ -172,7 +172,7 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     }
     // GEMV for M <= 2, split-K tensor cores up to M = 16.  Measured on GB300
     // for N = 12288 (B read from HBM, graph-replayed launches): at K = 4096
-    // the GEMV takes 10.2 us at M = 1 and grows with M (its FMA count), the
+    // the GEMV takes 9.7 us at M = 1 and grows with M (its FMA count), the
     // split-K kernel a flat 11.1-11.5 us for M = 1..16; at K = 1024 4.4
     // against 6.9 us.  DG_GEMV_MAX_M (0..16) moves the crossover.
     int gemv_max_m = 2;
@@ -182,7 +182,22 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     }
     if (M <= gemv_max_m) {
         p->path = 2;
-        const int rows = M <= 4 ? 8 : 4;   // 4 warps x (2 or 1) rows of B
+        int rows = M <= 4 ? 8 : 4;   // 4 warps x (2 or 1) rows of B
+        // M = 1, E4M3, K <= 8192: the fewest rows per CTA (4, 8, 16: warps of
+        // 1 row x 8 chunks, 2 x 4, 4 x 2 in flight) whose grid fits in one
+        // wave of 8 CTAs per SM, so no partial second wave trails the stream.
+        // Measured on GB300, graph-replayed: 1 x 12288 x 4096 9.70 us with 16
+        // rows (768 CTAs) vs 10.10 with 8 (1536); 1 x 4096 x 4096 5.09 with 4
+        // vs 5.27; 1 x 28672 x 4096 (no width fits) and K = 14336 stay at 8.
+        if (M == 1 && !fp16_in && K <= 8192) {
+            const int64_t wave = static_cast<int64_t>(sm_count) * 8;
+            for (const int r : {4, 8, 16}) {
+                if ((N + r - 1) / r <= wave) {
+                    rows = r;
+                    break;
+                }
+            }
+        }
         p->grid = static_cast<int>((N + rows - 1) / rows);
         p->block_m = static_cast<int>(M);
         p->block_n = rows;
@@ -321,7 +336,7 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
         case 2:
             return from_cuda(launch_gemv(A, B, D, static_cast<int>(M), static_cast<int>(N),
                                          static_cast<int>(K), fp16_in, sa, sb, sd, ok, amax_bits,
-                                         s));
+                                         plan.block_n, s));
         case 4:
         default: {
             TcLaunch L;

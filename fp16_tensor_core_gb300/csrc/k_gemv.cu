@@ -205,7 +205,11 @@ cudaError_t launch_one(const void* A, const void* B, void* D, int M, int N, int 
 template <bool kFp16>
 cudaError_t launch_mt(int MT, const void* A, const void* B, void* D, int M, int N, int K,
                       const float* sa, const float* sb, const float* sd, int out_kind,
-                      uint32_t* amax_out, cudaStream_t s) {
+                      uint32_t* amax_out, int rows_per_cta, cudaStream_t s) {
+    if (MT == 1 && !kFp16 && rows_per_cta == 4)
+        return launch_one<1, kFp16, 1, 8>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
+    if (MT == 1 && !kFp16 && rows_per_cta == 16)
+        return launch_one<1, kFp16, 4, 2>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
     switch (MT) {
         case 1: return launch_one<1, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
         case 2: return launch_one<2, kFp16, 2, 4>(A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
@@ -219,11 +223,13 @@ cudaError_t launch_mt(int MT, const void* A, const void* B, void* D, int M, int 
 
 cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N, int K, bool fp16_in,
                         const float* sa, const float* sb, const float* sd, int out_kind,
-                        uint32_t* amax_out, cudaStream_t s) {
+                        uint32_t* amax_out, int rows_per_cta, cudaStream_t s) {
     if (M <= 0 || M > 16 || N <= 0 || K <= 0) return cudaErrorInvalidValue;
     const int MT = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
-    return fp16_in ? launch_mt<true>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s)
-                   : launch_mt<false>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out, s);
+    return fp16_in ? launch_mt<true>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out,
+                                     rows_per_cta, s)
+                   : launch_mt<false>(MT, A, B, D, M, N, K, sa, sb, sd, out_kind, amax_out,
+                                      rows_per_cta, s);
 }
 
 }  // namespace dg
