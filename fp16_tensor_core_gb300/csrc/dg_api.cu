@@ -183,26 +183,49 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     if (M <= gemv_max_m) {
         p->path = 2;
         int rows = M <= 4 ? 8 : 4;   // 4 warps x (2 or 1) rows of B
-        // M = 1, E4M3, K <= 8192: the fewest rows per CTA (4, 8, 16: warps of
-        // 1 row x 8 chunks, 2 x 4, 4 x 2 in flight) whose grid fits in one
-        // wave of 8 CTAs per SM, so no partial second wave trails the stream.
-        // Measured on GB300, graph-replayed: 1 x 12288 x 4096 9.70 us with 16
-        // rows (768 CTAs) vs 10.10 with 8 (1536); 1 x 4096 x 4096 5.09 with 4
-        // vs 5.27; 1 x 28672 x 4096 (no width fits) and K = 14336 stay at 8.
-        if (M == 1 && !fp16_in && K <= 8192) {
-            const int64_t wave = static_cast<int64_t>(sm_count) * 8;
-            for (const int r : {4, 8, 16}) {
-                if ((N + r - 1) / r <= wave) {
-                    rows = r;
+        int chunks = 4;              // 16-byte chunks per lane per row in flight
+        // M <= 2 with rows of B of at most 8 KB: the fewest rows per CTA whose
+        // grid fits in one wave (at that layout's CTAs per SM, set by its
+        // registers), so no partial second wave trails the stream; if none
+        // fits, 8 for E4M3 and 4 for FP16.  Layouts per warp: 4 rows = 1 row x
+        // 8 chunks, 8 = 2 x 4, 16 = 4 x 3 (E4M3, M = 1) or 4 x 2.  Measured on
+        // GB300, graph-replayed (us, 8 rows -> chosen): E4M3 1 x 12288 x 4096
+        // 10.10 -> 9.70 (4 x 2) -> 9.60 (4 x 3); 1 x 4096 x 4096 5.27 -> 5.09
+        // (4 rows); 2 x 12288 x 4096 13.4 -> 10.9 (16); FP16 1 x 12288 x 4096
+        // 22.3 -> 16.2 (16); 1 x 4096 x 4096 10.3 -> 7.2 (4); 1 x 28672 x 4096
+        // 38.1 -> 33.8 (4, none fits); E4M3 1 x 28672 x 4096 and 1 x 8192 x
+        // 8192 best at 8.
+        const int64_t row_bytes = K * (fp16_in ? 2 : 1);
+        if (M <= 2 && row_bytes <= 8192) {
+            struct Layout { int rows, chunks, per_sm; };
+            const Layout e4_m1[4] = {{4, 8, 8}, {8, 4, 8}, {16, 3, 6}, {16, 2, 8}};
+            const Layout e4_m2[3] = {{4, 8, 8}, {8, 4, 8}, {16, 2, 6}};
+            const Layout f16[3] = {{4, 8, 8}, {8, 4, 8}, {16, 2, M == 1 ? 8 : 7}};
+            const Layout* cand = fp16_in ? f16 : (M == 1 ? e4_m1 : e4_m2);
+            const int ncand = (!fp16_in && M == 1) ? 4 : 3;
+            rows = fp16_in ? 4 : 8;
+            chunks = fp16_in ? 8 : 4;
+            for (int i = 0; i < ncand; ++i) {
+                if ((N + cand[i].rows - 1) / cand[i].rows <=
+                    static_cast<int64_t>(sm_count) * cand[i].per_sm) {
+                    rows = cand[i].rows;
+                    chunks = cand[i].chunks;
                     break;
                 }
+            }
+        }
+        if (const char* v = std::getenv("DG_GEMV_ROWS")) {   // sweeps (M <= 2)
+            const int r = std::atoi(v);
+            if (M <= 2 && (r == 4 || r == 8 || r == 16)) {
+                rows = r;
+                chunks = r == 4 ? 8 : r == 8 ? 4 : 2;
             }
         }
         p->grid = static_cast<int>((N + rows - 1) / rows);
         p->block_m = static_cast<int>(M);
         p->block_n = rows;
         p->block_k = fp16_in ? 8 * 32 : 16 * 32;
-        p->stages = 1;
+        p->stages = chunks;
         return DG_OK;
     }
     // Split-K with swapped operands (every SM streams an equal share of B)
@@ -336,7 +359,7 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
         case 2:
             return from_cuda(launch_gemv(A, B, D, static_cast<int>(M), static_cast<int>(N),
                                          static_cast<int>(K), fp16_in, sa, sb, sd, ok, amax_bits,
-                                         plan.block_n, s));
+                                         plan.block_n, plan.stages, s));
         case 4:
         default: {
             TcLaunch L;

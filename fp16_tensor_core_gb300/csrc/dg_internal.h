@@ -72,12 +72,13 @@ cudaError_t launch_amax(const float* x, int64_t n, float* amax_out,
                         bool pow2 = false);
 cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale,
                                  uint8_t* q, int sm_count, cudaStream_t s);
-// rows_per_cta: rows of B per 4-warp CTA from the plan (4, 8 or 16 at M = 1;
-// 8 for M <= 4, 4 above).
+// rows_per_cta and chunks: rows of B per 4-warp CTA and 16-byte chunks per
+// lane per row in flight, from the plan (4 x 8, 8 x 4, 16 x 3 or 16 x 2 at
+// M <= 2; otherwise 8 x 4 for M <= 4 and 4 x 4 above).
 cudaError_t launch_gemv(const void* A, const void* B, void* D, int M, int N,
                         int K, bool fp16_in, const float* sa, const float* sb,
                         const float* sd, int out_kind, uint32_t* amax_out,
-                        int rows_per_cta, cudaStream_t s);
+                        int rows_per_cta, int chunks, cudaStream_t s);
 // Quantise with a given scale and record max |x| (and optionally the next
 // scale = amax / 448) in the same pass over x.
 cudaError_t launch_quantize_e4m3_amax(const float* x, int64_t n, const float* scale, uint8_t* q,

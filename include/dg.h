@@ -272,7 +272,8 @@ typedef struct {
     int block_m;    /* output rows per tile (tensor-core paths)             */
     int block_n;    /* output columns per tile                              */
     int block_k;    /* K elements per pipeline stage                        */
-    int stages;     /* shared-memory pipeline depth                         */
+    int stages;     /* shared-memory pipeline depth; for the GEMV (path 2)
+                       the 16-byte chunks per lane per row of B in flight   */
     int grid;       /* CTAs launched                                        */
     int tiles;      /* output tiles (tensor-core paths)                     */
     int smem_bytes; /* dynamic shared memory per CTA                        */

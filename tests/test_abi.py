@@ -190,17 +190,24 @@ def test_plan_paths_and_tiles(L):
     assert dg.dg_gemm_plan(0, 10, 16, sm_count=sm)["path"] == 0
     assert dg.dg_gemm_plan(10, 0, 16, sm_count=sm)["path"] == 0
     assert dg.dg_gemm_plan(10, 10, 0, sm_count=sm)["path"] == 1
-    # M = 1 (E4M3, K <= 8192): the fewest rows per CTA whose grid fits in one
-    # wave of 8 CTAs per SM; otherwise (and for M = 2, FP16) 8 rows
-    for n, rows in ((12288, 16), (4096, 4), (1000, 4), (28672, 8)):
-        p = dg.dg_gemm_plan(1, n, 4096, sm_count=sm)
-        assert p["path"] == 2 and p["block_n"] == rows and p["grid"] == (n + rows - 1) // rows, (n, p)
-    assert dg.dg_gemm_plan(1, 4096, 14336, sm_count=sm)["block_n"] == 8
-    assert dg.dg_gemm_plan(1, 12288, 4096, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16,
-                           sm_count=sm)["block_n"] == 8
-    for m in (2,):
-        p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
-        assert p["path"] == 2 and p["block_n"] == 8 and p["grid"] == 12288 // 8
+    # M <= 2, rows of B <= 8 KB: the fewest rows per CTA whose grid fits in one
+    # wave of 8 CTAs per SM; if none fits, 8 (E4M3) or 4 (FP16)
+    for m in (1, 2):
+        for n, rows in ((12288, 16), (4096, 4), (1000, 4), (28672, 8)):
+            p = dg.dg_gemm_plan(m, n, 4096, sm_count=sm)
+            assert p["path"] == 2 and p["block_n"] == rows and p["grid"] == (n + rows - 1) // rows, (m, n, p)
+    assert dg.dg_gemm_plan(1, 4096, 14336, sm_count=sm)["block_n"] == 8     # 14 KB rows
+    # the layout's own residency decides: 4 rows x 3 chunks (6 CTAs per SM)
+    # while it fits one wave, then 4 x 2 (8 per SM); M = 2 has only 4 x 2 (6)
+    p = dg.dg_gemm_plan(1, 12288, 4096, sm_count=sm)
+    assert (p["block_n"], p["stages"]) == (16, 3)
+    p = dg.dg_gemm_plan(1, 16384, 4096, sm_count=sm)
+    assert (p["block_n"], p["stages"]) == (16, 2)
+    assert dg.dg_gemm_plan(2, 16384, 4096, sm_count=sm)["block_n"] == 8
+    assert dg.dg_gemm_plan(1, 4096, 4096, sm_count=sm)["stages"] == 8
+    for n, rows in ((12288, 16), (4096, 4), (28672, 4)):
+        p = dg.dg_gemm_plan(1, n, 4096, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16, sm_count=sm)
+        assert p["path"] == 2 and p["block_n"] == rows, (n, p)
     for m in (3, 16):
         # split-K: 96 tiles of 128 rows of B, 96 x 32 K blocks over 152 CTAs
         p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)

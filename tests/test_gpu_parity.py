@@ -304,6 +304,27 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     fp8_chain(A, B)
 
 
+@pytest.mark.parametrize("M,N,K,rows", [
+    (1, 1000, 1040, 4),      # 1 row x 8 chunks per warp
+    (2, 4001, 2048, 4),
+    (1, 12288, 1024, 16),    # 4 rows x 2 chunks per warp: 768 CTAs, one wave
+    (2, 12000, 1040, 16),    # ragged last CTA
+    (1, 16000, 512, 16),     # 4 x 3 would not fit one wave: 4 rows x 2 chunks
+    (1, 30000, 512, 8),      # no width fits one wave: 2 rows x 4 chunks
+])
+def test_gemv_one_wave_layouts(M, N, K, rows):
+    """M <= 2: the planner's rows per CTA (the fewest whose grid fits one wave)
+    for E4M3 and FP16 operands, every element against the oracle."""
+    p = dg.dg_gemm_plan(M, N, K)
+    assert p["path"] == 2 and p["block_n"] == rows, p
+    A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+    fp8_chain(A, B)
+    p16 = dg.dg_gemm_plan(M, N, K, dg.DG_FP16, dg.DG_FP16)
+    assert p16["path"] == 2 and p16["block_n"] == (4 if rows == 8 else rows), p16
+    A16, B16 = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
+    hgemm_case(A16, B16)
+
+
 @pytest.mark.parametrize("M,N,K", [(4, 1000, 1040), (7, 513, 512), (16, 513, 4096), (3, 300, 272)])
 def test_gemv_for_larger_m_when_forced(M, N, K):
     """The GEMV handles M up to 16 (its 2-, 4-, 8- and 16-row instantiations),
