@@ -28,8 +28,12 @@
 // K blocks (16 KB of B + NC x 128 bytes of A each; 12 of them for NC = 16,
 // 6 for NC = 128; 1 or 2 blocks per stage) and two NC-column accumulators in
 // tensor memory.  Partial tiles are kept as FP32 column quads (16 bytes per
-// row and 4 columns) and the finishing CTA requests four segments' quads at a
-// time before adding them in segment order.  Launch overlap: before its
+// row and 4 columns).  The finishing CTA adds them in segment order: from its
+// idle ring, bulk-copied there, when the tile is its last segment and they
+// fit, else four segments' quads at a time from L2; for its last tile, warps
+// 0-3 (done with their own roles) take the odd 16-column chunks.  With at
+// least two CTAs per tile the grid is a whole multiple of the tile count.
+// Launch overlap: before its
 // dependency wait a CTA prefetches its first ring of B into L2, and right
 // after it the grid lets the next kernel take over SMs as CTAs exit, so the
 // start-up of one launch hides in the straggling tail of the one before.
