@@ -10,8 +10,9 @@
 // is streamed from HBM without shared-memory staging; §4.1: the single A row
 // is broadcast to every thread instead of 2-D tiling.  [FP8-guide] §2.3:
 // 128-bit vector loads.  Here one warp owns R consecutive rows of B (N x K,
-// K contiguous; R = 2 for M <= 4): lane l reads 16-byte chunks l, l+32,
-// l+64, ... of each row (fully coalesced 512-byte warp loads, several per
+// K contiguous; R = 1, 2 or 4 at M <= 2, chosen by the planner so that the
+// grid fits one wave; 2 for M <= 4, 1 above): lane l reads 16-byte chunks l,
+// l+32, l+64, ... of each row (fully coalesced 512-byte warp loads, U per
 // row in flight at once) and widens them to FP16 pairs; the matching A
 // chunk (L1-resident, shared by every warp) is widened once and used for all
 // R rows.  Products and sums use fma.rn.f32.f16 -- the exact product of two
