@@ -1,5 +1,5 @@
-"""Seeded random shapes over every GEMM path (GEMV, split-K, single CTA, CTA
-pairs), E4M3 and FP16 inputs and each output type, every element checked
+"""Seeded random shapes over every GEMM path (GEMV layouts, split-K, single
+CTA, CTA pairs), E4M3 and FP16 inputs and each output type, every element checked
 against the oracle and every byte around D checked untouched.  K is a
 multiple of 16 (E4M3) or 8 (FP16), the only shape rule of the library."""
 import numpy as np
@@ -37,7 +37,21 @@ def _shapes(seed, count):
     return out
 
 
-@pytest.mark.parametrize("M,N,K", _shapes(123, 24))
+def _shapes_wide(seed, count):
+    """Decode-style shapes: M <= 128 against wide B (N up to 13000), where
+    the planner chooses between the GEMV layouts, split-K (with its
+    tile-aligned grid, staged fix-up and helper warps) and the tiled kernel."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(count):
+        M = int(rng.integers(1, 3)) if i % 4 == 0 else int(rng.integers(3, 129))
+        N = int(rng.integers(2000, 13000))
+        K = 16 * int(rng.integers(16, 200))
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", _shapes(123, 24) + _shapes_wide(777, 16))
 def test_random_fp8_shapes(M, N, K):
     A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
     qa, _, sa_d = gpu_quantize(A)
@@ -62,7 +76,7 @@ def test_random_fp8_shapes(M, N, K):
     check_e4m3(D8.cpu().numpy().reshape(M, N), R, sa, sb, sd)
 
 
-@pytest.mark.parametrize("M,N,K", [(m, n, k // 2) for (m, n, k) in _shapes(321, 12)])
+@pytest.mark.parametrize("M,N,K", [(m, n, k // 2) for (m, n, k) in _shapes(321, 12) + _shapes_wide(654, 6)])
 def test_random_fp16_shapes(M, N, K):
     K = max(8, K - K % 8)
     A, B = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
