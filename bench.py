@@ -336,6 +336,17 @@ def kernel_cases(torch, dg):
         fn = lambda i, s: dg.dg_hgemm(Hs[i % nb], Hb[i % nb], D, dg.DG_FP16, stream=s)  # noqa: E731
         return fn, 2.0 * S ** 3, 6 * S * S, "tensor_fp16", f"{nb} rotating copies"
 
+    def hgemv(m, Nq=12288, Kq=4096):
+        # FP16 operands on the decode QKV shape (the HGEMM's GEMV path)
+        nb = ncopies(2 * Nq * Kq)
+        g = torch.Generator(device=dev)
+        g.manual_seed(6)
+        Ha = [(torch.rand((m, Kq), device=dev, generator=g) * 2 - 1).half() for _ in range(nb)]
+        Hb = [((torch.rand((Nq, Kq), device=dev, generator=g) * 2 - 1) * 0.02).half() for _ in range(nb)]
+        D = torch.empty((m, Nq), dtype=torch.float16, device=dev)
+        fn = lambda i, s: dg.dg_hgemm(Ha[i % nb], Hb[i % nb], D, dg.DG_FP16, stream=s)  # noqa: E731
+        return fn, 2.0 * m * Nq * Kq, 2 * (Nq * Kq + m * Kq + m * Nq), "hbm", f"{nb} rotating copies"
+
     def amax():
         x = torch.randn((8192, 8192), device=dev)
         am = torch.zeros(4, dtype=torch.float32, device=dev)
@@ -439,6 +450,7 @@ def kernel_cases(torch, dg):
         "fp8_gemm_4096": lambda: fp8_sq(4096, dg.DG_BF16),
         "fp8_gemm_8192_e4m3out": lambda: fp8_sq(8192, dg.DG_E4M3),
         "fp16_hgemm_4096": lambda: hgemm(4096),
+        "fp16_qkv_gemv_1x12288x4096": lambda: hgemv(1),
         "amax_8192sq": amax,
         "quantise_8192sq": quant,
         "quantise_with_amax_8192sq": quant_amax,
