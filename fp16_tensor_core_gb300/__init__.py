@@ -22,7 +22,8 @@ __all__ = [
     "dg_fp8_gemm_amax", "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static",
     "dg_hgemm", "dg_hgemm_scaled", "dg_fp16_range_scale", "dg_convert_f16",
     "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
-    "dg_debug_skip_first_load", "dg_status_string", "dg_version", "EXPORTED_SYMBOLS",
+    "dg_debug_skip_first_load", "dg_status_string", "dg_version", "dg_release_stream",
+    "dg_reload_env", "EXPORTED_SYMBOLS",
 ]
 
 DG_OK, DG_ERR_INVALID_VALUE, DG_ERR_MISALIGNED, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_TIMEOUT = range(6)
@@ -35,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_hgemm", "dg_hgemm_scaled",
     "dg_fp16_range_scale", "dg_convert_f16", "dg_gemm_plan",
     "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
-    "dg_status_string", "dg_version",
+    "dg_status_string", "dg_version", "dg_release_stream", "dg_reload_env",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -96,10 +97,13 @@ def lib():
             L.dg_status_string.argtypes = [ctypes.c_int]
             L.dg_status_string.restype = ctypes.c_char_p
             L.dg_version.argtypes = []
+            L.dg_release_stream.argtypes = [vp]
+            L.dg_reload_env.argtypes = []
+            L.dg_reload_env.restype = None
             for name in ("dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm",
                          "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_gemm_plan", "dg_init",
                          "dg_sync_status", "dg_version", "dg_hgemm_scaled", "dg_fp16_range_scale",
-                         "dg_convert_f16", "dg_quantize_e4m3_amax"):
+                         "dg_convert_f16", "dg_quantize_e4m3_amax", "dg_release_stream"):
                 getattr(L, name).restype = st
             _lib = L
     return _lib
@@ -269,3 +273,13 @@ def dg_set_wait_timeout_us(us: int) -> None:
 
 def dg_debug_skip_first_load(enable: bool = True) -> None:
     lib().dg_debug_skip_first_load(1 if enable else 0)
+
+
+def dg_release_stream(stream=None) -> None:
+    """Free the split-K workspace the stream holds (synchronises the stream)."""
+    _check(lib().dg_release_stream(_stream(stream)), "dg_release_stream")
+
+
+def dg_reload_env() -> None:
+    """Re-read the DG_* tuning variables (otherwise read once, at first use)."""
+    lib().dg_reload_env()

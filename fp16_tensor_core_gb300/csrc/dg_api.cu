@@ -25,14 +25,17 @@ bool g_dev_ready[kMaxDevices] = {};
 
 // Split-K workspaces per device, one per stream that has run a split-K GEMM
 // (calls on different streams may execute concurrently, so they must not
-// share partial slots and arrival counters).  The first such stream uses
-// the workspace allocated with the device state.
+// share partial slots and arrival counters).  One stream at a time uses the
+// workspace allocated with the device state; each other stream gets one of
+// its own, up to kMaxStreamWorkspaces per device, until dg_release_stream.
 struct SplitkWs {
     float* partials;
     uint32_t* counts;
 };
+constexpr size_t kMaxStreamWorkspaces = 16;
 std::mutex g_ws_mu[kMaxDevices];
 std::unordered_map<cudaStream_t, SplitkWs> g_ws[kMaxDevices];
+bool g_dev_ws_taken[kMaxDevices] = {};   // the device-state workspace is in g_ws
 
 size_t splitk_partial_bytes(int sm_count) {
     return sizeof(float) * 2 * static_cast<size_t>(sm_count) * kSplitkMaxCols * kSkinnyTileRows;
@@ -43,17 +46,62 @@ std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_skip_first_load{0};
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// FP32 device scalars (scales, amax words) are read by 4-byte loads.
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 inline dg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
 
 }  // namespace
 
-bool pdl_enabled() {
-    static const bool on = [] {
-        const char* v = std::getenv("DG_PDL");
-        return !(v && v[0] == '0');
-    }();
-    return on;
+namespace {
+
+// Integer value of environment variable `name` if set and within [lo, hi].
+bool env_int(const char* name, int64_t lo, int64_t hi, int64_t* out) {
+    const char* v = std::getenv(name);
+    if (v == nullptr || v[0] == '\0') return false;
+    char* end = nullptr;
+    const long long x = std::strtoll(v, &end, 10);
+    if (end == v || x < lo || x > hi) return false;
+    *out = x;
+    return true;
+}
+
+Knobs read_knobs() {
+    Knobs k;
+    int64_t v = 0;
+    if (const char* e = std::getenv("DG_PDL")) k.pdl = e[0] != '0';
+    if (const char* e = std::getenv("DG_LOG")) k.log = e[0] != '\0' && e[0] != '0';
+    if (env_int("DG_GEMV_MAX_M", 0, 16, &v)) k.gemv_max_m = static_cast<int>(v);
+    if (env_int("DG_GEMV_ROWS", 4, 16, &v) && (v == 4 || v == 8 || v == 16))
+        k.gemv_rows = static_cast<int>(v);
+    if (const char* e = std::getenv("DG_SPLITK")) k.splitk = e[0] == '0' ? 0 : e[0] == '1' ? 1 : -1;
+    if (env_int("DG_SPLITK_GRID", 1, INT_MAX, &v)) k.splitk_grid = static_cast<int>(v);
+    if (env_int("DG_SPLITK_PREFETCH", 0, 256, &v)) k.splitk_prefetch = static_cast<int>(v);
+    if (env_int("DG_SPLITK_KPS", 1, 2, &v)) k.splitk_kps = static_cast<int>(v);
+    if (const char* e = std::getenv("DG_ONE_WAVE")) k.one_wave = e[0] != '0';
+    if (env_int("DG_ONE_WAVE_KB", INT64_MIN, INT64_MAX, &v)) k.one_wave_kb = v;
+    if (env_int("DG_FORCE_BLOCK_N", 64, 256, &v)) k.force_block_n = static_cast<int>(v);
+    if (const char* e = std::getenv("DG_2CTA")) k.two_cta = e[0] == '0' ? 0 : e[0] == '1' ? 1 : -1;
+    if (env_int("DG_GROUP_M", 1, 4096, &v)) k.group_m = static_cast<int>(v);
+    return k;
+}
+
+// The current snapshot.  dg_reload_env() publishes a new one and keeps the
+// old one alive (a few bytes per reload), so a concurrent reader never sees
+// freed memory.
+std::atomic<const Knobs*> g_knobs{nullptr};
+std::once_flag g_knobs_once;
+
+}  // namespace
+
+const Knobs& knobs() {
+    const Knobs* k = g_knobs.load(std::memory_order_acquire);
+    if (k != nullptr) return *k;
+    std::call_once(g_knobs_once, [] {
+        if (g_knobs.load(std::memory_order_acquire) == nullptr)
+            g_knobs.store(new Knobs(read_knobs()), std::memory_order_release);
+    });
+    return *g_knobs.load(std::memory_order_acquire);
 }
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
@@ -108,16 +156,8 @@ dg_status current_device_state(DeviceState** out) {
 namespace {
 
 // DG_LOG=1: one line per GEMM call on stderr with the chosen path and tile.
-bool log_enabled() {
-    static const bool on = [] {
-        const char* v = std::getenv("DG_LOG");
-        return v != nullptr && v[0] != '\0' && v[0] != '0';
-    }();
-    return on;
-}
-
 void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& p) {
-    if (!log_enabled()) return;
+    if (!knobs().log) return;
     static const char* const kPath[5] = {"no-op", "zero-fill", "gemv", "tensor-core",
                                          "split-k"};
     std::fprintf(stderr,
@@ -175,12 +215,8 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     // the GEMV takes 9.7 us at M = 1 and grows with M (its FMA count), the
     // split-K kernel a flat 11.1-11.5 us for M = 1..16; at K = 1024 4.4
     // against 6.9 us.  DG_GEMV_MAX_M (0..16) moves the crossover.
-    int gemv_max_m = 2;
-    if (const char* v = std::getenv("DG_GEMV_MAX_M")) {
-        const int x = std::atoi(v);
-        if (x >= 0 && x <= 16) gemv_max_m = x;
-    }
-    if (M <= gemv_max_m) {
+    const Knobs& kn = knobs();
+    if (M <= kn.gemv_max_m) {
         p->path = 2;
         int rows = M <= 4 ? 8 : 4;   // 4 warps x (2 or 1) rows of B
         int chunks = 4;              // 16-byte chunks per lane per row in flight
@@ -214,12 +250,9 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
                 }
             }
         }
-        if (const char* v = std::getenv("DG_GEMV_ROWS")) {   // sweeps (M <= 2)
-            const int r = std::atoi(v);
-            if (M <= 2 && (r == 4 || r == 8 || r == 16)) {
-                rows = r;
-                chunks = r == 4 ? 8 : r == 8 ? 4 : 2;
-            }
+        if (kn.gemv_rows != 0 && M <= 2) {   // sweeps
+            rows = kn.gemv_rows;
+            chunks = rows == 4 ? 8 : rows == 8 ? 4 : 2;
         }
         p->grid = static_cast<int>((N + rows - 1) / rows);
         p->block_m = static_cast<int>(M);
@@ -233,9 +266,8 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     // plan would keep fewer than 3/4 of the SMs busy and the time estimate
     // below favours it.  DG_SPLITK=0 turns it off, DG_SPLITK=1 uses it for
     // every M <= 128.
-    const char* sk = std::getenv("DG_SPLITK");
-    const bool splitk_off = sk != nullptr && sk[0] == '0';
-    const bool splitk_forced = sk != nullptr && sk[0] == '1';
+    const bool splitk_off = kn.splitk == 0;
+    const bool splitk_forced = kn.splitk == 1;
     const bool splitk_fits = (N + kSkinnyTileRows - 1) / kSkinnyTileRows <= kSkinnyMaxTiles;
     if (!splitk_off && splitk_fits && M <= kSkinnyMaxM) {
         p->path = 4;
@@ -279,6 +311,8 @@ dg_status check_fp8_gemm_args(const void* A, const void* B, const void* D, int64
         if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
         if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0)
             return DG_ERR_MISALIGNED;
+        if (!aligned4(scale_a) || !aligned4(scale_b) || (out == DG_E4M3 && !aligned4(scale_d)))
+            return DG_ERR_MISALIGNED;
     }
     return DG_OK;
 }
@@ -298,22 +332,27 @@ dg_status check_hgemm_args(const void* A, const void* B, const void* D, int64_t 
     return DG_OK;
 }
 
-// The split-K workspace of `s` on the device of `st` (created on the first
-// split-K call on a stream other than the first one; never while the stream
-// is being captured into a graph).
+// The split-K workspace of `s` on the device of `st`: the device-state one
+// if no other stream holds it, else one allocated on the stream's first
+// split-K call (never while the stream is being captured into a graph).
+// *out stays null when the stream already holds none and the per-device cap
+// of allocated workspaces is reached.
 dg_status splitk_workspace(const DeviceState* st, cudaStream_t s, SplitkWs* out) {
     std::lock_guard<std::mutex> lk(g_ws_mu[st->device]);
     auto& map = g_ws[st->device];
+    *out = SplitkWs{nullptr, nullptr};
     auto it = map.find(s);
     if (it != map.end()) {
         *out = it->second;
         return DG_OK;
     }
-    if (map.empty()) {
+    if (!g_dev_ws_taken[st->device]) {
         map[s] = SplitkWs{st->splitk_partials, st->splitk_counts};
+        g_dev_ws_taken[st->device] = true;
         *out = map[s];
         return DG_OK;
     }
+    if (map.size() > kMaxStreamWorkspaces) return DG_OK;   // cap reached: none
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -384,8 +423,16 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
                 SplitkWs ws;
                 rc = splitk_workspace(st, s, &ws);
                 if (rc != DG_OK) return rc;
-                return from_cuda(
-                    launch_gemm_skinny(L, ws.partials, ws.counts, kSplitkMaxCols, s));
+                if (ws.partials != nullptr)
+                    return from_cuda(
+                        launch_gemm_skinny(L, ws.partials, ws.counts, kSplitkMaxCols, s));
+                // No workspace left for this stream: the tiled kernel, which
+                // needs none, computes the same product.
+                plan = dg_plan{};
+                plan.path = 3;
+                plan_tc(M, N, K, fp16_in, st->sm_count, &plan);
+                log_plan(fp16_in ? "hgemm (no split-K workspace)" : "fp8_gemm (no split-K workspace)",
+                         M, N, K, plan);
             }
             return from_cuda(launch_gemm_tc(L, s));
         }
@@ -496,6 +543,8 @@ dg_status dg_fp8_gemm_grouped(const uint8_t* A, const uint8_t* B, void* D, int64
         return DG_ERR_INVALID_VALUE;
     if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0) return DG_ERR_MISALIGNED;
+    if (!aligned4(scale_a) || !aligned4(scale_b) || (out == DG_E4M3 && !aligned4(scale_d)))
+        return DG_ERR_MISALIGNED;
     DeviceState* st = nullptr;
     rc = current_device_state(&st);
     if (rc != DG_OK) return rc;
@@ -629,6 +678,32 @@ dg_status dg_sync_status(dg_stream_t stream) {
         if (word & kStatusBadArgument) return DG_ERR_INVALID_VALUE;
     }
     return DG_OK;
+}
+
+dg_status dg_release_stream(dg_stream_t stream) {
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lk(g_ws_mu[st->device]);
+    auto& map = g_ws[st->device];
+    auto it = map.find(s);
+    if (it == map.end()) return DG_OK;
+    // The stream's earlier split-K launches may still be running.
+    if (cudaStreamSynchronize(s) != cudaSuccess) return DG_ERR_CUDA;
+    if (it->second.partials == st->splitk_partials) {
+        g_dev_ws_taken[st->device] = false;
+    } else if (cudaFree(it->second.partials) != cudaSuccess) {
+        return DG_ERR_CUDA;
+    }
+    map.erase(it);
+    return DG_OK;
+}
+
+void dg_reload_env(void) {
+    const Knobs* k = new Knobs(read_knobs());
+    (void)knobs();   // the first snapshot exists before it is replaced
+    g_knobs.store(k, std::memory_order_release);
 }
 
 void dg_set_wait_timeout_us(uint64_t us) {

@@ -38,9 +38,28 @@ struct DeviceState {
 // Returns the current device's state, creating it on first use.
 dg_status current_device_state(DeviceState** out);
 
-// Whether launches use programmatic dependent launch (on unless the
-// environment sets DG_PDL=0; read once).
-bool pdl_enabled();
+// Tuning and diagnostic switches taken from DG_* environment variables.
+// They are read once, on first use, and again only by dg_reload_env(); the
+// per-call path reads this snapshot and never the environment.
+struct Knobs {
+    bool pdl = true;            // DG_PDL=0: no programmatic dependent launch
+    bool log = false;           // DG_LOG=1: one stderr line per GEMM call
+    int gemv_max_m = 2;         // DG_GEMV_MAX_M (0..16): largest M on the GEMV
+    int gemv_rows = 0;          // DG_GEMV_ROWS (4, 8, 16): GEMV rows of B per CTA, M <= 2
+    int splitk = -1;            // DG_SPLITK: 0 off, 1 for every M <= 128, else planned
+    int splitk_grid = 0;        // DG_SPLITK_GRID: CTAs of a split-K launch
+    int splitk_prefetch = -1;   // DG_SPLITK_PREFETCH (0..256): B boxes moved into L2 early
+    int splitk_kps = 2;         // DG_SPLITK_KPS (1, 2): K blocks per split-K stage
+    bool one_wave = true;       // DG_ONE_WAVE=0: no one-wave tile rule
+    int64_t one_wave_kb = 64;   // DG_ONE_WAVE_KB: K-block limit of that rule
+    int force_block_n = 0;      // DG_FORCE_BLOCK_N: tile width of the tiled kernels
+    int two_cta = -1;           // DG_2CTA: 0 no CTA pairs, 1 pairs for every M >= 256
+    int group_m = 0;            // DG_GROUP_M (1..4096): raster group of M tiles
+};
+const Knobs& knobs();
+
+// Whether launches use programmatic dependent launch (knobs().pdl).
+inline bool pdl_enabled() { return knobs().pdl; }
 
 // Launches `kern` on `s`, with programmatic stream serialization when
 // pdl_enabled(): the kernel may be scheduled while the preceding kernel in

@@ -93,6 +93,10 @@ extern "C" dg_status dg_fp8_gemm_splitk_static(const uint8_t* A, const uint8_t* 
         return DG_ERR_INVALID_VALUE;
     if (K > 0 && out == DG_E4M3 && scale_d == nullptr) return DG_ERR_INVALID_VALUE;
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 16) != 0) return DG_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(scale_a) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(scale_b) & 3u) != 0 ||
+        (out == DG_E4M3 && (reinterpret_cast<uintptr_t>(scale_d) & 3u) != 0))
+        return DG_ERR_MISALIGNED;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) {
         const size_t bytes = static_cast<size_t>(M * N) * (out == DG_E4M3 ? 1 : 2);

@@ -42,7 +42,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "dg_internal.h"
@@ -632,11 +631,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
 // B boxes each CTA prefetches into L2 before its dependency wait:
 // DG_SPLITK_PREFETCH=n (sweeps, 0..256), default one ring.
 int splitk_prefetch_kblocks(int ring) {
-    if (const char* v = std::getenv("DG_SPLITK_PREFETCH")) {
-        const int n = std::atoi(v);
-        if (n >= 0 && n <= 256) return n;
-    }
-    return ring;
+    const int n = knobs().splitk_prefetch;
+    return n >= 0 ? n : ring;
 }
 
 template <bool kFp16In, int KPS, int NC>
@@ -684,13 +680,7 @@ cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cuda
 }
 
 // K blocks per stage: DG_SPLITK_KPS=1|2 (sweeps), default 2.
-int splitk_kps() {
-    if (const char* v = std::getenv("DG_SPLITK_KPS")) {
-        const int k = std::atoi(v);
-        if (k == 1 || k == 2) return k;
-    }
-    return 2;
-}
+int splitk_kps() { return knobs().splitk_kps; }
 
 // MMA N for M rows of A: M rounded up to 16, 32, 64 or 128.
 int nc_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
@@ -740,9 +730,8 @@ void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg
     const int64_t per_tile = sm_count / tiles;
     const int64_t g = per_tile >= 2 ? per_tile * tiles : sm_count;
     p->grid = static_cast<int>(units < g ? units : g);
-    if (const char* v = std::getenv("DG_SPLITK_GRID")) {   // sweeps: CTAs per launch
-        const int64_t g = std::atoll(v);
-        if (g >= 1 && g <= sm_count && g <= units) p->grid = static_cast<int>(g);
+    if (const int64_t g = knobs().splitk_grid) {   // sweeps: CTAs per launch
+        if (g <= sm_count && g <= units) p->grid = static_cast<int>(g);
     }
     p->smem_bytes = smem_for_nc(nc);
 }

@@ -32,7 +32,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "dg_internal.h"
@@ -406,11 +405,9 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     // 4096.  DG_ONE_WAVE=0 turns the rule off and DG_ONE_WAVE_KB sets its
     // K-block limit (sweeps).
     const int64_t kblocks = (K + (fp16_in ? 64 : 128) - 1) / (fp16_in ? 64 : 128);
-    const char* ow = std::getenv("DG_ONE_WAVE");
+    const Knobs& kn = knobs();
     bool one_wave = false;
-    int64_t max_kb = 64;
-    if (const char* mk = std::getenv("DG_ONE_WAVE_KB")) max_kb = std::atoll(mk);
-    if (!(ow != nullptr && ow[0] == '0') && kblocks <= max_kb) {
+    if (kn.one_wave && kblocks <= kn.one_wave_kb) {
         for (int i = 5; i >= 0; --i) {   // narrowest first
             if (num_m * ((N + cand[i] - 1) / cand[i]) <= sm_count) {
                 // past 32 K blocks a wide tile is MMA-bound enough for the
@@ -425,8 +422,8 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
         }
     }
     // DG_FORCE_BLOCK_N=64|128|160|192|224|256 pins the tile width (sweeps).
-    if (const char* f = std::getenv("DG_FORCE_BLOCK_N")) {
-        const int v = std::atoi(f);
+    {
+        const int v = kn.force_block_n;
         if (v == 64 || v == 128 || v == 160 || v == 192 || v == 224 || v == 256) best = v;
     }
     const int64_t tiles = num_m * ((N + best - 1) / best);
@@ -444,9 +441,8 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     // 8192^3 E4M3 3607 vs 3399 TFLOP/s (1.06); at 4096^3 (BN 224) both run
     // 48 us.  Pairs are used when their estimate is no worse; DG_2CTA=0
     // disables them, DG_2CTA=1 forces them for M >= 256.
-    const char* pair_env = std::getenv("DG_2CTA");
-    const bool pairs_off = pair_env != nullptr && pair_env[0] == '0';
-    const bool pairs_forced = pair_env != nullptr && pair_env[0] == '1';
+    const bool pairs_off = kn.two_cta == 0;
+    const bool pairs_forced = kn.two_cta == 1;
     if (!pairs_off && (!one_wave || pairs_forced) && M >= 256 && sm_count >= 2) {
         const int64_t pm = (M + 255) / 256;
         const int slots = sm_count / 2;
@@ -461,8 +457,8 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
             const double cost = static_cast<double>(waves) * bn / peff[i];
             if (i == 0 || cost < pcost) { pbest = bn; pcost = cost; }
         }
-        if (const char* f = std::getenv("DG_FORCE_BLOCK_N")) {
-            const int v = std::atoi(f);
+        {
+            const int v = kn.force_block_n;
             if (v == 128 || v == 160 || v == 192 || v == 224 || v == 256) pbest = v;
         }
         if (pairs_forced || pcost <= best_cost) {
@@ -498,10 +494,7 @@ Params make_params(const TcLaunch& L) {
     prm.group_m = ((L.M + kBM - 1) / kBM) >= 48 ? 32 : 8;
     if (L.plan->block_m == 256) prm.group_m /= 2;   // pair tiles are 256 rows
     // DG_GROUP_M=<n> overrides the raster group size (sweeps).
-    if (const char* g = std::getenv("DG_GROUP_M")) {
-        const int v = std::atoi(g);
-        if (v >= 1 && v <= 4096) prm.group_m = v;
-    }
+    if (knobs().group_m != 0) prm.group_m = knobs().group_m;
     prm.group_off = L.group_off;
     prm.groups = L.groups;
     return prm;

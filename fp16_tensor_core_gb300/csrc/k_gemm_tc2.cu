@@ -33,7 +33,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "dg_internal.h"

@@ -18,14 +18,18 @@
  *            workspace (two 128 x 128 FP32 partial tiles per SM and 8192
  *            counters, 20 MB on 152 SMs) that live until exit.  Split-K
  *            GEMMs (plan path 4) issued on a second, third, ... stream get a
- *            workspace of their own (same size, kept until exit) on that
- *            stream's first such call, so calls on different streams may run
- *            concurrently; that first call must not happen while the stream
- *            is being captured into a graph (it returns DG_ERR_UNSUPPORTED
- *            then).
+ *            workspace of their own (same size) on that stream's first such
+ *            call, so calls on different streams may run concurrently; that
+ *            first call must not happen while the stream is being captured
+ *            into a graph (it returns DG_ERR_UNSUPPORTED then).  A stream
+ *            keeps its workspace until dg_release_stream(stream) or exit.
+ *            At most 16 streams per device hold an allocated one at a time;
+ *            past that, split-K shapes on further streams run on the tiled
+ *            tensor-core kernel (no workspace, same tolerance).
  * Layout.    Dense, row-major, no leading-dimension arguments: A is M x K,
  *            B is N x K (both K contiguous, the "TN" form), D is M x N.
- * Alignment. Every data pointer must be 16-byte aligned and K * element
+ * Alignment. Every data pointer must be 16-byte aligned, every FP32 device
+ *            scalar (scales, amax words) 4-byte aligned, and K * element
  *            size must be a multiple of 16 bytes; otherwise the call returns
  *            DG_ERR_MISALIGNED and launches nothing (there is no slow path).
  * Streams.   Work is enqueued on `stream` (NULL = the legacy default stream)
@@ -74,8 +78,9 @@ typedef enum {
  *              n == 0.
  *   scale_out  FP32[1], device, may be NULL: amax / 448 as one binary32
  *              division, or 1 when amax == 0.
- * Three stream operations: a 4-byte memset of amax_out, a reduction kernel,
- * and (when scale_out is set) a one-thread kernel. */
+ * Three kernel launches on the stream: a one-thread kernel that zeroes
+ * amax_out, the reduction, and (when scale_out is set) a one-thread kernel
+ * that forms the scale. */
 dg_status dg_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
                   dg_stream_t stream);
 
@@ -202,7 +207,9 @@ dg_status dg_quantize_e4m3_amax(const float* x, int64_t n, const float* scale,
  *          rows of B); larger sizes return DG_ERR_INVALID_VALUE.
  *   status_out  optional device uint32, 4-byte aligned: the kernel ORs its
  *          error bits into it (1 = a bounded wait ran out, the output is
- *          incomplete).  NULL: the bits go to a library word nobody reads.
+ *          incomplete).  It is the only way to learn of a timeout on this
+ *          entry point: dg_sync_status does not see these bits, and with
+ *          status_out NULL they go to a library word nobody reads.
  * Each call first zeroes the arrival counters of the static workspace on
  * `stream` (cudaMemsetAsync), then launches the kernel.  Calls share that one
  * workspace per device: two calls whose executions overlap (different
@@ -291,6 +298,22 @@ dg_status dg_init(void);
  * status word: DG_ERR_TIMEOUT if a kernel's bounded wait ran out since the
  * last call, DG_ERR_CUDA if the synchronisation failed, else DG_OK. */
 dg_status dg_sync_status(dg_stream_t stream);
+
+/* Gives back the split-K workspace that `stream` holds on the current
+ * device (see Memory above): synchronises the stream, then frees the
+ * workspace (or returns the device's own to the pool).  Call it before
+ * destroying a stream that ran split-K GEMMs; a later split-K call on the
+ * stream takes a workspace again.  A stream that holds none: DG_OK, no
+ * synchronisation.  DG_ERR_CUDA if the synchronisation or the free fails.
+ * Not while the stream is being captured, nor concurrently with GEMM calls
+ * on the same stream. */
+dg_status dg_release_stream(dg_stream_t stream);
+
+/* Re-reads the DG_* tuning variables of the environment (tile, path and
+ * launch switches used for sweeps and tests).  They are otherwise read
+ * once, at the library's first call; no call reads the environment
+ * again.  Applies to calls made afterwards. */
+void dg_reload_env(void);
 
 /* Upper bound, in microseconds, on any single in-kernel wait (default
  * 2 000 000).  Applies to launches made after the call. */

@@ -40,6 +40,22 @@ def test_library_exports_every_declared_symbol(L):
         getattr(L, "dgo_gemm_e4m3")
 
 
+def test_reload_env_reads_the_tuning_variables(L):
+    """Tuning variables are read once; a change shows only after dg_reload_env."""
+    import os
+    dg.dg_reload_env()
+    assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=152)["path"] == 4
+    os.environ["DG_SPLITK"] = "0"
+    try:
+        assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=152)["path"] == 4   # not re-read yet
+        dg.dg_reload_env()
+        assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=152)["path"] == 3
+    finally:
+        os.environ.pop("DG_SPLITK", None)
+        dg.dg_reload_env()
+    assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=152)["path"] == 4
+
+
 def test_status_strings_and_version(L):
     assert dg.dg_status_string(dg.DG_OK) == "DG_OK"
     assert dg.dg_status_string(dg.DG_ERR_TIMEOUT) == "DG_ERR_TIMEOUT"
@@ -69,6 +85,11 @@ FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced: every call below f
     ((FAKE, FAKE + 8, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
     ((FAKE, FAKE, FAKE + 2, 8, 8, 16, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
     ((FAKE, FAKE, FAKE, 8, 8, 24, FAKE, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
+    # FP32 scales that a 4-byte load cannot read
+    ((FAKE, FAKE, FAKE, 8, 8, 16, FAKE + 1, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE, 8, 8, 16, FAKE, FAKE + 2, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, FAKE + 3, dg.DG_E4M3, None), dg.DG_ERR_MISALIGNED),
+    ((FAKE, FAKE, FAKE, 1, 8, 16, FAKE + 1, FAKE, None, dg.DG_BF16, None), dg.DG_ERR_MISALIGNED),
 ])
 def test_fp8_gemm_argument_errors(L, args, expect):
     assert L.dg_fp8_gemm(*args) == expect
@@ -93,6 +114,8 @@ def test_gemm_amax_argument_errors(L):
     assert L.dg_fp8_gemm_amax(*bad, FAKE, None) == dg.DG_ERR_MISALIGNED        # K pitch
     e4 = (FAKE, FAKE, FAKE, 8, 8, 16, FAKE, FAKE, None, dg.DG_E4M3)
     assert L.dg_fp8_gemm_amax(*e4, FAKE, None) == dg.DG_ERR_INVALID_VALUE      # no scale_d
+    sa1 = (FAKE, FAKE, FAKE, 8, 8, 16, FAKE + 1, FAKE, None, dg.DG_BF16)
+    assert L.dg_fp8_gemm_amax(*sa1, FAKE, None) == dg.DG_ERR_MISALIGNED        # scale_a
 
 
 def test_grouped_argument_errors(L):
@@ -112,6 +135,9 @@ def test_grouped_argument_errors(L):
     assert call(K=24) == dg.DG_ERR_MISALIGNED
     assert call(M=-1) == dg.DG_ERR_INVALID_VALUE
     assert call(N=1 << 30, G=8) == dg.DG_ERR_INVALID_VALUE      # groups * N overflows
+    assert call(sa=FAKE + 1) == dg.DG_ERR_MISALIGNED
+    assert call(sb=FAKE + 2) == dg.DG_ERR_MISALIGNED
+    assert call(sd=FAKE + 3, out=dg.DG_E4M3) == dg.DG_ERR_MISALIGNED
 
 
 def test_splitk_static_argument_errors(L):
@@ -131,6 +157,9 @@ def test_splitk_static_argument_errors(L):
     assert call(K=24) == dg.DG_ERR_MISALIGNED
     assert call(A=FAKE + 8) == dg.DG_ERR_MISALIGNED
     assert call(status=FAKE + 2) == dg.DG_ERR_MISALIGNED
+    assert call(sa=FAKE + 1) == dg.DG_ERR_MISALIGNED
+    assert call(sb=FAKE + 2) == dg.DG_ERR_MISALIGNED
+    assert call(sd=FAKE + 3, out=dg.DG_E4M3) == dg.DG_ERR_MISALIGNED
     assert call(M=0) == dg.DG_OK and call(N=0) == dg.DG_OK       # empty: nothing launched
 
 
@@ -224,10 +253,12 @@ def test_plan_paths_and_tiles(L):
     assert dg.dg_gemm_plan(5, 200, 256, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16,
                            sm_count=sm)["grid"] == 8
     os.environ["DG_SPLITK"] = "0"
+    dg.dg_reload_env()
     try:
         assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=sm)["path"] == 3
     finally:
         del os.environ["DG_SPLITK"]
+        dg.dg_reload_env()
     # 17 <= M <= 128: split-K only where the tiled plan leaves SMs idle and the
     # time estimate favours it (few columns of A, or a long K per tile)
     for m in (17, 32):
@@ -245,6 +276,7 @@ def test_plan_paths_and_tiles(L):
                     (64, 1024, 4096), (128, 32768, 4096), (129, 4096, 4096)):
         assert dg.dg_gemm_plan(m, n, k, sm_count=sm)["path"] == 3, (m, n, k)
     os.environ["DG_SPLITK"] = "1"
+    dg.dg_reload_env()
     try:
         for m, nc in ((33, 64), (64, 64), (65, 128), (128, 128)):
             p = dg.dg_gemm_plan(m, 4096, 4096, sm_count=sm)
@@ -253,14 +285,17 @@ def test_plan_paths_and_tiles(L):
         assert dg.dg_gemm_plan(129, 4096, 4096, sm_count=sm)["path"] == 3
     finally:
         del os.environ["DG_SPLITK"]
+        dg.dg_reload_env()
     assert dg.dg_gemm_plan(16, 128 * 8192 + 1, 64, sm_count=sm)["path"] == 3   # too many tiles
     os.environ["DG_GEMV_MAX_M"] = "16"
+    dg.dg_reload_env()
     try:
         for m, rows in ((4, 8), (5, 4), (16, 4)):
             p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
             assert p["path"] == 2 and p["block_n"] == rows and p["grid"] == 12288 // rows
     finally:
         del os.environ["DG_GEMV_MAX_M"]
+        dg.dg_reload_env()
     for m in (17, 63, 65, 129, 256, 4096, 8192):
         p = dg.dg_gemm_plan(m, 1000, 1040, sm_count=sm)
         assert p["path"] == 3

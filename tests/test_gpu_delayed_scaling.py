@@ -51,10 +51,13 @@ def _amax_bound(R, S, sa, sb):
 ])
 def test_output_amax_matches_oracle(M, N, K, pairs, path):
     os.environ["DG_2CTA"] = pairs
+    dg.dg_reload_env()
     if path == 2:
         os.environ["DG_GEMV_MAX_M"] = "16"
+        dg.dg_reload_env()
     if path == 4 and M > 16:
         os.environ["DG_SPLITK"] = "1"
+        dg.dg_reload_env()
     try:
         assert dg.dg_gemm_plan(M, N, K, dg.DG_E4M3, dg.DG_BF16)["path"] == path
         A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
@@ -77,6 +80,7 @@ def test_output_amax_matches_oracle(M, N, K, pairs, path):
         os.environ.pop("DG_2CTA", None)
         os.environ.pop("DG_GEMV_MAX_M", None)
         os.environ.pop("DG_SPLITK", None)
+        dg.dg_reload_env()
 
 
 def test_delayed_scaling_round_trip():

@@ -27,6 +27,7 @@ def _lib():
     dg.dg_init()
     yield
     os.environ.pop("DG_2CTA", None)
+    dg.dg_reload_env()
     assert dg.dg_sync_status() == dg.DG_OK
 
 
@@ -34,11 +35,14 @@ def _lib():
 def kernel(request):
     old = os.environ.get("DG_2CTA")
     os.environ["DG_2CTA"] = "1" if request.param == "pair" else "0"
+    dg.dg_reload_env()
     yield request.param
     if old is None:
         os.environ.pop("DG_2CTA", None)
+        dg.dg_reload_env()
     else:
         os.environ["DG_2CTA"] = old
+        dg.dg_reload_env()
 
 
 def _expect_kernel(kind, M, N, K, in_dtype=dg.DG_E4M3):

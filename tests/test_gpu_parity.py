@@ -330,6 +330,7 @@ def test_gemv_for_larger_m_when_forced(M, N, K):
     """The GEMV handles M up to 16 (its 2-, 4-, 8- and 16-row instantiations),
     although the planner only sends M <= 2 to it by default."""
     os.environ["DG_GEMV_MAX_M"] = "16"
+    dg.dg_reload_env()
     try:
         assert dg.dg_gemm_plan(M, N, K)["path"] == 2
         A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
@@ -338,3 +339,4 @@ def test_gemv_for_larger_m_when_forced(M, N, K):
         hgemm_case(A16, B16)
     finally:
         del os.environ["DG_GEMV_MAX_M"]
+        dg.dg_reload_env()

@@ -83,6 +83,7 @@ def test_splitk_wide_bf16_matches_oracle(M, N, K):
     """17 <= M <= 128: MMA N = 32 / 64 / 128 columns of A per CTA, the
     partial slots and the fixup walked 16 columns at a time."""
     os.environ["DG_SPLITK"] = "1"
+    dg.dg_reload_env()
     try:
         p = _plan(M, N, K)
         assert p["block_m"] == (32 if M <= 32 else 64 if M <= 64 else 128), p
@@ -96,11 +97,13 @@ def test_splitk_wide_bf16_matches_oracle(M, N, K):
         check_bf16_like(d, R, S, sa_ref, sb_ref)
     finally:
         os.environ.pop("DG_SPLITK", None)
+        dg.dg_reload_env()
 
 
 @pytest.mark.parametrize("M,N,K", [(48, 1000, 2080), (120, 640, 1040)])
 def test_splitk_wide_e4m3_out_and_fp16(M, N, K):
     os.environ["DG_SPLITK"] = "1"
+    dg.dg_reload_env()
     try:
         _plan(M, N, K)
         A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
@@ -129,6 +132,7 @@ def test_splitk_wide_e4m3_out_and_fp16(M, N, K):
                         R16, S16, 1.0, 1.0, "FP16")
     finally:
         os.environ.pop("DG_SPLITK", None)
+        dg.dg_reload_env()
 
 
 @pytest.mark.parametrize("M,N,K", [(48, 4096, 2048), (24, 2048, 1040)])
@@ -138,6 +142,7 @@ def test_splitk_staged_fixup_all_outputs(M, N, K):
     partial tile fits in the ring): BF16 and E4M3 out from E4M3 inputs and
     FP16 out from FP16 inputs."""
     os.environ["DG_SPLITK"] = "1"
+    dg.dg_reload_env()
     try:
         p = _plan(M, N, K)
         assert p["grid"] % p["tiles"] == 0 and p["grid"] // p["tiles"] >= 2, p
@@ -172,11 +177,13 @@ def test_splitk_staged_fixup_all_outputs(M, N, K):
                         1.0, 1.0, "FP16")
     finally:
         os.environ.pop("DG_SPLITK", None)
+        dg.dg_reload_env()
 
 
 def test_splitk_m1_when_forced():
     """M = 1 and 2 on the split-K kernel (the GEMV crossover moved to 0)."""
     os.environ["DG_GEMV_MAX_M"] = "0"
+    dg.dg_reload_env()
     try:
         for M in (1, 2):
             N, K = 1000, 1040
@@ -190,6 +197,7 @@ def test_splitk_m1_when_forced():
                             sa_ref, sb_ref)
     finally:
         os.environ.pop("DG_GEMV_MAX_M", None)
+        dg.dg_reload_env()
 
 
 def test_splitk_qkv_m16_sampled():
@@ -298,6 +306,7 @@ def test_splitk_staged_fixup_repeatable_back_to_back(M, N, K):
     arrival atomic; a missing ordering would show as an occasional stale
     partial, so a different sum."""
     os.environ["DG_SPLITK"] = "1"
+    dg.dg_reload_env()
     try:
         p = _plan(M, N, K)
         assert p["grid"] % p["tiles"] == 0
@@ -327,6 +336,7 @@ def test_splitk_staged_fixup_repeatable_back_to_back(M, N, K):
         assert dg.dg_sync_status() == dg.DG_OK
     finally:
         os.environ.pop("DG_SPLITK", None)
+        dg.dg_reload_env()
 
 
 def test_splitk_timeout_then_recovers():

@@ -44,6 +44,7 @@ def _inputs(M, N, K):
 ])
 def test_static_workspace_matches_regular_entry(M, N, K, out):
     os.environ["DG_GEMV_MAX_M"] = "0"     # the regular entry takes the split-K path for M = 1 too
+    dg.dg_reload_env()
     try:
         assert dg.dg_gemm_plan(M, N, K, dg.DG_E4M3, out)["path"] == 4
         qa, qb, sa, sb, *_ = _inputs(M, N, K)
@@ -62,6 +63,7 @@ def test_static_workspace_matches_regular_entry(M, N, K, out):
             assert torch.equal(D, ref)
     finally:
         os.environ.pop("DG_GEMV_MAX_M", None)
+        dg.dg_reload_env()
 
 
 def test_static_workspace_matches_oracle():
