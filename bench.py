@@ -38,9 +38,14 @@ FLOP_PER_STEP = 2.0 * M * N * K
 WORKLOAD = "fp8_8192_e4m3out"
 CPU_SAMPLE_ROWS = 3072  # ~10-20 s of oracle work on 16 cores
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
-# Sources of the kernel the headline step runs (CTA-pair tensor-core GEMM).
+# Kernel sources whose change invalidates recorded ncu traffic (the tiled
+# GEMMs, the split-K kernel and the GEMV).
 GEMM_SOURCES = [os.path.join(ROOT, "fp16_tensor_core_gb300", "csrc", f)
-                for f in ("k_gemm_tc2.cu", "gemm_common.cuh", "dg_ptx.cuh")]
+                for f in ("k_gemm_tc2.cu", "k_gemm_tc.cu", "k_gemm_skinny.cu", "k_gemv.cu",
+                          "gemm_common.cuh", "dg_ptx.cuh")]
+# Nominal dense FP8 tensor rate of one GB300 (NVIDIA's figure without 2:4
+# sparsity), for context beside the measured-peak fraction.
+NOMINAL_FP8_TFLOPS = 4500.0
 
 
 # ---------------------------------------------------------------- plumbing
@@ -113,16 +118,18 @@ def gemm_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+def recorded_traffic(workload: str = WORKLOAD):
+    """DRAM bytes per launch of `workload`'s kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as f:
         rec = json.load(f)
-    if rec.get("source_sha256_16") != gemm_source_hash() or rec.get("workload") != WORKLOAD:
-        return None
-    return rec.get("dram_bytes_per_launch")
+    entries = rec.get("entries", [rec])
+    for e in entries:
+        if e.get("workload") == workload and e.get("source_sha256_16") == gemm_source_hash():
+            return e.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:
@@ -493,6 +500,35 @@ def extras(torch, dg, stream, peaks) -> dict:
     return out
 
 
+def compact(rec: dict) -> dict:
+    """The per-workload numbers that matter, rounded (keeps the line short)."""
+    keep = {"us": 2, "us_stream": 2, "TFLOPS": 1, "GB/s": 0, "frac_hbm": 3, "frac_fp8_peak": 3,
+            "frac_fp16_peak": 3}
+    return {k: round(rec[k], d) for k, d in keep.items() if k in rec}
+
+
+# Kernels behind the bandwidth-bound decode shapes (the M <= 16 half of the metric).
+SKINNY_ROOFLINES = {
+    "m1": ("qkv_gemv_1x12288x4096", "gemv_kernel (CUDA cores, M = 1)"),
+    "m16": ("qkv_m16_16x12288x4096", "gemm_skinny_kernel (split-K tcgen05, M = 16)"),
+}
+
+
+def skinny_roofline(ex: dict, key: str, peaks: dict) -> dict:
+    """roofline-shaped entry for one decode shape, from its `extra` record."""
+    name, kernel = SKINNY_ROOFLINES[key]
+    rec = ex[name]
+    m = int(name.split("_")[-1].split("x")[0])
+    algo = 12288 * 4096 + m * 4096 + m * 12288 * 2
+    return {"bound": "hbm", "kernel": kernel, "workload": name.replace("_", " "),
+            "achieved": round(rec["GB/s"], 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(rec["GB/s"] / peaks["hbm_gbs"], 4), "us": round(rec["us"], 3),
+            "us_stream": round(rec.get("us_stream", rec["us"]), 3),
+            "algorithmic_bytes": algo, "traffic": recorded_traffic(name),
+            "timing": "CUDA events over 250 graph-replayed back-to-back launches, weights "
+                      "rotated over copies larger than 3 x L2"}
+
+
 def run_kernel(args):
     """`--kernel NAME`: time one kernel workload alone (W warm-up + K timed
     launches); used for ncu captures and tile sweeps."""
@@ -684,13 +720,16 @@ def run_own(args):
         },
         "roofline": {
             "bound": "tensor",
-            "kernel": f"gemm_tc_kernel (tcgen05 E4M3, {plan['block_m']}x{plan['block_n']} tiles, "
+            "kernel": f"{'gemm_tc_pair_kernel' if plan['block_m'] == 256 else 'gemm_tc_kernel'} "
+                      f"(tcgen05 E4M3, {plan['block_m']}x{plan['block_n']} tiles, "
                       f"{plan['stages']} stages, grid {plan['grid']})",
             "achieved": achieved,
             "peak": fp8_peak,
             "unit": "TFLOP/s",
             "frac": achieved / fp8_peak,
             "peak_source": f"{peaks['source']}: bf16 burst {peaks['bf16_tflops']} x 2 (FP8/BF16 dense ratio)",
+            "frac_vs_nominal": achieved / NOMINAL_FP8_TFLOPS,
+            "nominal_peak": NOMINAL_FP8_TFLOPS,
             "launch_ms": gemm_ms,
             "traffic": traffic,
         },
@@ -706,8 +745,12 @@ def run_own(args):
         "clocks": clk,
     }
     del hA, hB, hD, wls
+    skinny = {}
     if rank == 0 and not args.no_extra:
-        line["extra"] = extras(torch, dg, stream, peaks)
+        ex = extras(torch, dg, stream, peaks)
+        skinny = {k: skinny_roofline(ex, k, peaks) for k in SKINNY_ROOFLINES}
+        line["roofline"].update(skinny)
+        line["extra"] = {k: compact(v) for k, v in ex.items()}
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline_sample(A32, B32, sd, rows=CPU_SAMPLE_ROWS)
         line["cpu_baseline"] = {
@@ -717,6 +760,9 @@ def run_own(args):
                       f"({CPU_SAMPLE_ROWS}x8192x8192): full-tensor "
                       "amax/scale of A and B, quantise of the sampled rows and all of B, FP64 "
                       "contraction, E4M3 epilogue"}
+    # The decode shapes last, so that they sit in the line's tail.
+    for k, v in skinny.items():
+        line[f"roofline_{k}"] = v
     if rank == 0:
         print(json.dumps(line), flush=True)
 

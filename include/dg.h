@@ -199,9 +199,12 @@ dg_status dg_quantize_e4m3_amax(const float* x, int64_t n, const float* scale,
  * split-K tensor-core kernel (plan path 4) runs with its workspace in fixed
  * static device arrays of the library (2.5 MiB of FP32 partial tiles and
  * 1025 32-bit words) instead of memory the library allocates.  The pages
- * have no counterpart; it exists for callers that forbid allocation inside
- * library calls.  For the same arguments the result is bit-identical to
- * dg_fp8_gemm on the split-K path.
+ * have no counterpart.  It is for callers that cannot let a library call
+ * cudaMalloc: a process whose own pool allocator has already reserved the
+ * device memory, code running while a stream is captured in global mode
+ * (where cudaMalloc is refused), or a latency-bound loop that cannot take
+ * cudaMalloc's implicit synchronisation.  For the same arguments the
+ * result is bit-identical to dg_fp8_gemm on the split-K path.
  *   A, B, D, M, N, K, scale_a, scale_b, scale_d, out, stream: as
  *          dg_fp8_gemm, with M <= 16 and N <= 131072 (1024 tiles of 128
  *          rows of B); larger sizes return DG_ERR_INVALID_VALUE.

@@ -200,8 +200,8 @@ def test_splitk_m1_when_forced():
         dg.dg_reload_env()
 
 
-def test_splitk_qkv_m16_sampled():
-    """The decode QKV weight shape with 16 activation rows, sampled."""
+def test_splitk_qkv_m16_all_outputs():
+    """The decode QKV weight shape with 16 activation rows, every output."""
     M, N, K = 16, 12288, 4096
     _plan(M, N, K)
     A, B = synth.make_inputs("fp8_qkv", M=M)
@@ -212,9 +212,8 @@ def test_splitk_qkv_m16_sampled():
     D = torch.empty((M, N), dtype=torch.int16, device="cuda")
     dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16)
     assert dg.dg_sync_status() == dg.DG_OK
-    ms, ns = sample_positions(M, N, 4000, tile_m=16, tile_n=128)
-    R, S = oracle.gemm_e4m3_at(qa_ref, qb_ref, ms, ns)
-    d = bf16_bits_to_f64(D.cpu().numpy().view(np.uint16)[ms, ns])
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    d = bf16_bits_to_f64(D.cpu().numpy().view(np.uint16))
     check_bf16_like(d, R, S, sa_ref, sb_ref)
 
 
