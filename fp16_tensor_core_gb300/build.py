@@ -18,8 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdg.so")
 
-SOURCES = ["dg_api.cu", "k_scale.cu", "k_gemv.cu", "k_gemm_tc.cu", "k_gemm_tc2.cu", "k_gemm_skinny.cu",
-           "dg_static.cu"]
+SOURCES = ["dg_api.cu", "k_scale.cu", "k_gemv.cu", "k_gemv_mma.cu", "k_gemm_tc.cu", "k_gemm_tc2.cu",
+           "k_gemm_skinny.cu", "dg_static.cu"]
 HEADERS = ["dg_ptx.cuh", "dg_internal.h", "gemm_common.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -83,6 +83,9 @@ Knobs read_knobs() {
     if (env_int("DG_FORCE_BLOCK_N", 64, 256, &v)) k.force_block_n = static_cast<int>(v);
     if (const char* e = std::getenv("DG_2CTA")) k.two_cta = e[0] == '0' ? 0 : e[0] == '1' ? 1 : -1;
     if (env_int("DG_GROUP_M", 1, 4096, &v)) k.group_m = static_cast<int>(v);
+    if (const char* e = std::getenv("DG_MMA_GEMV")) k.mma_gemv = e[0] == '0' ? 0 : e[0] == '1' ? 1 : -1;
+    if (env_int("DG_MMA_GEMV_WARPS", 4, 8, &v) && (v == 4 || v == 8))
+        k.mma_gemv_warps = static_cast<int>(v);
     return k;
 }
 
@@ -158,12 +161,12 @@ namespace {
 // DG_LOG=1: one line per GEMM call on stderr with the chosen path and tile.
 void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& p) {
     if (!knobs().log) return;
-    static const char* const kPath[5] = {"no-op", "zero-fill", "gemv", "tensor-core",
-                                         "split-k"};
+    static const char* const kPath[6] = {"no-op", "zero-fill", "gemv", "tensor-core",
+                                         "split-k", "gemv-mma"};
     std::fprintf(stderr,
                  "dg: %s M=%lld N=%lld K=%lld path=%s tile=%dx%d stages=%d tiles=%d grid=%d\n",
                  what, static_cast<long long>(M), static_cast<long long>(N),
-                 static_cast<long long>(K), kPath[p.path >= 0 && p.path <= 4 ? p.path : 0],
+                 static_cast<long long>(K), kPath[p.path >= 0 && p.path <= 5 ? p.path : 0],
                  p.block_m, p.block_n, p.stages, p.tiles, p.grid);
 }
 
@@ -216,6 +219,23 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     // split-K kernel a flat 11.1-11.5 us for M = 1..16; at K = 1024 4.4
     // against 6.9 us.  DG_GEMV_MAX_M (0..16) moves the crossover.
     const Knobs& kn = knobs();
+    // Decode shapes on the warp-MMA GEMV (B streamed into registers, K sums
+    // on the tensor cores, no workspace): one CTA per 16 rows of B, 4 warps
+    // splitting K when there are at least four CTAs per SM, else 8.
+    const int64_t kbytes = K * (fp16_in ? 2 : 1);
+    if (kn.mma_gemv == 1 && M <= 16 && kbytes <= INT32_MAX - 64) {
+        p->path = 5;
+        const int64_t ctas = (N + 15) / 16;
+        if (ctas > INT_MAX) return DG_ERR_UNSUPPORTED;
+        p->block_m = M <= 8 ? 8 : 16;
+        p->block_n = 16;
+        p->block_k = fp16_in ? 32 : 64;
+        p->stages = kn.mma_gemv_warps != 0 ? kn.mma_gemv_warps
+                                            : (ctas >= 4 * static_cast<int64_t>(sm_count) ? 4 : 8);
+        p->grid = static_cast<int>(ctas);
+        p->tiles = static_cast<int>(ctas);
+        return DG_OK;
+    }
     if (M <= kn.gemv_max_m) {
         p->path = 2;
         int rows = M <= 4 ? 8 : 4;   // 4 warps x (2 or 1) rows of B
@@ -399,6 +419,7 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             return from_cuda(launch_gemv(A, B, D, static_cast<int>(M), static_cast<int>(N),
                                          static_cast<int>(K), fp16_in, sa, sb, sd, ok, amax_bits,
                                          plan.block_n, plan.stages, s));
+        case 5:
         case 4:
         default: {
             TcLaunch L;
@@ -419,6 +440,7 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             L.amax_out = amax_bits;
             L.group_off = nullptr;
             L.groups = 0;
+            if (plan.path == 5) return from_cuda(launch_gemv_mma(L, s));
             if (plan.path == 4) {
                 SplitkWs ws;
                 rc = splitk_workspace(st, s, &ws);

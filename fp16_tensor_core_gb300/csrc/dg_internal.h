@@ -55,6 +55,8 @@ struct Knobs {
     int force_block_n = 0;      // DG_FORCE_BLOCK_N: tile width of the tiled kernels
     int two_cta = -1;           // DG_2CTA: 0 no CTA pairs, 1 pairs for every M >= 256
     int group_m = 0;            // DG_GROUP_M (1..4096): raster group of M tiles
+    int mma_gemv = -1;          // DG_MMA_GEMV: 0 off, 1 for every M <= 16, else planned
+    int mma_gemv_warps = 0;     // DG_MMA_GEMV_WARPS (4, 8): warps per CTA of that path
 };
 const Knobs& knobs();
 
@@ -133,6 +135,10 @@ cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s);
 // Grouped variant (single-CTA tiles; L.plan->block_n is 128 or 256).
 cudaError_t launch_gemm_tc_grouped(const TcLaunch& L, cudaStream_t s);
 constexpr int kMaxGemmGroups = 1024;
+
+// Decode-shape GEMM for 1 <= M <= 16 with the K sums on warp-level MMAs
+// (plan path 5): one CTA per 16 rows of B, L.plan->stages warps per CTA.
+cudaError_t launch_gemv_mma(const TcLaunch& L, cudaStream_t s);
 
 // Skinny split-K tensor-core GEMM (plan path 4).
 // partials must hold 2 * grid slots of nc_for(M) x 128 floats, with

@@ -278,7 +278,10 @@ typedef struct {
                        M <= 128 where it is estimated faster (operands
                        swapped: block_m = 16, 32, 64 or 128 padded rows of
                        A, block_n = 128 rows of B per tile, K blocks of all
-                       tiles spread over grid CTAs)                         */
+                       tiles spread over grid CTAs), 5 warp-MMA GEMV for
+                       M <= 16 (block_n = 16 rows of B per CTA, the K sum
+                       split over `stages` warps, block_k = K elements per
+                       warp step)                                           */
     int block_m;    /* output rows per tile (tensor-core paths)             */
     int block_n;    /* output columns per tile                              */
     int block_k;    /* K elements per pipeline stage                        */

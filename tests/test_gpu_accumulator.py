@@ -11,8 +11,8 @@ binary32 for every j (p is a multiple of the binary32 spacing at P, and
 every partial sum stays below the next power of two): FP32 accumulation in
 ANY order and grouping returns the exact result, while an accumulator that
 keeps fewer bits than FP32 next to P loses the small products outright.
-The exact results are powers of two (or small integers times one), so the
-BF16 / FP16 outputs represent them exactly and the check is equality.
+The exact results are powers of two times p, so the BF16 / FP16 outputs
+represent them exactly and the check is equality.
 
 Cases, for E4M3 inputs (kind::f8f6f4 MMA, 32 K elements per instruction)
 and FP16 inputs (kind::f16, 16 per instruction):
@@ -20,8 +20,8 @@ and FP16 inputs (kind::f16, 16 per instruction):
     in between, spread over many MMA instructions and K blocks;
   * within one instruction: P, the small products and -P inside one
     instruction's K window.
-Each runs on the GEMV, split-K (16 and 64 columns), single-CTA and CTA-pair
-kernels.  The E4M3 cases also read max |acc| back in binary32 through
+Each runs on the GEMV, split-K (16 and 64 columns), single-CTA, CTA-pair
+and warp-MMA GEMV kernels.  The E4M3 cases also read max |acc| back in binary32 through
 dg_fp8_gemm_amax, which must equal the exact largest output.
 """
 import numpy as np
@@ -53,6 +53,8 @@ KERNELS = {
     "splitk64": (64, 1000, {"DG_SPLITK": "1"}, 4, 64),
     "single_cta": (129, 1000, {"DG_2CTA": "0"}, 3, 128),
     "cta_pair": (512, 1000, {"DG_2CTA": "1"}, 3, 256),
+    "gemv_mma1": (1, 1000, {"DG_MMA_GEMV": "1"}, 5, None),
+    "gemv_mma16": (16, 1000, {"DG_MMA_GEMV": "1"}, 5, None),
 }
 
 

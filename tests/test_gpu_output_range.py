@@ -5,7 +5,8 @@ through the same map after the division by the output scale, so with a small
 scale_d many outputs saturate, and with a large one they fall into the E4M3
 subnormal range (|y| < 2^-6).  [DG-FP16] §3.3 is about FP16 overflow: a sum
 beyond 65504 becomes +-Inf when rounded to binary16.  Each case here drives
-one kernel (GEMV, split-K, single-CTA tiles, CTA pairs, grouped) into those
+one kernel (GEMV, split-K, single-CTA tiles, CTA pairs, warp-MMA GEMV,
+grouped) into those
 ranges and compares every output with the oracle: E4M3 codes within one
 step of e4m3(Dref / sD) and exactly +-448 where Dref / sD is clearly beyond
 the clamp; FP16 outputs +-Inf exactly where the exact sum is clearly beyond
@@ -30,6 +31,7 @@ PATHS = {
     "splitk": (8, 1000, 1040, {}, 4, 16),
     "single_cta": (129, 1000, 1040, {"DG_2CTA": "0"}, 3, 128),
     "cta_pair": (512, 1000, 1040, {"DG_2CTA": "1"}, 3, 256),
+    "gemv_mma": (16, 1000, 1040, {"DG_MMA_GEMV": "1"}, 5, None),
 }
 
 
