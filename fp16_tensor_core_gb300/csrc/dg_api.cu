@@ -84,7 +84,7 @@ Knobs read_knobs() {
     if (const char* e = std::getenv("DG_2CTA")) k.two_cta = e[0] == '0' ? 0 : e[0] == '1' ? 1 : -1;
     if (env_int("DG_GROUP_M", 1, 4096, &v)) k.group_m = static_cast<int>(v);
     if (const char* e = std::getenv("DG_MMA_GEMV")) k.mma_gemv = e[0] == '0' ? 0 : e[0] == '1' ? 1 : -1;
-    if (env_int("DG_MMA_GEMV_WARPS", 4, 8, &v) && (v == 4 || v == 8))
+    if (env_int("DG_MMA_GEMV_WARPS", 2, 8, &v) && (v == 2 || v == 3 || v == 4 || v == 8))
         k.mma_gemv_warps = static_cast<int>(v);
     return k;
 }

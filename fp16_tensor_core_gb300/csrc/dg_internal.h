@@ -56,7 +56,7 @@ struct Knobs {
     int two_cta = -1;           // DG_2CTA: 0 no CTA pairs, 1 pairs for every M >= 256
     int group_m = 0;            // DG_GROUP_M (1..4096): raster group of M tiles
     int mma_gemv = -1;          // DG_MMA_GEMV: 0 off, 1 for every M <= 16, else planned
-    int mma_gemv_warps = 0;     // DG_MMA_GEMV_WARPS (4, 8): warps per CTA of that path
+    int mma_gemv_warps = 0;     // DG_MMA_GEMV_WARPS (2, 3, 4, 8): warps per CTA of that path
 };
 const Knobs& knobs();
 

@@ -80,12 +80,14 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
 }
 
 // MT: MMAs per step (1: M <= 8, 2: M <= 16).  W: warps per CTA (K split).
-// U: steps whose loads are in flight together.
-// Resident CTAs per SM the register budget is capped for: six 4-warp CTAs
-// (912 on 152 SMs, so that N = 12288 / 16 = 768 CTAs fit one wave), three
-// 8-warp ones.
+// U: steps of B in flight per warp (2 U loads of 16 bytes per lane).
+// Shapes: W = 2, 3, 4 with U = 8, 6, 4, register-capped for six resident
+// CTAs per SM (912 on 152 SMs, so that N = 12288 / 16 = 768 CTAs fit one
+// wave); W = 8, U = 4 for small N, capped for three.
 template <int W>
 constexpr int min_ctas_per_sm() { return W >= 8 ? 3 : 6; }
+template <int W>
+constexpr int batch_for() { return W == 2 ? 8 : W == 3 ? 6 : 4; }
 
 template <int MT, bool kFp16, int W, int U>
 __global__ void __launch_bounds__(W * 32, min_ctas_per_sm<W>())
@@ -131,32 +133,36 @@ gemv_mma_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ B,
     const uint4 zero = make_uint4(0, 0, 0, 0);
     const int span = (s_end - s_begin) * kStepBytes;
     for (int o = 0; o < span; o += U * kStepBytes) {
-        uint4 bl[U], bh[U], al[U], ah[U];
+        // Only B is in flight across the batch; A (a few rows, L1-resident)
+        // is read right before its MMAs, so the registers go to B.
+        uint4 bl[U], bh[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int off = o + u * kStepBytes;
             bl[u] = off < lim_b_lo ? ld_stream(pb_lo + off, policy) : zero;
             bh[u] = off < lim_b_hi ? ld_stream(pb_hi + off, policy) : zero;
-            al[u] = off < lim_a_lo ? __ldg(reinterpret_cast<const uint4*>(pa_lo + off)) : zero;
-            if constexpr (MT == 2)
-                ah[u] = off < lim_a_hi ? __ldg(reinterpret_cast<const uint4*>(pa_hi + off)) : zero;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int off = o + u * kStepBytes;
+            const uint4 al = off < lim_a_lo ? __ldg(reinterpret_cast<const uint4*>(pa_lo + off)) : zero;
             // two MMAs per 16 loaded bytes: words (x, y), then (z, w)
             if constexpr (kFp16) {
-                mma_f16(c[0], bl[u].x, bh[u].x, bl[u].y, bh[u].y, al[u].x, al[u].y);
-                mma_f16(c[0], bl[u].z, bh[u].z, bl[u].w, bh[u].w, al[u].z, al[u].w);
-                if constexpr (MT == 2) {
-                    mma_f16(c[1], bl[u].x, bh[u].x, bl[u].y, bh[u].y, ah[u].x, ah[u].y);
-                    mma_f16(c[1], bl[u].z, bh[u].z, bl[u].w, bh[u].w, ah[u].z, ah[u].w);
-                }
+                mma_f16(c[0], bl[u].x, bh[u].x, bl[u].y, bh[u].y, al.x, al.y);
+                mma_f16(c[0], bl[u].z, bh[u].z, bl[u].w, bh[u].w, al.z, al.w);
             } else {
-                mma_e4m3(c[0], bl[u].x, bh[u].x, bl[u].y, bh[u].y, al[u].x, al[u].y);
-                mma_e4m3(c[0], bl[u].z, bh[u].z, bl[u].w, bh[u].w, al[u].z, al[u].w);
-                if constexpr (MT == 2) {
-                    mma_e4m3(c[1], bl[u].x, bh[u].x, bl[u].y, bh[u].y, ah[u].x, ah[u].y);
-                    mma_e4m3(c[1], bl[u].z, bh[u].z, bl[u].w, bh[u].w, ah[u].z, ah[u].w);
+                mma_e4m3(c[0], bl[u].x, bh[u].x, bl[u].y, bh[u].y, al.x, al.y);
+                mma_e4m3(c[0], bl[u].z, bh[u].z, bl[u].w, bh[u].w, al.z, al.w);
+            }
+            if constexpr (MT == 2) {
+                const uint4 ah =
+                    off < lim_a_hi ? __ldg(reinterpret_cast<const uint4*>(pa_hi + off)) : zero;
+                if constexpr (kFp16) {
+                    mma_f16(c[1], bl[u].x, bh[u].x, bl[u].y, bh[u].y, ah.x, ah.y);
+                    mma_f16(c[1], bl[u].z, bh[u].z, bl[u].w, bh[u].w, ah.z, ah.w);
+                } else {
+                    mma_e4m3(c[1], bl[u].x, bh[u].x, bl[u].y, bh[u].y, ah.x, ah.y);
+                    mma_e4m3(c[1], bl[u].z, bh[u].z, bl[u].w, bh[u].w, ah.z, ah.w);
                 }
             }
         }
@@ -227,8 +233,10 @@ cudaError_t launch_one(const TcLaunch& L, cudaStream_t s) {
 template <int MT, bool kFp16>
 cudaError_t launch_w(const TcLaunch& L, cudaStream_t s) {
     switch (L.plan->stages) {   // warps per CTA
-        case 8: return launch_one<MT, kFp16, 8, MT == 1 ? 4 : 2>(L, s);
-        default: return launch_one<MT, kFp16, 4, MT == 1 ? 4 : 2>(L, s);
+        case 2: return launch_one<MT, kFp16, 2, batch_for<2>()>(L, s);
+        case 3: return launch_one<MT, kFp16, 3, batch_for<3>()>(L, s);
+        case 8: return launch_one<MT, kFp16, 8, batch_for<8>()>(L, s);
+        default: return launch_one<MT, kFp16, 4, batch_for<4>()>(L, s);
     }
 }
 

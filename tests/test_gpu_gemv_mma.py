@@ -51,7 +51,7 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-@pytest.mark.parametrize("warps", ["4", "8"])
+@pytest.mark.parametrize("warps", ["2", "3", "4", "8"])
 def test_fp8_bf16_out(M, N, K, warps):
     with knobs(DG_MMA_GEMV_WARPS=warps):
         assert _plan(M, N, K)["stages"] == int(warps)
