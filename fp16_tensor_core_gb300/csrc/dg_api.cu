@@ -220,20 +220,38 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     // against 6.9 us.  DG_GEMV_MAX_M (0..16) moves the crossover.
     const Knobs& kn = knobs();
     // Decode shapes on the warp-MMA GEMV (B streamed into registers, K sums
-    // on the tensor cores, no workspace): one CTA per 16 rows of B, 4 warps
-    // splitting K when there are at least four CTAs per SM, else 8.
+    // on warp-level MMAs, no workspace), one CTA per 16 rows of B.  Measured
+    // on GB300 (graph-replayed, B from HBM; us): E4M3 x 12288 x 4096 at
+    // M = 1 / 2 / 4 / 8: 9.3-9.5 / 9.5-10.0 / 9.7-10.1 / 9.9-10.2 against
+    // 9.6 (GEMV) / 10.9 (GEMV) / 11.2-11.4 / 11.2-11.3 (split-K); x 4096 x
+    // 4096: 5.0-5.2 against 5.1-6.7; x 1000 x 1040: 2.1-2.3 against 2.3-5.1.
+    // With 9-16 rows of A an E4M3 step takes two MMAs, and the warp-level
+    // MMA rate (about 1/16 of the tcgen05 one on this part) then sets the
+    // time once N * K is large (16 x 12288 x 4096: 12.9 against 11.4 us on
+    // split-K), so split-K keeps those; FP16 operands carry half the
+    // products per byte and stay here (16 x 12288 x 4096: 20.8 against
+    // 21.6 us).  M = 1 with E4M3 and more CTAs than one wave of four-warp
+    // CTAs keeps the CUDA-core GEMV (1 x 28672 x 4096: 19.3 against 19.9).
+    // Warps per CTA: 8 up to two CTAs per SM (small N), 4 up to six (one
+    // wave), else 2; with two MMAs per step 2 from three CTAs per SM.
     const int64_t kbytes = K * (fp16_in ? 2 : 1);
-    if (kn.mma_gemv == 1 && M <= 16 && kbytes <= INT32_MAX - 64) {
+    const int64_t mma_ctas = (N + 15) / 16;
+    const int64_t sms = sm_count;
+    bool use_mma = M <= 16 && kbytes <= INT32_MAX - 64 && mma_ctas <= INT_MAX;
+    if (use_mma && kn.mma_gemv != 1) {
+        use_mma = kn.mma_gemv != 0 &&
+                  (fp16_in || M <= 8 || N * K <= (int64_t{1} << 22)) &&
+                  !(M == 1 && !fp16_in && mma_ctas > 6 * sms);
+    }
+    if (use_mma) {
         p->path = 5;
-        const int64_t ctas = (N + 15) / 16;
-        if (ctas > INT_MAX) return DG_ERR_UNSUPPORTED;
         p->block_m = M <= 8 ? 8 : 16;
         p->block_n = 16;
         p->block_k = fp16_in ? 32 : 64;
-        p->stages = kn.mma_gemv_warps != 0 ? kn.mma_gemv_warps
-                                            : (ctas >= 4 * static_cast<int64_t>(sm_count) ? 4 : 8);
-        p->grid = static_cast<int>(ctas);
-        p->tiles = static_cast<int>(ctas);
+        const int warps = mma_ctas <= 2 * sms ? 8 : (mma_ctas <= 6 * sms && M <= 8) ? 4 : 2;
+        p->stages = kn.mma_gemv_warps != 0 ? kn.mma_gemv_warps : warps;
+        p->grid = static_cast<int>(mma_ctas);
+        p->tiles = static_cast<int>(mma_ctas);
         return DG_OK;
     }
     if (M <= kn.gemv_max_m) {

@@ -12,8 +12,8 @@ int main(void) {
     /* 8192^3 E4M3 on 152 SMs: CTA-pair 256 x 256 tiles, one CTA per SM. */
     if (dg_gemm_plan(8192, 8192, 8192, DG_E4M3, DG_E4M3, 152, &p) != DG_OK) return 3;
     if (p.path != 3 || p.block_m != 256 || p.block_n != 256 || p.grid != 152) return 4;
-    /* M = 1 takes the GEMV path. */
-    if (dg_gemm_plan(1, 12288, 4096, DG_E4M3, DG_BF16, 152, &p) != DG_OK || p.path != 2) return 5;
+    /* M = 1 against the decode QKV weights takes the warp-MMA GEMV. */
+    if (dg_gemm_plan(1, 12288, 4096, DG_E4M3, DG_BF16, 152, &p) != DG_OK || p.path != 5) return 5;
     /* Argument errors come back before any device access. */
     if (dg_fp8_gemm(0, 0, 0, -1, 1, 16, 0, 0, 0, DG_BF16, 0) != DG_ERR_INVALID_VALUE) return 6;
     if (dg_gemm_plan(4, 4, 16, DG_BF16, DG_BF16, 10, &p) != DG_ERR_INVALID_VALUE) return 7;

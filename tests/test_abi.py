@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import fp16_tensor_core_gb300 as dg
+from _knobs import knobs
 from fp16_tensor_core_gb300 import build as dg_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -42,18 +43,17 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_reload_env_reads_the_tuning_variables(L):
     """Tuning variables are read once; a change shows only after dg_reload_env."""
-    import os
     dg.dg_reload_env()
-    assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=152)["path"] == 4
+    assert dg.dg_gemm_plan(16, 12288, 4096, sm_count=152)["path"] == 4
     os.environ["DG_SPLITK"] = "0"
     try:
-        assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=152)["path"] == 4   # not re-read yet
+        assert dg.dg_gemm_plan(16, 12288, 4096, sm_count=152)["path"] == 4   # not re-read yet
         dg.dg_reload_env()
-        assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=152)["path"] == 3
+        assert dg.dg_gemm_plan(16, 12288, 4096, sm_count=152)["path"] == 3
     finally:
         os.environ.pop("DG_SPLITK", None)
         dg.dg_reload_env()
-    assert dg.dg_gemm_plan(3, 12288, 4096, sm_count=152)["path"] == 4
+    assert dg.dg_gemm_plan(16, 12288, 4096, sm_count=152)["path"] == 4
 
 
 def test_status_strings_and_version(L):
@@ -214,8 +214,45 @@ def test_scale_and_quantise_argument_errors(L):
     assert L.dg_quantize_e4m3(FAKE, 10, FAKE, FAKE + 1, None) == dg.DG_ERR_MISALIGNED
 
 
-def test_plan_paths_and_tiles(L):
+def test_plan_decode_shapes_default_to_warp_mma(L):
+    """1 <= M <= 16: the warp-MMA GEMV (path 5) except where it measured
+    slower -- E4M3 with 9-16 rows of A against a large N * K (split-K), and
+    M = 1 E4M3 beyond one wave of 4-warp CTAs (CUDA-core GEMV)."""
     sm = 152
+    for m, n, k, fp16, path, warps in (
+            (1, 12288, 4096, False, 5, 4),     # 768 CTAs: one wave of 4-warp CTAs
+            (8, 12288, 4096, False, 5, 4),
+            (2, 28672, 4096, False, 5, 2),     # 1792 CTAs: several waves
+            (1, 28672, 4096, False, 2, None),  # M = 1 E4M3 there: the CUDA-core GEMV
+            (4, 4096, 4096, False, 5, 8),      # 256 CTAs: at most two per SM
+            (16, 1000, 1040, False, 5, 8),     # small N * K
+            (9, 12288, 4096, False, 4, None),  # 9-16 rows, large N * K: split-K
+            (16, 12288, 4096, False, 4, None),
+            (16, 12288, 4096, True, 5, 2),     # FP16 operands
+            (1, 12288, 4096, True, 5, 4)):
+        p = dg.dg_gemm_plan(m, n, k, dg.DG_FP16 if fp16 else dg.DG_E4M3,
+                            dg.DG_FP16 if fp16 else dg.DG_BF16, sm_count=sm)
+        assert p["path"] == path, (m, n, k, fp16, p)
+        if path == 5:
+            assert p["block_n"] == 16 and p["grid"] == (n + 15) // 16 and p["tiles"] == p["grid"]
+            assert p["block_m"] == (8 if m <= 8 else 16) and p["stages"] == warps, p
+    with knobs(DG_MMA_GEMV="1"):
+        assert dg.dg_gemm_plan(16, 12288, 4096, sm_count=sm)["path"] == 5
+        assert dg.dg_gemm_plan(17, 12288, 4096, sm_count=sm)["path"] != 5
+    with knobs(DG_MMA_GEMV_WARPS="3"):
+        assert dg.dg_gemm_plan(4, 12288, 4096, sm_count=sm)["stages"] == 3
+    # a K longer than the path's 32-bit byte offsets: not path 5
+    assert dg.dg_gemm_plan(4, 64, (1 << 31) - 16, sm_count=sm)["path"] != 5
+
+
+def test_plan_paths_and_tiles(L):
+    """The CUDA-core GEMV, split-K and tiled choices, with the warp-MMA GEMV
+    turned off (the kernels stay selectable and are tested on their own)."""
+    with knobs(DG_MMA_GEMV="0"):
+        _plan_paths_and_tiles(152)
+
+
+def _plan_paths_and_tiles(sm):
     assert dg.dg_gemm_plan(0, 10, 16, sm_count=sm)["path"] == 0
     assert dg.dg_gemm_plan(10, 0, 16, sm_count=sm)["path"] == 0
     assert dg.dg_gemm_plan(10, 10, 0, sm_count=sm)["path"] == 1

@@ -48,8 +48,8 @@ F16_NEG = 0x8000
 
 # (M, N, tuning variables, expected path, expected block_m)
 KERNELS = {
-    "gemv": (1, 1000, {}, 2, None),
-    "splitk16": (8, 1000, {}, 4, 16),
+    "gemv": (1, 1000, {"DG_MMA_GEMV": "0"}, 2, None),
+    "splitk16": (8, 1000, {"DG_MMA_GEMV": "0"}, 4, 16),
     "splitk64": (64, 1000, {"DG_SPLITK": "1"}, 4, 64),
     "single_cta": (129, 1000, {"DG_2CTA": "0"}, 3, 128),
     "cta_pair": (512, 1000, {"DG_2CTA": "1"}, 3, 256),

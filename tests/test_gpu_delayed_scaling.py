@@ -2,9 +2,9 @@
 that value, over 448, serves as the next call's E4M3 output scale (delayed
 scaling; [FP8-guide] = "DeepGEMM实战：FP8矩阵乘法与JIT编译优化指南" §3.2).
 
-Checked against the oracle's max |Dref| on every kernel path: GEMV (M <= 2 by
-default, M = 7 with the crossover raised), single CTA, CTA pairs, and FP8 /
-BF16 outputs.
+Checked against the oracle's max |Dref| on every kernel path: warp-MMA GEMV
+(M <= 8 by default), CUDA-core GEMV and split-K (with the warp-MMA path
+off), single CTA, CTA pairs, and FP8 / BF16 outputs.
 """
 import os
 
@@ -39,7 +39,9 @@ def _amax_bound(R, S, sa, sb):
 
 
 @pytest.mark.parametrize("M,N,K,pairs,path", [
-    (1, 1000, 1040, "0", 2),      # GEMV
+    (1, 1000, 1040, "0", 5),      # warp-MMA GEMV
+    (13, 300, 1040, "0", 5),      # warp-MMA GEMV, two MMAs per step
+    (1, 1000, 1040, "0", 2),      # CUDA-core GEMV
     (7, 300, 512, "0", 2),        # GEMV, several rows (crossover raised to 16)
     (7, 300, 512, "0", 4),        # the same shape on the split-K kernel
     (16, 1000, 1040, "0", 4),     # split-K, every tile split across CTAs
@@ -51,6 +53,8 @@ def _amax_bound(R, S, sa, sb):
 ])
 def test_output_amax_matches_oracle(M, N, K, pairs, path):
     os.environ["DG_2CTA"] = pairs
+    if path in (2, 4):
+        os.environ["DG_MMA_GEMV"] = "0"
     dg.dg_reload_env()
     if path == 2:
         os.environ["DG_GEMV_MAX_M"] = "16"
@@ -80,6 +84,7 @@ def test_output_amax_matches_oracle(M, N, K, pairs, path):
         os.environ.pop("DG_2CTA", None)
         os.environ.pop("DG_GEMV_MAX_M", None)
         os.environ.pop("DG_SPLITK", None)
+        os.environ.pop("DG_MMA_GEMV", None)
         dg.dg_reload_env()
 
 

@@ -10,6 +10,7 @@ import torch
 import fp16_tensor_core_gb300 as dg
 import oracle
 import synth
+from _knobs import knobs
 from _parity import bf16_bits_to_f64, check_bf16_like, dev, scalar
 
 pytestmark = pytest.mark.gpu
@@ -70,10 +71,18 @@ def test_convert_special_values():
     assert np.array_equal(got[~is_nan(want)], want[~is_nan(want)])
 
 
-@pytest.mark.parametrize("M,N,K", [(2, 300, 512), (9, 1000, 1040), (129, 520, 1040), (384, 1000, 2048)])
-def test_range_scaled_hgemm_chain(M, N, K):
+@pytest.mark.parametrize("M,N,K,mma", [(2, 300, 512, "0"), (9, 1000, 1040, "0"), (2, 300, 512, None),
+                                       (9, 1000, 1040, None), (129, 520, 1040, None),
+                                       (384, 1000, 2048, None)])
+def test_range_scaled_hgemm_chain(M, N, K, mma):
     """Operands with FP16-overflowing outliers: the whole chain on the GPU
-    against the oracle's chain (GEMV, split-K, single-CTA and pair paths)."""
+    against the oracle's chain (CUDA-core GEMV and split-K with the warp-MMA
+    path off, warp-MMA GEMV, single-CTA and pair paths)."""
+    with knobs(DG_MMA_GEMV=mma):
+        _range_chain(M, N, K)
+
+
+def _range_chain(M, N, K):
     A, B = synth.make_inputs("fp8_256", M=M, N=N, K=K)
     A = A.copy()
     A[0, 3] = 9.0e4

@@ -29,7 +29,8 @@ def chain(A, B, bufs, out):
 
 
 @pytest.mark.parametrize("M,N,K,out", [
-    (1, 1000, 1040, dg.DG_BF16),      # GEMV
+    (1, 1000, 1040, dg.DG_BF16),      # warp-MMA GEMV
+    (16, 12288, 512, dg.DG_BF16),     # split-K
     (129, 1000, 1040, dg.DG_BF16),    # single CTA
     (640, 1536, 2048, dg.DG_E4M3),    # CTA pairs, E4M3 out
 ])

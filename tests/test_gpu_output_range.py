@@ -27,8 +27,8 @@ pytestmark = pytest.mark.gpu
 
 # (M, N, K, tuning variables, expected plan path, expected block_m)
 PATHS = {
-    "gemv": (1, 1000, 1040, {}, 2, None),
-    "splitk": (8, 1000, 1040, {}, 4, 16),
+    "gemv": (1, 1000, 1040, {"DG_MMA_GEMV": "0"}, 2, None),
+    "splitk": (8, 1000, 1040, {"DG_MMA_GEMV": "0"}, 4, 16),
     "single_cta": (129, 1000, 1040, {"DG_2CTA": "0"}, 3, 128),
     "cta_pair": (512, 1000, 1040, {"DG_2CTA": "1"}, 3, 256),
     "gemv_mma": (16, 1000, 1040, {"DG_MMA_GEMV": "1"}, 5, None),

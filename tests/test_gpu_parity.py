@@ -17,6 +17,7 @@ import torch
 import fp16_tensor_core_gb300 as dg
 import oracle
 import synth
+from _knobs import knobs
 from _parity import (check_bf16_like, check_e4m3, check_guards, check_quantised, dev,
                      fp16_bits_to_f64, bf16_bits_to_f64, gpu_quantize, guarded,
                      sample_positions, scalar)
@@ -144,8 +145,8 @@ def test_fp16_shapes_full(M, N, K):
     (128, 256, 128),     # exactly one tile, one K block
     (200, 24, 16),       # K smaller than one stage, N < one tile
     (300, 777, 272),     # ragged everywhere, N*2 not a multiple of 16 (scalar stores)
-    (2, 1000, 1040),     # GEMV, several rows
-    (16, 513, 4096),     # GEMV at its M limit
+    (2, 1000, 1040),     # warp-MMA GEMV, two rows of A
+    (16, 513, 4096),     # warp-MMA GEMV at its M limit
     (17, 64, 64),        # smallest tensor-core M
     (1, 1, 16),          # 1x1 output
     (640, 1536, 2048),   # several waves of tiles over the grid
@@ -322,8 +323,14 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     (1, 30000, 512, 8),      # no width fits one wave: 2 rows x 4 chunks
 ])
 def test_gemv_one_wave_layouts(M, N, K, rows):
-    """M <= 2: the planner's rows per CTA (the fewest whose grid fits one wave)
-    for E4M3 and FP16 operands, every element against the oracle."""
+    """M <= 2 on the CUDA-core GEMV (the warp-MMA path turned off): the
+    planner's rows per CTA (the fewest whose grid fits one wave) for E4M3 and
+    FP16 operands, every element against the oracle."""
+    with knobs(DG_MMA_GEMV="0"):
+        _gemv_layout_case(M, N, K, rows)
+
+
+def _gemv_layout_case(M, N, K, rows):
     p = dg.dg_gemm_plan(M, N, K)
     assert p["path"] == 2 and p["block_n"] == rows, p
     A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
@@ -339,6 +346,7 @@ def test_gemv_for_larger_m_when_forced(M, N, K):
     """The GEMV handles M up to 16 (its 2-, 4-, 8- and 16-row instantiations),
     although the planner only sends M <= 2 to it by default."""
     os.environ["DG_GEMV_MAX_M"] = "16"
+    os.environ["DG_MMA_GEMV"] = "0"
     dg.dg_reload_env()
     try:
         assert dg.dg_gemm_plan(M, N, K)["path"] == 2
@@ -348,4 +356,5 @@ def test_gemv_for_larger_m_when_forced(M, N, K):
         hgemm_case(A16, B16)
     finally:
         del os.environ["DG_GEMV_MAX_M"]
+        del os.environ["DG_MMA_GEMV"]
         dg.dg_reload_env()

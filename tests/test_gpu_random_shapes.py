@@ -1,5 +1,5 @@
-"""Seeded random shapes over every GEMM path (GEMV layouts, split-K, single
-CTA, CTA pairs), E4M3 and FP16 inputs and each output type, every element checked
+"""Seeded random shapes over every GEMM path the planner picks (warp-MMA GEMV,
+CUDA-core GEMV layouts, split-K, single CTA, CTA pairs), E4M3 and FP16 inputs and each output type, every element checked
 against the oracle and every byte around D checked untouched.  K is a
 multiple of 16 (E4M3) or 8 (FP16), the only shape rule of the library."""
 import numpy as np
@@ -39,8 +39,9 @@ def _shapes(seed, count):
 
 def _shapes_wide(seed, count):
     """Decode-style shapes: M <= 128 against wide B (N up to 13000), where
-    the planner chooses between the GEMV layouts, split-K (with its
-    tile-aligned grid, staged fix-up and helper warps) and the tiled kernel."""
+    the planner chooses between the warp-MMA GEMV, the CUDA-core GEMV,
+    split-K (with its tile-aligned grid, staged fix-up and helper warps) and
+    the tiled kernel."""
     rng = np.random.default_rng(seed)
     out = []
     for i in range(count):
