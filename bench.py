@@ -507,18 +507,22 @@ def compact(rec: dict) -> dict:
     return {k: round(rec[k], d) for k, d in keep.items() if k in rec}
 
 
-# Kernels behind the bandwidth-bound decode shapes (the M <= 16 half of the metric).
-SKINNY_ROOFLINES = {
-    "m1": ("qkv_gemv_1x12288x4096", "gemv_kernel (CUDA cores, M = 1)"),
-    "m16": ("qkv_m16_16x12288x4096", "gemm_skinny_kernel (split-K tcgen05, M = 16)"),
-}
+# The bandwidth-bound decode shapes (the M <= 16 half of the metric): the
+# QKV projection weights B[12288, 4096] with M = 1, 8 and 16 rows of A.
+SKINNY_ROOFLINES = {"m1": "qkv_gemv_1x12288x4096", "m8": "qkv_m8_8x12288x4096",
+                    "m16": "qkv_m16_16x12288x4096"}
+KERNEL_OF_PATH = {2: "gemv_kernel (CUDA-core GEMV)", 3: "gemm_tc_kernel (tiled tcgen05)",
+                  4: "gemm_skinny_kernel (split-K tcgen05)",
+                  5: "gemv_mma_kernel (warp-MMA GEMV, B streamed into registers)"}
 
 
-def skinny_roofline(ex: dict, key: str, peaks: dict) -> dict:
+def skinny_roofline(dg, ex: dict, key: str, peaks: dict) -> dict:
     """roofline-shaped entry for one decode shape, from its `extra` record."""
-    name, kernel = SKINNY_ROOFLINES[key]
+    name = SKINNY_ROOFLINES[key]
     rec = ex[name]
     m = int(name.split("_")[-1].split("x")[0])
+    plan = dg.dg_gemm_plan(m, 12288, 4096, dg.DG_E4M3, dg.DG_BF16)
+    kernel = f"{KERNEL_OF_PATH.get(plan['path'], plan['path'])}, grid {plan['grid']}"
     algo = 12288 * 4096 + m * 4096 + m * 12288 * 2
     return {"bound": "hbm", "kernel": kernel, "workload": name.replace("_", " "),
             "achieved": round(rec["GB/s"], 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -748,7 +752,7 @@ def run_own(args):
     skinny = {}
     if rank == 0 and not args.no_extra:
         ex = extras(torch, dg, stream, peaks)
-        skinny = {k: skinny_roofline(ex, k, peaks) for k in SKINNY_ROOFLINES}
+        skinny = {k: skinny_roofline(dg, ex, k, peaks) for k in SKINNY_ROOFLINES}
         line["roofline"].update(skinny)
         line["extra"] = {k: compact(v) for k, v in ex.items()}
     if rank == 0 and not args.no_cpu_baseline:
