@@ -406,6 +406,29 @@ def kernel_cases(torch, dg):
             dg.dg_hgemm_scaled(A16, B16, D, f[2:3], f[3:4], dg.DG_BF16, stream=s)
         return fn, 2.0 * S ** 3, 0.0, "tensor_fp16", "FP32 operands 2 x 67 MB (> L2 together with the FP16 copies)"
 
+    def fp16_range_recorded_chain(S):
+        # the same chain with delayed scaling: each step converts with the
+        # factors of the previous step's maxima, recorded by the conversions
+        # (one read of each FP32 operand instead of two), then forms the next
+        # factors
+        g = torch.Generator(device=dev)
+        g.manual_seed(9)
+        A = torch.randn((S, S), device=dev, generator=g)
+        B = torch.randn((S, S), device=dev, generator=g)
+        A[0, 0] = 9.0e4
+        am_a, am_b = (torch.zeros(4, dtype=torch.float32, device=dev) for _ in range(2))
+        f = torch.ones(4, dtype=torch.float32, device=dev)
+        A16 = torch.empty((S, S), dtype=torch.int16, device=dev)
+        B16 = torch.empty((S, S), dtype=torch.int16, device=dev)
+        D = torch.empty((S, S), dtype=torch.bfloat16, device=dev)
+
+        def fn(i, s):
+            dg.dg_convert_f16_amax(A, A16, f[1:2], am_a, stream=s)
+            dg.dg_convert_f16_amax(B, B16, f[1:2], am_b, stream=s)
+            dg.dg_hgemm_scaled(A16, B16, D, f[2:3], f[3:4], dg.DG_BF16, stream=s)
+            dg.dg_fp16_range_scale(am_a, am_b, f, stream=s)
+        return fn, 2.0 * S ** 3, 0.0, "tensor_fp16", "FP32 operands 2 x 67 MB (> L2 together with the FP16 copies)"
+
     def moe(grouped: bool):
         # 16 experts, 8192 routed rows with a skewed load, N = 2048, K = 4096
         import synth
@@ -463,6 +486,7 @@ def kernel_cases(torch, dg):
         "quantise_with_amax_8192sq": quant_amax,
         "convert_f16_8192sq": convert16,
         "fp16_range_scaled_hgemm_chain_4096": lambda: fp16_range_chain(4096),
+        "fp16_range_recorded_chain_4096": lambda: fp16_range_recorded_chain(4096),
     }
 
 

@@ -23,7 +23,7 @@ __all__ = [
     "dg_hgemm", "dg_hgemm_scaled", "dg_fp16_range_scale", "dg_convert_f16",
     "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
     "dg_debug_skip_first_load", "dg_status_string", "dg_version", "dg_release_stream",
-    "dg_reload_env", "EXPORTED_SYMBOLS",
+    "dg_reload_env", "dg_convert_f16_amax", "EXPORTED_SYMBOLS",
 ]
 
 DG_OK, DG_ERR_INVALID_VALUE, DG_ERR_MISALIGNED, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_TIMEOUT = range(6)
@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_hgemm", "dg_hgemm_scaled",
     "dg_fp16_range_scale", "dg_convert_f16", "dg_gemm_plan",
     "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
-    "dg_status_string", "dg_version", "dg_release_stream", "dg_reload_env",
+    "dg_status_string", "dg_version", "dg_release_stream", "dg_reload_env", "dg_convert_f16_amax",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -86,6 +86,7 @@ def lib():
             L.dg_hgemm_scaled.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, ctypes.c_int, vp]
             L.dg_fp16_range_scale.argtypes = [vp, vp, vp, vp]
             L.dg_convert_f16.argtypes = [vp, i64, vp, vp, vp]
+            L.dg_convert_f16_amax.argtypes = [vp, i64, vp, vp, vp, vp]
             L.dg_gemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(_Plan)]
             L.dg_init.argtypes = []
@@ -103,7 +104,8 @@ def lib():
             for name in ("dg_amax", "dg_amax_pow2", "dg_quantize_e4m3", "dg_fp8_gemm", "dg_fp8_gemm_amax", "dg_hgemm",
                          "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_gemm_plan", "dg_init",
                          "dg_sync_status", "dg_version", "dg_hgemm_scaled", "dg_fp16_range_scale",
-                         "dg_convert_f16", "dg_quantize_e4m3_amax", "dg_release_stream"):
+                         "dg_convert_f16", "dg_quantize_e4m3_amax", "dg_release_stream",
+                         "dg_convert_f16_amax"):
                 getattr(L, name).restype = st
             _lib = L
     return _lib
@@ -252,6 +254,13 @@ def dg_convert_f16(x, out, factor=None, stream=None) -> None:
     """out = fp16_rn(x * factor[0]) elementwise (binary16 bit patterns)."""
     _check(lib().dg_convert_f16(_ptr(x), x.numel(), _ptr(factor), _ptr(out), _stream(stream)),
            "dg_convert_f16")
+
+
+def dg_convert_f16_amax(x, out, factor, amax_out, stream=None) -> None:
+    """out = fp16_rn(x * factor[0]) and amax_out[0] = max |x| in one pass
+    (the next call's factors come from dg_fp16_range_scale on such maxima)."""
+    _check(lib().dg_convert_f16_amax(_ptr(x), x.numel(), _ptr(factor), _ptr(out), _ptr(amax_out),
+                                     _stream(stream)), "dg_convert_f16_amax")
 
 
 def dg_gemm_plan(M, N, K, in_dtype=DG_E4M3, out_dtype=DG_BF16, sm_count=0) -> dict:

@@ -671,6 +671,20 @@ dg_status dg_convert_f16(const float* x, int64_t n, const float* factor, uint16_
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dg_status dg_convert_f16_amax(const float* x, int64_t n, const float* factor, uint16_t* out,
+                              float* amax_out, dg_stream_t stream) {
+    if (n < 0 || amax_out == nullptr || (n > 0 && (x == nullptr || out == nullptr)))
+        return DG_ERR_INVALID_VALUE;
+    if (!aligned16(x) || !aligned16(out) || !aligned4(factor) || !aligned4(amax_out))
+        return DG_ERR_MISALIGNED;
+    if (amax_out == factor) return DG_ERR_INVALID_VALUE;   // zeroed before the factor is read
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_convert_f16_amax(x, n, factor, out, amax_out, st->sm_count,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dg_status dg_gemm_plan(int64_t M, int64_t N, int64_t K, dg_dtype in, dg_dtype out,
                        int sm_count, dg_plan* plan) {
     if (plan == nullptr) return DG_ERR_INVALID_VALUE;

@@ -111,6 +111,10 @@ cudaError_t launch_fp16_range_scale(const float* amax_a, const float* amax_b, fl
                                     cudaStream_t s);
 cudaError_t launch_convert_f16(const float* x, int64_t n, const float* factor, uint16_t* out,
                                int sm_count, cudaStream_t s);
+// The conversion with a given factor that also records max |x| in the same
+// pass (zeroing kernel first).
+cudaError_t launch_convert_f16_amax(const float* x, int64_t n, const float* factor, uint16_t* out,
+                                    float* amax_out, int sm_count, cudaStream_t s);
 // Sets *bits = 0 on stream s (one-thread kernel).
 cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s);
 

@@ -198,10 +198,12 @@ __device__ __forceinline__ uint2 half4(float4 v, float f) {
 
 // out_i = fp16_rn(fl32(x_i * factor)): each warp converts 512-element slabs
 // (four 512-byte loads, four 256-byte stores per slab); the ragged tail is
-// converted by block 0.
+// converted by block 0.  kAmax: also the running max |x| (ordered bits) into
+// *amax_bits, for the factors of the next call (delayed scaling).
+template <bool kAmax>
 __global__ void __launch_bounds__(kQuantThreads)
 convert_f16_kernel(const float* __restrict__ x, int64_t n, const float* __restrict__ factor_p,
-                   uint16_t* __restrict__ out) {
+                   uint16_t* __restrict__ out, uint32_t* __restrict__ amax_bits) {
     pdl_wait();
     const float f = factor_p != nullptr ? *factor_p : 1.0f;
     const int lane = threadIdx.x & 31;
@@ -210,6 +212,7 @@ convert_f16_kernel(const float* __restrict__ x, int64_t n, const float* __restri
     const int64_t nslab = n >> 9;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     uint2* o4 = reinterpret_cast<uint2*>(out);
+    uint32_t m = 0u;
     for (int64_t slab = warp; slab < nslab; slab += nwarps) {
         const int64_t b = slab * 128 + lane;
         const float4 v0 = ld_stream_f4(x4 + b);
@@ -220,10 +223,27 @@ convert_f16_kernel(const float* __restrict__ x, int64_t n, const float* __restri
         o4[b + 32] = half4(v1, f);
         o4[b + 64] = half4(v2, f);
         o4[b + 96] = half4(v3, f);
+        if constexpr (kAmax)
+            m = max(m, max(max(abs_bits4(v0), abs_bits4(v1)), max(abs_bits4(v2), abs_bits4(v3))));
     }
     if (blockIdx.x == 0) {
-        for (int64_t i = (nslab << 9) + threadIdx.x; i < n; i += blockDim.x)
-            out[i] = static_cast<uint16_t>(f32x2_to_f16x2(__fmul_rn(x[i], f), 0.0f) & 0xFFFFu);
+        for (int64_t i = (nslab << 9) + threadIdx.x; i < n; i += blockDim.x) {
+            const float v = x[i];
+            out[i] = static_cast<uint16_t>(f32x2_to_f16x2(__fmul_rn(v, f), 0.0f) & 0xFFFFu);
+            if constexpr (kAmax) m = max(m, abs_bits(v));
+        }
+    }
+    if constexpr (kAmax) {
+        __shared__ uint32_t partial[kQuantThreads / 32];
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        const int w = threadIdx.x >> 5;
+        if (lane == 0) partial[w] = m;
+        __syncthreads();
+        if (w == 0) {
+            m = lane < kQuantThreads / 32 ? partial[lane] : 0u;
+            m = __reduce_max_sync(0xFFFFFFFFu, m);
+            if (lane == 0 && m != 0u) atomicMax(amax_bits, m);
+        }
     }
 }
 
@@ -249,8 +269,18 @@ cudaError_t launch_convert_f16(const float* x, int64_t n, const float* factor, u
                                int sm_count, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
     const int64_t blocks = slab_grid(n, sm_count);
-    return launch_kernel(convert_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kQuantThreads),
-                         0, s, x, n, factor, out);
+    return launch_kernel(convert_f16_kernel<false>, dim3(static_cast<unsigned>(blocks)),
+                         dim3(kQuantThreads), 0, s, x, n, factor, out, static_cast<uint32_t*>(nullptr));
+}
+
+cudaError_t launch_convert_f16_amax(const float* x, int64_t n, const float* factor, uint16_t* out,
+                                    float* amax_out, int sm_count, cudaStream_t s) {
+    uint32_t* bits = reinterpret_cast<uint32_t*>(amax_out);
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
+    if (e != cudaSuccess || n <= 0) return e;
+    const int64_t blocks = slab_grid(n, sm_count);
+    return launch_kernel(convert_f16_kernel<true>, dim3(static_cast<unsigned>(blocks)),
+                         dim3(kQuantThreads), 0, s, x, n, factor, out, bits);
 }
 
 cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale_out,

@@ -266,6 +266,21 @@ dg_status dg_fp16_range_scale(const float* amax_a, const float* amax_b,
 dg_status dg_convert_f16(const float* x, int64_t n, const float* factor,
                          uint16_t* out, dg_stream_t stream);
 
+/* dg_convert_f16 with a factor recorded earlier (delayed scaling), fused
+ * with the amax of this tensor for the next call: one pass over x writes
+ * out[i] = fp16_rn(fl32(x[i] * factor[0])) and amax_out[0] = max |x|
+ * (NaN propagates; 0 for n == 0).  [DG-FP16] §3.3 forms the scale from the
+ * two operands' maxima; recording them while converting (as [FP8-guide]
+ * §3.2's calibration records each tensor's maximum) lets the factors of the
+ * next call come from dg_fp16_range_scale on these maxima, so each operand
+ * is read once per call instead of twice.  amax_out: FP32 device word,
+ * 4-byte aligned, zeroed by the call (a one-thread kernel) before the pass;
+ * it must not be the factor word.  Other arguments and errors as
+ * dg_convert_f16; factor NULL = 1. */
+dg_status dg_convert_f16_amax(const float* x, int64_t n, const float* factor,
+                              uint16_t* out, float* amax_out,
+                              dg_stream_t stream);
+
 /* Tile / path selection for a GEMM shape, host only (launches nothing).
  * [FP8-guide] §2.2, §3.1, §3.3 (per-shape tile choice, smaller tiles where
  * edge waste is high) and [HGEMM-L2] §3.1-§3.3 (tile and stage count chosen

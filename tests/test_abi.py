@@ -181,6 +181,18 @@ def test_fp16_range_argument_errors(L):
                              None) == dg.DG_ERR_MISALIGNED
 
 
+def test_convert_f16_amax_argument_errors(L):
+    c = L.dg_convert_f16_amax
+    assert c(FAKE, -1, None, FAKE, FAKE + 64, None) == dg.DG_ERR_INVALID_VALUE
+    assert c(FAKE, 8, None, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE        # no amax word
+    assert c(None, 8, None, FAKE, FAKE, None) == dg.DG_ERR_INVALID_VALUE
+    assert c(FAKE, 8, FAKE + 64, FAKE, FAKE + 64, None) == dg.DG_ERR_INVALID_VALUE   # amax is factor
+    assert c(FAKE + 4, 8, None, FAKE, FAKE, None) == dg.DG_ERR_MISALIGNED
+    assert c(FAKE, 8, None, FAKE + 8, FAKE, None) == dg.DG_ERR_MISALIGNED
+    assert c(FAKE, 8, FAKE + 1, FAKE, FAKE + 64, None) == dg.DG_ERR_MISALIGNED
+    assert c(FAKE, 8, None, FAKE, FAKE + 2, None) == dg.DG_ERR_MISALIGNED
+
+
 def test_quantize_amax_argument_errors(L):
     q = L.dg_quantize_e4m3_amax
     assert q(FAKE, 10, None, FAKE, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE    # no scale

@@ -107,3 +107,73 @@ def _range_chain(M, N, K):
     check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16)), R, S,
                     float(fr[2]), 1.0, "range-scaled HGEMM")
     assert np.all(np.isfinite(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16))))
+
+
+@pytest.mark.parametrize("n", [0, 1, 511, 512, 4097, (1 << 20) + 7])
+def test_convert_with_amax_is_bit_exact(n):
+    """The fused pass: codes identical to dg_convert_f16 (and the oracle) and
+    the maximum identical to dg_amax (and the oracle), ragged tails included."""
+    x = synth.normal_f32(60 + n % 89, (n,)) * np.float32(700.0)
+    if n > 10:
+        x[7] = -9.5e4             # overflows FP16 at factor 1
+    f = scalar()
+    f[0] = 0.37
+    out = torch.empty(max(n, 1), dtype=torch.int16, device="cuda")[:n]
+    am = scalar()
+    am[0] = 5.0e6                 # stale: the call zeroes it first
+    dg.dg_convert_f16_amax(dev(x), out, f[0:1], am)
+    assert dg.dg_sync_status() == dg.DG_OK
+    want = oracle.convert_f16(x, np.float32(0.37))
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), want)
+    assert np.float32(am[0].item()).view(np.uint32) == np.float32(oracle.amax(x)).view(np.uint32)
+
+
+def test_convert_with_amax_propagates_nan():
+    x = synth.normal_f32(3, (5000,))
+    x[4321] = np.nan
+    out = torch.empty(5000, dtype=torch.int16, device="cuda")
+    am = scalar()
+    dg.dg_convert_f16_amax(dev(x), out, None, am)
+    assert dg.dg_sync_status() == dg.DG_OK
+    assert np.isnan(am[0].item())
+
+
+@pytest.mark.parametrize("M,N,K,mma", [(2, 300, 512, None), (9, 1000, 1040, "0"), (129, 520, 1040, None),
+                                       (384, 1000, 2048, None)])
+def test_recorded_factor_chain(M, N, K, mma):
+    """Delayed dynamic-range scaling: each step converts with the factors
+    formed from the previous step's maxima, recorded by the conversions
+    themselves.  From the second step on (same operands) every factor, FP16
+    operand and output matches the oracle's chain of [DG-FP16] §3.3, and the
+    factors the step leaves for the next one are the ones it used."""
+    A, B = synth.make_inputs("fp8_256", M=M, N=N, K=K)
+    A = A.copy()
+    A[0, 3] = 9.0e4
+    A[M - 1, K - 1] = -7.0e4
+    dA, dB = dev(A), dev(B)
+    am_a, am_b = scalar(), scalar()
+    f = torch.tensor([1.0, 1.0, 1.0, 1.0], dtype=torch.float32, device="cuda")   # no record yet
+    A16 = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    B16 = torch.empty((N, K), dtype=torch.int16, device="cuda")
+    D = torch.empty((M, N), dtype=torch.int16, device="cuda")
+
+    def step():
+        dg.dg_convert_f16_amax(dA, A16, f[1:2], am_a)
+        dg.dg_convert_f16_amax(dB, B16, f[1:2], am_b)
+        dg.dg_hgemm_scaled(A16, B16, D, f[2:3], f[3:4], dg.DG_BF16)
+        used = f.clone()
+        dg.dg_fp16_range_scale(am_a, am_b, f)      # factors for the next step
+        return used
+
+    with knobs(DG_MMA_GEMV=mma):
+        step()
+        used = step()
+        assert dg.dg_sync_status() == dg.DG_OK
+    fr, A16r, B16r, Dr, S = oracle.fp16_range_chain(A, B)
+    assert np.array_equal(used.cpu().numpy().view(np.uint32), fr.view(np.uint32))
+    assert np.array_equal(f.cpu().numpy().view(np.uint32), fr.view(np.uint32))
+    assert np.array_equal(A16.cpu().numpy().view(np.uint16), A16r)
+    assert np.array_equal(B16.cpu().numpy().view(np.uint16), B16r)
+    R, _ = oracle.hgemm(A16r, B16r)
+    check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16)), R, S,
+                    float(fr[2]), 1.0, "recorded-factor HGEMM")
