@@ -127,6 +127,68 @@ __device__ __forceinline__ uint32_t store_chunk(const Params& p, int row, int ro
     return amax_bits;
 }
 
+// Staged epilogue: each epilogue warp converts 32 rows x 32 columns of the
+// accumulator into a box in shared memory laid out as the output tensor map
+// expects (64-byte swizzle for 2-byte outputs, 32-byte for E4M3) and writes
+// it with one bulk tensor store, which moves whole lines and clips rows >= M
+// and columns >= N.
+constexpr int kBoxBytes = 2048;   // 32 x 32 two-byte elements (E4M3 uses half)
+
+// Thread `lane` converts accumulator row `row`, columns col0 .. col0 + 31,
+// into its line of `box`.  Returns max |acc| over the columns < N of a row
+// < row_end (ordered bits) when p.amax_out is set, else 0.
+__device__ __forceinline__ uint32_t stage_box(const Params& p, uint8_t* box, int row, int row_end,
+                                              int col0, const uint32_t (&r)[32], float alpha,
+                                              int lane) {
+    uint32_t amax_bits = 0u;
+    if (p.amax_out != nullptr && row < row_end) {
+        const int ncols = min(32, p.N - col0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < ncols) amax_bits = max(amax_bits, r[i] & 0x7FFFFFFFu);
+    }
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
+    if (p.out_kind == kOutE4M3) {
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            w[j] = static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j], v[4 * j + 1])) |
+                   (static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j + 2], v[4 * j + 3])) << 16);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int ph = k ^ ((lane >> 2) & 1);   // 32-byte swizzle: 16-byte halves
+            st_shared_v4(smem_addr(box + lane * 32 + ph * 16), w[4 * k], w[4 * k + 1], w[4 * k + 2],
+                         w[4 * k + 3]);
+        }
+    } else {
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            w[j] = p.out_kind == kOutFP16 ? f32x2_to_f16x2(v[2 * j], v[2 * j + 1])
+                                          : f32x2_to_bf16x2(v[2 * j], v[2 * j + 1]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int ph = k ^ ((lane >> 1) & 3);   // 64-byte swizzle: 16-byte quarters
+            st_shared_v4(smem_addr(box + lane * 64 + ph * 16), w[4 * k], w[4 * k + 1], w[4 * k + 2],
+                         w[4 * k + 3]);
+        }
+    }
+    return amax_bits;
+}
+
+// Waits until every bulk store this thread committed has finished reading
+// shared memory (the staging box may then be rewritten).
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// The output tensor map of the staged epilogue: D (M x N of the output
+// type), 32 x 32 boxes, swizzled to the width of one box line.  False if the
+// rows of D are not 16-byte multiples (then the epilogue stores directly).
+inline bool make_out_map(CUtensorMap* map, const TcLaunch& L);
+
 // Publishes one warp's running max |acc| (ordered bits) as
 // max |acc| * (sa * sb) into p.amax_out.  Rounding is monotone, so
 // fl(max|acc| * c) = max fl(|acc| * c) exactly.  Whole warp, converged.
@@ -170,6 +232,23 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int k, bool fp16, in
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+inline bool make_out_map(CUtensorMap* map, const TcLaunch& L) {
+    if ((static_cast<int64_t>(L.N) * L.out_elem) % 16 != 0) return false;
+    auto encode = get_encode_fn();
+    if (!encode) return false;
+    const bool e4 = L.out_kind == kOutE4M3;
+    const CUtensorMapDataType dt = e4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : (L.out_kind == kOutFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.N), static_cast<cuuint64_t>(L.M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.N) * L.out_elem};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return encode(map, dt, 2, L.D, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  e4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace

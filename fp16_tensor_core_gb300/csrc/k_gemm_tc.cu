@@ -24,7 +24,10 @@
 //    and epilogue stores are predicated on m < M, n < N.
 // The kernel is persistent (one CTA per SM, tiles strided by the grid) and
 // double-buffers the accumulator in tensor memory so that the epilogue of
-// one tile overlaps the main loop of the next.  Every mbarrier wait is
+// one tile overlaps the main loop of the next; the epilogue writes each
+// warp's 32 x 32 output boxes through a staging box in shared memory with
+// bulk tensor stores (whole lines; direct stores only for a grouped tile's
+// rows that cross its group's end).  Every mbarrier wait is
 // bounded: on a timeout the CTA raises its abort flag, records
 // kStatusTimeout, lets in-flight copies and MMAs land, frees its tensor
 // memory and returns.
@@ -46,9 +49,14 @@ constexpr int kBM = 128;
 // Shared memory for the grouped variant's per-group tile prefix.
 constexpr int kGroupSmem = 4 * (kMaxGroups + 1) + 12;
 
-// Stage count = what fits in 227 KB, at most 8.
+// Staging boxes of the epilogue: one 32 x 32 box per epilogue warp.
+constexpr int kStagingBytes = 4 * kBoxBytes;
+
+// Stage count = what fits in 227 KB beside the barrier block (1 KB, keeping
+// the staging boxes 1024-byte aligned), the staging boxes and the grouped
+// variant's tile prefix, at most 8.
 constexpr int stages_for(int bn, bool grouped = false) {
-    const int st = (kSmemLimit - 1024 - 256 - (grouped ? kGroupSmem : 0)) /
+    const int st = (kSmemLimit - 1024 - 1024 - kStagingBytes - (grouped ? kGroupSmem : 0)) /
                    (kBM * kBKBytes + bn * kBKBytes);
     return st > 8 ? 8 : st;
 }
@@ -61,8 +69,9 @@ struct Cfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // two accumulators
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes =
-        1024 + STAGES * kStageBytes + kBarBytes + (kGrouped ? kGroupSmem : 0);
+    static constexpr int kStagingOff = STAGES * kStageBytes + 1024;   // after the barriers
+    static constexpr int kGroupOff = kStagingOff + kStagingBytes;     // grouped: tile prefix
+    static constexpr int kSmemBytes = 1024 + kGroupOff + (kGrouped ? kGroupSmem : 0);
     static constexpr uint32_t kIdesc = idesc_f32acc(kBM, BN, 0, 0);
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256,
                   "BN: MMA N (multiple of 16, <= 256) and 32-column epilogue chunks");
@@ -80,7 +89,8 @@ struct Tile {
 template <int BN, int STAGES, bool kFp16In, bool kGrouped = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
-               const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+               const __grid_constant__ CUtensorMap tmap_b,
+               const __grid_constant__ CUtensorMap tmap_d, const Params p) {
     using C = Cfg<BN, STAGES, kFp16In, kGrouped>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -95,7 +105,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     // grouped only: tile_start[g] = first tile of group g (G + 1 entries)
-    int* tile_start = reinterpret_cast<int*>(smem + STAGES * C::kStageBytes + C::kBarBytes);
+    int* tile_start = reinterpret_cast<int*>(smem + C::kGroupOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -279,33 +289,59 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         int acc = 0;
         uint32_t acc_phase = 0;
         int gcur = 0;
+        uint8_t* box = smem + C::kStagingOff + q * kBoxBytes;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const Tile T = tile_of(t, gcur);
             if (T.g != alpha_g) {
                 alpha = alpha_of(T.g);
                 alpha_g = T.g;
             }
+            // The next kernel in the stream may be scheduled once every CTA
+            // is on its last tile (it still waits for this grid's memory).
+            if (t + static_cast<int>(gridDim.x) >= num_tiles && warp == 4 && lane == 0)
+                pdl_launch_dependents();
             // Every lane waits; the vote reconverges the warp (tcgen05.ld is
             // .sync.aligned) and makes the whole warp leave together.
             const bool got = wait_bounded(&acc_full[acc], acc_phase, ctl);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
             tc_fence_after_sync();
             const int row = T.a_row + q * 32 + lane;
+            const int row0 = T.a_row + q * 32;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
+            // Staged bulk stores (whole lines, M / N edges clipped by the
+            // tensor map) unless the warp's 32 rows cross a group's end,
+            // which the tensor map cannot clip: those rows store directly.
+            const bool staged = p.vec_ok && (!kGrouped || row0 + 32 <= T.row_end);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 __syncwarp();
                 tmem_load_32cols(tbase + c * 32, r);
-                tmem_load_wait(r);
-                amax_bits = max(amax_bits, store_chunk(p, row, T.row_end, T.col0 + c * 32, r, alpha));
+                if (staged) {
+                    if (lane == 0) bulk_wait_read_all();   // the box is free again
+                    __syncwarp();
+                    tmem_load_wait(r);
+                    const int col0 = T.col0 + c * 32;
+                    amax_bits = max(amax_bits, stage_box(p, box, row, T.row_end, col0, r, alpha, lane));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < T.row_end && col0 < p.N) {
+                        tma_store_2d(&tmap_d, box, col0, row0);
+                        bulk_commit();
+                    }
+                } else {
+                    tmem_load_wait(r);
+                    amax_bits = max(amax_bits, store_chunk(p, row, T.row_end, T.col0 + c * 32, r, alpha));
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        // The staging box must have been written out before the CTA exits.
+        if (lane == 0) bulk_wait_all();
         __syncwarp();
         publish_amax(p, amax_bits);
     }
@@ -336,12 +372,18 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
             attr_done[dev] = true;
         }
     }
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     const int b_rows = kGrouped ? L.N * L.groups : L.N;   // grouped: B is (G*N) x K
     if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kBM) || !make_map(&tb, L.B, b_rows, L.K, kFp16In, BN))
         return cudaErrorInvalidValue;
+    Params prm2 = prm;
+    // Output map of the staged epilogue (else the epilogue stores directly).
+    if (!prm2.vec_ok || !make_out_map(&td, L)) {
+        prm2.vec_ok = 0;
+        td = ta;
+    }
     return launch_kernel(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped>, dim3(L.plan->grid),
-                         dim3(kThreads), C::kSmemBytes, s, ta, tb, prm);
+                         dim3(kThreads), C::kSmemBytes, s, ta, tb, td, prm2);
 }
 
 template <bool kFp16In>

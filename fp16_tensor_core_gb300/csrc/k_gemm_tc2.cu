@@ -24,11 +24,14 @@
 //  * a final multicast commit to `drain` tells both CTAs that no pair MMA
 //    still reads their shared memory or writes their tensor memory; only
 //    then is tensor memory freed (collectively) and the CTAs exit;
-//  * the last tile's epilogue, which nothing overlaps, stages each warp's
-//    32 x 32 output boxes in the idle A stages (TMA's 64- or 32-byte swizzle)
-//    and writes them with bulk tensor stores (whole lines, edges clipped by
-//    the tensor map) instead of one scattered row per lane; earlier tiles'
-//    epilogues overlap the next tile's main loop and store directly.
+//  * the epilogue (which overlaps the next tile's main loop) stages each
+//    warp's 32 x 32 output boxes in a buffer of its own (TMA's 64- or 32-byte
+//    swizzle) and writes them with bulk tensor stores -- whole lines, edges
+//    clipped by the tensor map -- instead of one scattered 16-byte row piece
+//    per lane, whose many partial-line writes slowed the concurrent main
+//    loop by ~1 us per tile at 4096^3;
+//  * once every CTA is on its last tile the grid lets the next kernel in the
+//    stream be scheduled, so that its CTAs start as these exit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -45,8 +48,14 @@ namespace {
 constexpr int kPairBM = 256;   // output rows of a pair tile
 constexpr int kHalfBM = 128;   // rows of it per CTA
 
+// Staging boxes of the epilogue: one 32 x 32 box per epilogue warp.
+constexpr int kStagingBytes = 4 * kBoxBytes;
+
+// Stage count: what fits in 227 KB beside the barrier block (1 KB, keeping
+// the staging boxes 1024-byte aligned) and the staging boxes, at most 8.
 constexpr int pair_stages_for(int bn) {
-    const int st = (kSmemLimit - 1024 - 256) / (kHalfBM * kBKBytes + (bn / 2) * kBKBytes);
+    const int st = (kSmemLimit - 1024 - 1024 - kStagingBytes) /
+                   (kHalfBM * kBKBytes + (bn / 2) * kBKBytes);
     return st > 8 ? 8 : st;
 }
 
@@ -58,7 +67,8 @@ struct PairCfg {
     static constexpr int kBBytes = kBRows * kBKBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);
-    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + 256;
+    static constexpr int kStagingOff = STAGES * kStageBytes + 1024;   // after the barriers
+    static constexpr int kSmemBytes = 1024 + kStagingOff + kStagingBytes;
     static constexpr uint32_t kIdesc = idesc_f32acc(kPairBM, BN, 0, 0);
     static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "BN");
     static_assert(kBBytes % 1024 == 0, "1024-byte aligned B stages (128-byte swizzle atoms)");
@@ -218,6 +228,10 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         for (int t = pair; t < num_tiles; t += npairs) {
             int mt, nt;
             tile_coords(t, num_m, num_n, p.group_m, mt, nt);
+            // The next kernel in the stream may be scheduled once every CTA
+            // is on its last tile: its CTAs then start on SMs as these exit
+            // (it still waits for this grid before touching memory).
+            if (t + npairs >= num_tiles && warp == 4 && lane == 0) pdl_launch_dependents();
             const bool got = wait_bounded_cluster(&acc_full[acc], acc_phase, ctl);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
             tc_fence_after_sync();
@@ -225,55 +239,23 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const int row0 = row - lane;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            if (p.vec_ok && t + npairs >= num_tiles) {
-                // Last tile: the pipeline stages are idle, so each warp stages
-                // its 32 x 32 output boxes in shared memory (TMA swizzled
-                // layout) and writes them with bulk tensor stores, which
-                // clip rows >= M and columns >= N.
-                const bool e4 = p.out_kind == kOutE4M3;
-                uint8_t* stg = sA + q * (BN * 64);
+            if (p.vec_ok) {
+                // Every tile: the warp's 32 x 32 boxes go through its staging
+                // box in shared memory and out by bulk tensor stores.  One
+                // store in flight per warp: the next box is written once the
+                // previous store has read the buffer (its tensor-memory load
+                // is already under way).
+                uint8_t* box = smem + C::kStagingOff + q * kBoxBytes;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     __syncwarp();
                     tmem_load_32cols(tbase + c * 32, r);
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
                     tmem_load_wait(r);
                     const int col0 = nt * BN + c * 32;
-                    const int ncols = min(32, p.N - col0);
-                    if (p.amax_out != nullptr && row < p.M) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i < ncols) amax_bits = max(amax_bits, r[i] & 0x7FFFFFFFu);
-                    }
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * alpha;
-                    uint8_t* box = stg + c * 2048;
-                    if (e4) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            w[j] = static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j], v[4 * j + 1])) |
-                                   (static_cast<uint32_t>(f32x2_to_e4m3x2(v[4 * j + 2], v[4 * j + 3])) << 16);
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const int ph = k ^ ((lane >> 2) & 1);
-                            st_shared_v4(smem_addr(box + lane * 32 + ph * 16), w[4 * k], w[4 * k + 1],
-                                         w[4 * k + 2], w[4 * k + 3]);
-                        }
-                    } else {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            w[j] = p.out_kind == kOutFP16 ? f32x2_to_f16x2(v[2 * j], v[2 * j + 1])
-                                                          : f32x2_to_bf16x2(v[2 * j], v[2 * j + 1]);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int ph = k ^ ((lane >> 1) & 3);
-                            st_shared_v4(smem_addr(box + lane * 64 + ph * 16), w[4 * k], w[4 * k + 1],
-                                         w[4 * k + 2], w[4 * k + 3]);
-                        }
-                    }
+                    amax_bits = max(amax_bits, stage_box(p, box, row, p.M, col0, r, alpha, lane));
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && row0 < p.M && col0 < p.N) {
@@ -281,8 +263,6 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         bulk_commit();
                     }
                 }
-                if (lane == 0) bulk_wait_all();
-                __syncwarp();
             } else {
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
@@ -303,6 +283,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        // The staging boxes must have been written out before the CTA exits.
+        if (lane == 0) bulk_wait_all();
         __syncwarp();
         publish_amax(p, amax_bits);
     }
@@ -379,26 +361,11 @@ cudaError_t launch_pair_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s
         !make_map(&tb, L.B, L.N, L.K, kFp16In, C::kBRows))
         return cudaErrorInvalidValue;
     Params prm2 = prm;
-    if (prm2.vec_ok) {
-        // Output map for the last tile's bulk stores: 32 x 32 boxes, swizzled
-        // to the width of one box row (64 B for 2-byte outputs, 32 B for E4M3).
-        auto encode = get_encode_fn();
-        const bool e4 = L.out_kind == kOutE4M3;
-        const CUtensorMapDataType dt = e4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                      : (L.out_kind == kOutFP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
-        cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.N), static_cast<cuuint64_t>(L.M)};
-        cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.N) * L.out_elem};
-        cuuint32_t box[2] = {32, 32};
-        cuuint32_t estr[2] = {1, 1};
-        if (!encode || encode(&td, dt, 2, L.D, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              e4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
-                              CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            prm2.vec_ok = 0;
+    // Output map of the staged epilogue (else the epilogue stores directly).
+    if (!prm2.vec_ok || !make_out_map(&td, L)) {
+        prm2.vec_ok = 0;
+        td = ta;
     }
-    if (!prm2.vec_ok) td = ta;
-    static_assert(STAGES * C::kABytes >= 4 * BN * 64, "staging for the last tile");
     const int pairs = L.plan->tiles < clusters ? L.plan->tiles : clusters;
     return launch_pair(kern, dim3(2 * pairs), C::kSmemBytes, s, ta, tb, td, prm2);
 }
