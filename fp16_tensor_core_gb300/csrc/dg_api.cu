@@ -86,6 +86,8 @@ Knobs read_knobs() {
     if (const char* e = std::getenv("DG_MMA_GEMV")) k.mma_gemv = e[0] == '0' ? 0 : e[0] == '1' ? 1 : -1;
     if (env_int("DG_MMA_GEMV_WARPS", 2, 8, &v) && (v == 2 || v == 3 || v == 4 || v == 8))
         k.mma_gemv_warps = static_cast<int>(v);
+    if (const char* e = std::getenv("DG_STAGED_EPI")) k.staged_epilogue = e[0] != '0';
+    if (const char* e = std::getenv("DG_EARLY_RELEASE")) k.early_release = e[0] != '0';
     return k;
 }
 

@@ -57,6 +57,8 @@ struct Knobs {
     int group_m = 0;            // DG_GROUP_M (1..4096): raster group of M tiles
     int mma_gemv = -1;          // DG_MMA_GEMV: 0 off, 1 for every M <= 16, else planned
     int mma_gemv_warps = 0;     // DG_MMA_GEMV_WARPS (2, 3, 4, 8): warps per CTA of that path
+    bool staged_epilogue = true;  // DG_STAGED_EPI=0: tiled epilogues store rows directly
+    bool early_release = true;    // DG_EARLY_RELEASE=0: tiled kernels release the next one at exit
 };
 const Knobs& knobs();
 

@@ -33,6 +33,8 @@ struct Params {
     // and D and rows [g*N, g*N + N) of B; sa/sb/sd hold one scale per group.
     const int* group_off;
     int groups;
+    int early_release;   // release the next kernel once every CTA is on its last tile
+    int staged;          // epilogue through staging boxes and bulk tensor stores (tmap_d)
 };
 
 constexpr int kMaxGroups = 1024;

@@ -298,7 +298,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
             // The next kernel in the stream may be scheduled once every CTA
             // is on its last tile (it still waits for this grid's memory).
-            if (t + static_cast<int>(gridDim.x) >= num_tiles && warp == 4 && lane == 0)
+            if (p.early_release && t + static_cast<int>(gridDim.x) >= num_tiles && warp == 4 &&
+                lane == 0)
                 pdl_launch_dependents();
             // Every lane waits; the vote reconverges the warp (tcgen05.ld is
             // .sync.aligned) and makes the whole warp leave together.
@@ -312,7 +313,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // Staged bulk stores (whole lines, M / N edges clipped by the
             // tensor map) unless the warp's 32 rows cross a group's end,
             // which the tensor map cannot clip: those rows store directly.
-            const bool staged = p.vec_ok && (!kGrouped || row0 + 32 <= T.row_end);
+            const bool staged = p.staged && (!kGrouped || row0 + 32 <= T.row_end);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
@@ -378,8 +379,8 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
         return cudaErrorInvalidValue;
     Params prm2 = prm;
     // Output map of the staged epilogue (else the epilogue stores directly).
-    if (!prm2.vec_ok || !make_out_map(&td, L)) {
-        prm2.vec_ok = 0;
+    if (!prm2.staged || !make_out_map(&td, L)) {
+        prm2.staged = 0;
         td = ta;
     }
     return launch_kernel(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped>, dim3(L.plan->grid),
@@ -527,6 +528,8 @@ Params make_params(const TcLaunch& L) {
     prm.out_kind = L.out_kind;
     prm.out_elem = L.out_elem;
     prm.vec_ok = ((static_cast<int64_t>(L.N) * L.out_elem) % 16 == 0) ? 1 : 0;
+    prm.staged = prm.vec_ok && knobs().staged_epilogue ? 1 : 0;   // confirmed by the launcher
+    prm.early_release = knobs().early_release ? 1 : 0;
     prm.status = L.status;
     prm.timeout_ns = wait_timeout_ns();
     prm.skip_first_load = take_skip_first_load() ? 1 : 0;

@@ -231,7 +231,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // The next kernel in the stream may be scheduled once every CTA
             // is on its last tile: its CTAs then start on SMs as these exit
             // (it still waits for this grid before touching memory).
-            if (t + npairs >= num_tiles && warp == 4 && lane == 0) pdl_launch_dependents();
+            if (p.early_release && t + npairs >= num_tiles && warp == 4 && lane == 0)
+                pdl_launch_dependents();
             const bool got = wait_bounded_cluster(&acc_full[acc], acc_phase, ctl);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
             tc_fence_after_sync();
@@ -239,7 +240,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const int row0 = row - lane;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            if (p.vec_ok) {
+            if (p.staged) {
                 // Every tile: the warp's 32 x 32 boxes go through its staging
                 // box in shared memory and out by bulk tensor stores.  One
                 // store in flight per warp: the next box is written once the
@@ -362,8 +363,8 @@ cudaError_t launch_pair_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s
         return cudaErrorInvalidValue;
     Params prm2 = prm;
     // Output map of the staged epilogue (else the epilogue stores directly).
-    if (!prm2.vec_ok || !make_out_map(&td, L)) {
-        prm2.vec_ok = 0;
+    if (!prm2.staged || !make_out_map(&td, L)) {
+        prm2.staged = 0;
         td = ta;
     }
     const int pairs = L.plan->tiles < clusters ? L.plan->tiles : clusters;
