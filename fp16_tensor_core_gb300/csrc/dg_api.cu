@@ -87,6 +87,7 @@ Knobs read_knobs() {
     if (env_int("DG_MMA_GEMV_WARPS", 2, 8, &v) && (v == 2 || v == 3 || v == 4 || v == 8))
         k.mma_gemv_warps = static_cast<int>(v);
     if (const char* e = std::getenv("DG_STAGED_EPI")) k.staged_epilogue = e[0] != '0';
+    if (const char* e = std::getenv("DG_SPLIT_TAIL")) k.split_tail = e[0] != '0';
     if (const char* e = std::getenv("DG_EARLY_RELEASE")) k.early_release = e[0] != '0';
     return k;
 }
@@ -377,7 +378,8 @@ dg_status check_hgemm_args(const void* A, const void* B, const void* D, int64_t 
 // split-K call (never while the stream is being captured into a graph).
 // *out stays null when the stream already holds none and the per-device cap
 // of allocated workspaces is reached.
-dg_status splitk_workspace(const DeviceState* st, cudaStream_t s, SplitkWs* out) {
+dg_status splitk_workspace(const DeviceState* st, cudaStream_t s, SplitkWs* out,
+                           bool may_allocate = true) {
     std::lock_guard<std::mutex> lk(g_ws_mu[st->device]);
     auto& map = g_ws[st->device];
     *out = SplitkWs{nullptr, nullptr};
@@ -392,7 +394,7 @@ dg_status splitk_workspace(const DeviceState* st, cudaStream_t s, SplitkWs* out)
         *out = map[s];
         return DG_OK;
     }
-    if (map.size() > kMaxStreamWorkspaces) return DG_OK;   // cap reached: none
+    if (!may_allocate || map.size() > kMaxStreamWorkspaces) return DG_OK;   // none
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -461,6 +463,17 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             L.group_off = nullptr;
             L.groups = 0;
             if (plan.path == 5) return from_cuda(launch_gemv_mma(L, s));
+            if (plan.path == 3 && plan.block_m == 256 && knobs().split_tail) {
+                // CTA pairs may split a partial last wave along K through the
+                // stream's split-K workspace (none: the tail runs whole).
+                SplitkWs ws;
+                if (splitk_workspace(st, s, &ws, /*may_allocate=*/false) == DG_OK &&
+                    ws.partials != nullptr) {
+                    L.tail_ws = ws.partials;
+                    L.tail_ws_bytes = splitk_partial_bytes(st->sm_count);
+                    L.tail_counts = ws.counts;
+                }
+            }
             if (plan.path == 4) {
                 SplitkWs ws;
                 rc = splitk_workspace(st, s, &ws);

@@ -58,6 +58,7 @@ struct Knobs {
     int mma_gemv = -1;          // DG_MMA_GEMV: 0 off, 1 for every M <= 16, else planned
     int mma_gemv_warps = 0;     // DG_MMA_GEMV_WARPS (2, 3, 4, 8): warps per CTA of that path
     bool staged_epilogue = true;  // DG_STAGED_EPI=0: tiled epilogues store rows directly
+    bool split_tail = true;       // DG_SPLIT_TAIL=0: CTA pairs run a partial last wave whole
     bool early_release = true;    // DG_EARLY_RELEASE=0: tiled kernels release the next one at exit
 };
 const Knobs& knobs();
@@ -136,6 +137,11 @@ struct TcLaunch {
     uint32_t* amax_out;   // optional running max |sa*sb*acc| (float bits)
     const int* group_off; // grouped GEMM: device offsets [groups + 1], else null
     int groups;
+    // CTA-pair kernel: workspace for splitting the tiles of a partial last
+    // wave along K (the split-K workspace of the stream), or null.
+    float* tail_ws = nullptr;
+    size_t tail_ws_bytes = 0;
+    uint32_t* tail_counts = nullptr;
 };
 cudaError_t launch_gemm_tc(const TcLaunch& L, cudaStream_t s);
 // Grouped variant (single-CTA tiles; L.plan->block_n is 128 or 256).

@@ -35,6 +35,11 @@ struct Params {
     int groups;
     int early_release;   // release the next kernel once every CTA is on its last tile
     int staged;          // epilogue through staging boxes and bulk tensor stores (tmap_d)
+    // CTA-pair kernel, split tail: the tiles left after the last full wave
+    // are cut into tail_split K ranges (>= 2; 1 = no split), one per pair.
+    int tail_split;
+    float* tail_ws;         // partial tiles: [slot][2 CTAs][BN / 4][128] float4
+    uint32_t* tail_counts;  // per tail tile and CTA: arrivals of the later parts
 };
 
 constexpr int kMaxGroups = 1024;

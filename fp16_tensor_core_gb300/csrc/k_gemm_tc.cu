@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "dg_internal.h"
@@ -481,23 +482,33 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     // CTA pairs (256 x BN tiles over sm_count / 2 clusters), for M >= 256.
     // Per-SM throughput relative to the single-CTA 128 x 256 tile: each SM
     // stores and reads only half of the tile's B rows.  Measured on GB300:
-    // 8192^3 E4M3 3607 vs 3399 TFLOP/s (1.06); at 4096^3 (BN 224) both run
-    // 48 us.  Pairs are used when their estimate is no worse; DG_2CTA=0
-    // disables them, DG_2CTA=1 forces them for M >= 256.
+    // 8192^3 E4M3 3607 vs 3399 TFLOP/s (1.06).  A pair MMA costs about the
+    // same whatever its N (4096^3 E4M3, interleaved: 45.6 / 45.7 / 53.4 /
+    // 61.3 / 70.3 us at BN 256 / 224 / 192 / 160 / 128 over 4 / 4 / 5 / 6 /
+    // 7 waves), so the narrower widths' relative rates are below their
+    // share of 256.  A partial last wave whose tiles the kernel splits along
+    // K (two to four K ranges per tile over idle pairs) counts as that
+    // fraction of a wave.  Pairs are used when their estimate is no worse;
+    // DG_2CTA=0 disables them, DG_2CTA=1 forces them for M >= 256.
     const bool pairs_off = kn.two_cta == 0;
     const bool pairs_forced = kn.two_cta == 1;
     if (!pairs_off && (!one_wave || pairs_forced) && M >= 256 && sm_count >= 2) {
         const int64_t pm = (M + 255) / 256;
         const int slots = sm_count / 2;
         const int pcand[5] = {256, 224, 192, 160, 128};
-        const double peff[5] = {1.06, 1.0, 0.93, 0.85, 0.76};
+        const double peff[5] = {1.06, 0.95, 0.83, 0.72, 0.58};
         int pbest = 256;
         double pcost = 0.0;
         for (int i = 0; i < 5; ++i) {
             const int bn = pcand[i];
             const int64_t pt = pm * ((N + bn - 1) / bn);
-            const int64_t waves = (pt + slots - 1) / slots;
-            const double cost = static_cast<double>(waves) * bn / peff[i];
+            const int64_t full = pt / slots, rem = pt % slots;
+            const int64_t split = rem > 0 ? std::min<int64_t>(slots / rem, 4) : 0;
+            double waves = static_cast<double>(full);
+            if (rem > 0)
+                waves += (kn.split_tail && split >= 2 && kblocks >= split)
+                             ? 1.0 / static_cast<double>(split) : 1.0;
+            const double cost = waves * bn / peff[i];
             if (i == 0 || cost < pcost) { pbest = bn; pcost = cost; }
         }
         {
@@ -530,6 +541,9 @@ Params make_params(const TcLaunch& L) {
     prm.vec_ok = ((static_cast<int64_t>(L.N) * L.out_elem) % 16 == 0) ? 1 : 0;
     prm.staged = prm.vec_ok && knobs().staged_epilogue ? 1 : 0;   // confirmed by the launcher
     prm.early_release = knobs().early_release ? 1 : 0;
+    prm.tail_split = 1;   // set by the CTA-pair launcher when the tail is split
+    prm.tail_ws = nullptr;
+    prm.tail_counts = nullptr;
     prm.status = L.status;
     prm.timeout_ns = wait_timeout_ns();
     prm.skip_first_load = take_skip_first_load() ? 1 : 0;

@@ -46,6 +46,7 @@ namespace dg {
 namespace {
 
 constexpr int kPairBM = 256;   // output rows of a pair tile
+constexpr uint32_t kEpiBarrier = 1;   // named barrier of the four epilogue warps
 constexpr int kHalfBM = 128;   // rows of it per CTA
 
 // Staging boxes of the epilogue: one 32 x 32 box per epilogue warp.
@@ -75,6 +76,53 @@ struct PairCfg {
     static_assert(kTmemCols <= 512, "TMEM columns");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
 };
+
+// One work item of a pair: a tile t and its K blocks [kb0, kb1); part -1 is
+// a whole tile, part s >= 0 the s-th K range of a split tail tile (part 0
+// finishes the tile: it adds the other parts' partial tiles in part order).
+struct PairItem {
+    int t, kb0, kb1, part, r;   // r: index of a split tile among the tail tiles
+};
+
+// Item i of pair `pair` (false when the pair has no item i).  Without a
+// split tail, tiles pair, pair + npairs, ...; with one (split >= 2), the
+// pair's tiles of the full waves, then -- for pairs < tail tiles x split --
+// part pair % split of tail tile pair / split.
+__device__ __forceinline__ bool pair_item(int i, int pair, int npairs, int num_tiles, int num_kb,
+                                          int split, PairItem& it) {
+    if (split < 2) {
+        it.t = pair + i * npairs;
+        it.kb0 = 0;
+        it.kb1 = num_kb;
+        it.part = -1;
+        it.r = 0;
+        return it.t < num_tiles;
+    }
+    const int full_tiles = num_tiles / npairs * npairs;
+    const int nfull = full_tiles / npairs;
+    if (i < nfull) {
+        it.t = pair + i * npairs;
+        it.kb0 = 0;
+        it.kb1 = num_kb;
+        it.part = -1;
+        it.r = 0;
+        return true;
+    }
+    if (i > nfull || pair >= (num_tiles - full_tiles) * split) return false;
+    it.r = pair / split;
+    it.part = pair % split;
+    it.t = full_tiles + it.r;
+    it.kb0 = it.part * num_kb / split;
+    it.kb1 = (it.part + 1) * num_kb / split;
+    return true;
+}
+
+// Acquire load of a split tail tile's arrival counter.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 template <int BN, int STAGES, bool kFp16In>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -145,12 +193,13 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
         bool ok = true;
         const uint32_t leader_full = map_to_rank(full, 0);
-        for (int t = pair; t < num_tiles && ok; t += npairs) {
+        PairItem it;
+        for (int i = 0; ok && pair_item(i, pair, npairs, num_tiles, num_kb, p.tail_split, it); ++i) {
             int mt, nt;
-            tile_coords(t, num_m, num_n, p.group_m, mt, nt);
+            tile_coords(it.t, num_m, num_n, p.group_m, mt, nt);
             const int a_row = mt * kPairBM + static_cast<int>(rank) * kHalfBM;
             const int b_row = nt * BN + static_cast<int>(rank) * C::kBRows;
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int kb = it.kb0; kb < it.kb1; ++kb) {
                 if (!wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
                 if (skip) {
                     skip = false;            // leave this stage unloaded
@@ -181,11 +230,12 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = pair; t < num_tiles && ok; t += npairs) {
+            PairItem it;
+            for (int i = 0; ok && pair_item(i, pair, npairs, num_tiles, num_kb, p.tail_split, it); ++i) {
                 if (!wait_bounded_cluster(&acc_empty[acc], acc_phase ^ 1u, ctl)) { ok = false; break; }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wait_bounded_cluster(&full[stage], phase, ctl)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
@@ -194,7 +244,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     for (int kk = 0; kk < kBKBytes / 32; ++kk) {
                         const uint64_t ad = sdesc_k_major_sw128(a0 + kk * 32);
                         const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
-                        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t accum = (kb > it.kb0 || kk > 0) ? 1u : 0u;
                         if constexpr (kFp16In)
                             mma_f16_pair(d_tmem, ad, bd, C::kIdesc, accum);
                         else
@@ -225,22 +275,95 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         uint32_t amax_bits = 0u;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = pair; t < num_tiles; t += npairs) {
+        const int r_local = q * 32 + lane;   // this thread's row of the CTA's 128
+        constexpr int kSlotF4 = BN / 4 * kHalfBM;   // float4s of one partial tile
+        PairItem it;
+        for (int i = 0; pair_item(i, pair, npairs, num_tiles, num_kb, p.tail_split, it); ++i) {
             int mt, nt;
-            tile_coords(t, num_m, num_n, p.group_m, mt, nt);
+            tile_coords(it.t, num_m, num_n, p.group_m, mt, nt);
             // The next kernel in the stream may be scheduled once every CTA
-            // is on its last tile: its CTAs then start on SMs as these exit
+            // is on its last item: its CTAs then start on SMs as these exit
             // (it still waits for this grid before touching memory).
-            if (p.early_release && t + npairs >= num_tiles && warp == 4 && lane == 0)
+            PairItem nx;
+            if (p.early_release && warp == 4 && lane == 0 &&
+                !pair_item(i + 1, pair, npairs, num_tiles, num_kb, p.tail_split, nx))
                 pdl_launch_dependents();
+            // The four warps continue or leave together (the split tail
+            // below synchronises them on a named barrier).
             const bool got = wait_bounded_cluster(&acc_full[acc], acc_phase, ctl);
-            if (!__all_sync(0xFFFFFFFFu, got)) break;
+            if (!named_bar_and(kEpiBarrier, 128, got)) break;
             tc_fence_after_sync();
             const int row = mt * kPairBM + static_cast<int>(rank) * kHalfBM + q * 32 + lane;
             const int row0 = row - lane;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            if (p.staged) {
+            // Split tail tile: this CTA's partial tile of part s lives in slot
+            // (r * (split - 1) + s - 1) * 2 + rank, as FP32 column quads
+            // ([BN / 4][128] float4: a warp's 32 rows are one 512-byte run).
+            auto slot_of = [&](int s) {
+                return reinterpret_cast<float4*>(p.tail_ws) +
+                       static_cast<int64_t>((it.r * (p.tail_split - 1) + s - 1) * 2 +
+                                            static_cast<int>(rank)) * kSlotF4;
+            };
+            uint32_t* const counter = p.tail_counts + it.r * 2 + static_cast<int>(rank);
+            bool ready = true;
+            if (it.part > 0) {
+                // A later part: publish the partial tile, count the arrival.
+                float4* mine = slot_of(it.part);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_load_32cols(tbase + c * 32, r);
+                    tmem_load_wait(r);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        __stcg(mine + (c * 8 + g) * kHalfBM + r_local,
+                               make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                           __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+                }
+                named_bar_sync(kEpiBarrier, 128);   // every row of the CTA's half is out
+                if (threadIdx.x == 128) {
+                    __threadfence();
+                    atomicAdd(counter, 1u);
+                }
+            } else if (it.part == 0) {
+                // The first part finishes the tile: wait (bounded) until the
+                // other parts have published theirs.
+                bool arrived = true;
+                if (threadIdx.x == 128) {
+                    const uint32_t want = static_cast<uint32_t>(p.tail_split - 1);
+                    const uint64_t t0 = global_timer_ns();
+                    while (ld_acquire_gpu(counter) < want) {
+                        if (*ctl.abort_flag || global_timer_ns() - t0 > ctl.timeout_ns) {
+                            *ctl.abort_flag = 1;
+                            atomicOr(ctl.status, kStatusTimeout);
+                            arrived = false;
+                            break;
+                        }
+                    }
+                }
+                ready = named_bar_and(kEpiBarrier, 128, arrived);
+            }
+            // Adds the other parts' partials (in part order) to a chunk of
+            // the first part's accumulator.
+            auto add_parts = [&](int c, uint32_t (&r)[32]) {
+                if (it.part != 0) return;
+                for (int s = 1; s < p.tail_split; ++s) {
+                    const float4* w = slot_of(s);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const float4 x = __ldcg(w + (c * 8 + g) * kHalfBM + r_local);
+                        r[4 * g] = __float_as_uint(__uint_as_float(r[4 * g]) + x.x);
+                        r[4 * g + 1] = __float_as_uint(__uint_as_float(r[4 * g + 1]) + x.y);
+                        r[4 * g + 2] = __float_as_uint(__uint_as_float(r[4 * g + 2]) + x.z);
+                        r[4 * g + 3] = __float_as_uint(__uint_as_float(r[4 * g + 3]) + x.w);
+                    }
+                }
+            };
+            if (it.part > 0 || !ready) {
+                // nothing to store (a later part, or a wait that ran out)
+            } else if (p.staged) {
                 // Every tile: the warp's 32 x 32 boxes go through its staging
                 // box in shared memory and out by bulk tensor stores.  One
                 // store in flight per warp: the next box is written once the
@@ -255,6 +378,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                     tmem_load_wait(r);
+                    add_parts(c, r);
                     const int col0 = nt * BN + c * 32;
                     amax_bits = max(amax_bits, stage_box(p, box, row, p.M, col0, r, alpha, lane));
                     fence_proxy_async_smem();
@@ -271,8 +395,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     __syncwarp();
                     tmem_load_32cols(tbase + c * 32, r);
                     tmem_load_wait(r);
+                    add_parts(c, r);
                     amax_bits = max(amax_bits, store_chunk(p, row, p.M, nt * BN + c * 32, r, alpha));
                 }
+            }
+            if (it.part == 0 && ready) {
+                // every partial has been read: the counter is zero again for
+                // the next launch
+                named_bar_sync(kEpiBarrier, 128);
+                if (threadIdx.x == 128) atomicExch(counter, 0u);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -362,12 +493,31 @@ cudaError_t launch_pair_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s
         !make_map(&tb, L.B, L.N, L.K, kFp16In, C::kBRows))
         return cudaErrorInvalidValue;
     Params prm2 = prm;
+    // Split tail: when the last wave is partial, its tiles are cut into
+    // `split` K ranges over the otherwise idle pairs (at least two per tile,
+    // at most four, each range at least one K block), if the stream's
+    // workspace holds their partial tiles.
+    const int pairs = L.plan->tiles < clusters ? L.plan->tiles : clusters;
+    prm2.tail_split = 1;
+    if (knobs().split_tail && L.tail_ws != nullptr && L.tail_counts != nullptr && pairs > 0) {
+        const int rem = L.plan->tiles % pairs;
+        const int num_kb = (L.K + C::kBK - 1) / C::kBK;
+        int split = rem > 0 ? pairs / rem : 0;
+        if (split > 4) split = 4;
+        const size_t need = static_cast<size_t>(rem) * (split > 1 ? split - 1 : 0) * 2 * BN *
+                            kHalfBM * sizeof(float);
+        if (split >= 2 && num_kb >= split && need <= L.tail_ws_bytes &&
+            2 * rem <= kSkinnyMaxTiles) {
+            prm2.tail_split = split;
+            prm2.tail_ws = L.tail_ws;
+            prm2.tail_counts = L.tail_counts;
+        }
+    }
     // Output map of the staged epilogue (else the epilogue stores directly).
     if (!prm2.staged || !make_out_map(&td, L)) {
         prm2.staged = 0;
         td = ta;
     }
-    const int pairs = L.plan->tiles < clusters ? L.plan->tiles : clusters;
     return launch_pair(kern, dim3(2 * pairs), C::kSmemBytes, s, ta, tb, td, prm2);
 }
 
