@@ -140,7 +140,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint64_t* acc_full = empty + STAGES;   // [2]
     uint64_t* acc_empty = acc_full + 2;    // [2], used in the even CTA
     uint64_t* drain = acc_empty + 2;       // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* fix_bar = drain + 1;         // [1] split tail: partial tiles staged in the ring
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fix_bar + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,6 +158,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             mbar_init(&acc_empty[b], 8);
         }
         mbar_init(drain, 1);
+        mbar_init(fix_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -277,6 +279,13 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         uint32_t acc_phase = 0;
         const int r_local = q * 32 + lane;   // this thread's row of the CTA's 128
         constexpr int kSlotF4 = BN / 4 * kHalfBM;   // float4s of one partial tile
+        constexpr int kSlotBytes = kSlotF4 * 16;
+        constexpr int kCopyPiece = 16384;           // bulk copies of 16 KB
+        static_assert(kSlotBytes % kCopyPiece == 0, "partial tile in whole pieces");
+        static_assert(STAGES * C::kStageBytes >= kSlotBytes, "a partial tile fits in the ring");
+        // every other part's partial tile fits in the idle ring: staged loads
+        const bool staged_parts =
+            static_cast<int64_t>(p.tail_split - 1) * kSlotBytes <= STAGES * C::kStageBytes;
         PairItem it;
         for (int i = 0; pair_item(i, pair, npairs, num_tiles, num_kb, p.tail_split, it); ++i) {
             int mt, nt;
@@ -308,8 +317,11 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             uint32_t* const counter = p.tail_counts + it.r * 2 + static_cast<int>(rank);
             bool ready = true;
             if (it.part > 0) {
-                // A later part: publish the partial tile, count the arrival.
-                float4* mine = slot_of(it.part);
+                // A later part (the CTA's last item: its ring of stages is
+                // idle): the partial tile goes into the ring in the slot's
+                // layout, then out with one bulk copy; the arrival is counted
+                // once the copy's writes are complete.
+                float4* ring4 = reinterpret_cast<float4*>(smem);
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
@@ -318,12 +330,17 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tmem_load_wait(r);
 #pragma unroll
                     for (int g = 0; g < 8; ++g)
-                        __stcg(mine + (c * 8 + g) * kHalfBM + r_local,
-                               make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                           __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+                        ring4[(c * 8 + g) * kHalfBM + r_local] =
+                            make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                        __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
                 }
-                named_bar_sync(kEpiBarrier, 128);   // every row of the CTA's half is out
+                fence_proxy_async_smem();
+                named_bar_sync(kEpiBarrier, 128);   // the whole partial tile is in the ring
                 if (threadIdx.x == 128) {
+                    bulk_store_s2g(slot_of(it.part), smem, kSlotBytes);
+                    bulk_commit();
+                    bulk_wait_all();
+                    fence_proxy_async_global();
                     __threadfence();
                     atomicAdd(counter, 1u);
                 }
@@ -344,16 +361,36 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     }
                 }
                 ready = named_bar_and(kEpiBarrier, 128, arrived);
+                if (ready && staged_parts) {
+                    // the other parts' partial tiles into the idle ring, in
+                    // part order, on one barrier (used once per CTA)
+                    if (threadIdx.x == 128) {
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(fix_bar, static_cast<uint32_t>(p.tail_split - 1) *
+                                                           kSlotBytes);
+                        for (int s2 = 1; s2 < p.tail_split; ++s2)
+                            for (int piece = 0; piece < kSlotBytes; piece += kCopyPiece)
+                                bulk_load_g2s(smem + (s2 - 1) * kSlotBytes + piece,
+                                              reinterpret_cast<const uint8_t*>(slot_of(s2)) + piece,
+                                              kCopyPiece, fix_bar);
+                    }
+                    const bool landed = wait_bounded(fix_bar, 0, ctl);
+                    ready = named_bar_and(kEpiBarrier, 128, landed);
+                    if (!ready && threadIdx.x == 128) wait_bounded(fix_bar, 0, ctl, false);
+                }
             }
             // Adds the other parts' partials (in part order) to a chunk of
-            // the first part's accumulator.
+            // the first part's accumulator, from the ring when staged.
             auto add_parts = [&](int c, uint32_t (&r)[32]) {
                 if (it.part != 0) return;
                 for (int s = 1; s < p.tail_split; ++s) {
-                    const float4* w = slot_of(s);
+                    const float4* w = staged_parts
+                        ? reinterpret_cast<const float4*>(smem + (s - 1) * kSlotBytes)
+                        : slot_of(s);
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
-                        const float4 x = __ldcg(w + (c * 8 + g) * kHalfBM + r_local);
+                        const float4 x = staged_parts ? w[(c * 8 + g) * kHalfBM + r_local]
+                                                      : __ldcg(w + (c * 8 + g) * kHalfBM + r_local);
                         r[4 * g] = __float_as_uint(__uint_as_float(r[4 * g]) + x.x);
                         r[4 * g + 1] = __float_as_uint(__uint_as_float(r[4 * g + 1]) + x.y);
                         r[4 * g + 2] = __float_as_uint(__uint_as_float(r[4 * g + 2]) + x.z);
