@@ -197,15 +197,6 @@ __device__ __forceinline__ void bulk_load_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
-// 1-D bulk copy shared -> global of `bytes` (a multiple of 16, both
-// addresses 16-byte aligned), tracked per thread in bulk groups
-// (bulk_commit / bulk_wait_all).
-__device__ __forceinline__ void bulk_store_s2g(void* dst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 :: "l"(reinterpret_cast<uint64_t>(dst)), "r"(smem_addr(src)), "r"(bytes)
-                 : "memory");
-}
-
 // Orders global-memory state this thread observes through the generic proxy
 // (e.g. after an acquire) before its later async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -85,35 +85,38 @@ struct PairItem {
 };
 
 // Item i of pair `pair` (false when the pair has no item i).  Without a
-// split tail, tiles pair, pair + npairs, ...; with one (split >= 2), the
-// pair's tiles of the full waves, then -- for pairs < tail tiles x split --
-// part pair % split of tail tile pair / split.
+// split tail, tiles pair, pair + npairs, ...; with one (split >= 2), pairs
+// < tail tiles x split hold part pair % split of tail tile pair / split.
+// A pair holding a later part runs it first, so that its partial tile is
+// published long before it is needed; the pair holding part 0 runs it last,
+// after its tiles of the full waves, and finishes the tile.
 __device__ __forceinline__ bool pair_item(int i, int pair, int npairs, int num_tiles, int num_kb,
                                           int split, PairItem& it) {
+    it.kb0 = 0;
+    it.kb1 = num_kb;
+    it.part = -1;
+    it.r = 0;
     if (split < 2) {
         it.t = pair + i * npairs;
-        it.kb0 = 0;
-        it.kb1 = num_kb;
-        it.part = -1;
-        it.r = 0;
         return it.t < num_tiles;
     }
     const int full_tiles = num_tiles / npairs * npairs;
     const int nfull = full_tiles / npairs;
-    if (i < nfull) {
-        it.t = pair + i * npairs;
-        it.kb0 = 0;
-        it.kb1 = num_kb;
-        it.part = -1;
-        it.r = 0;
+    const bool has_part = pair < (num_tiles - full_tiles) * split;
+    const int part = pair % split;
+    int tail_at = -1;                        // position of the tail item
+    if (has_part) tail_at = part > 0 ? 0 : nfull;
+    if (i == tail_at) {
+        it.r = pair / split;
+        it.part = part;
+        it.t = full_tiles + it.r;
+        it.kb0 = part * num_kb / split;
+        it.kb1 = (part + 1) * num_kb / split;
         return true;
     }
-    if (i > nfull || pair >= (num_tiles - full_tiles) * split) return false;
-    it.r = pair / split;
-    it.part = pair % split;
-    it.t = full_tiles + it.r;
-    it.kb0 = it.part * num_kb / split;
-    it.kb1 = (it.part + 1) * num_kb / split;
+    const int f = (tail_at == 0) ? i - 1 : i;   // index among the pair's full tiles
+    if (f < 0 || f >= nfull) return false;
+    it.t = pair + f * npairs;
     return true;
 }
 
@@ -317,11 +320,11 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             uint32_t* const counter = p.tail_counts + it.r * 2 + static_cast<int>(rank);
             bool ready = true;
             if (it.part > 0) {
-                // A later part (the CTA's last item: its ring of stages is
-                // idle): the partial tile goes into the ring in the slot's
-                // layout, then out with one bulk copy; the arrival is counted
-                // once the copy's writes are complete.
-                float4* ring4 = reinterpret_cast<float4*>(smem);
+                // A later part (the pair's first item; its next tiles'
+                // main loop runs meanwhile): publish the partial tile with
+                // coalesced stores (a warp's 32 rows of a column quad are one
+                // 512-byte run), then count the arrival.
+                float4* mine = slot_of(it.part);
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
@@ -330,17 +333,12 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tmem_load_wait(r);
 #pragma unroll
                     for (int g = 0; g < 8; ++g)
-                        ring4[(c * 8 + g) * kHalfBM + r_local] =
-                            make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                        __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+                        __stcg(mine + (c * 8 + g) * kHalfBM + r_local,
+                               make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                           __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
                 }
-                fence_proxy_async_smem();
-                named_bar_sync(kEpiBarrier, 128);   // the whole partial tile is in the ring
+                named_bar_sync(kEpiBarrier, 128);   // every row of the CTA's half is out
                 if (threadIdx.x == 128) {
-                    bulk_store_s2g(slot_of(it.part), smem, kSlotBytes);
-                    bulk_commit();
-                    bulk_wait_all();
-                    fence_proxy_async_global();
                     __threadfence();
                     atomicAdd(counter, 1u);
                 }
