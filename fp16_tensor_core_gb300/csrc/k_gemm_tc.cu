@@ -79,6 +79,8 @@ struct Cfg {
     static_assert(kTmemCols <= 512, "TMEM columns");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
     static_assert(kBBytes % 1024 == 0, "1024-byte aligned B stages (128-byte swizzle atoms)");
+    static_assert(STAGES * kStageBytes >= 4 * (BN / 32) * kBoxBytes,
+                  "every output box of a tile fits in the ring");
 };
 
 // Output tile t of this launch: A rows from a_row, B rows from b_row,
@@ -290,7 +292,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         int acc = 0;
         uint32_t acc_phase = 0;
         int gcur = 0;
-        uint8_t* box = smem + C::kStagingOff + q * kBoxBytes;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
             const Tile T = tile_of(t, gcur);
             if (T.g != alpha_g) {
@@ -299,9 +300,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
             // The next kernel in the stream may be scheduled once every CTA
             // is on its last tile (it still waits for this grid's memory).
-            if (p.early_release && t + static_cast<int>(gridDim.x) >= num_tiles && warp == 4 &&
-                lane == 0)
-                pdl_launch_dependents();
+            const bool last_tile = t + static_cast<int>(gridDim.x) >= num_tiles;
+            if (p.early_release && last_tile && warp == 4 && lane == 0) pdl_launch_dependents();
             // Every lane waits; the vote reconverges the warp (tcgen05.ld is
             // .sync.aligned) and makes the whole warp leave together.
             const bool got = wait_bounded(&acc_full[acc], acc_phase, ctl);
@@ -314,6 +314,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // Staged bulk stores (whole lines, M / N edges clipped by the
             // tensor map) unless the warp's 32 rows cross a group's end,
             // which the tensor map cannot clip: those rows store directly.
+            // One staging box per warp while later tiles' main loops run;
+            // on the last tile the ring of stages is idle and every box has
+            // a place of its own in it, so the stores go out back to back.
             const bool staged = p.staged && (!kGrouped || row0 + 32 <= T.row_end);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -321,7 +324,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 tmem_load_32cols(tbase + c * 32, r);
                 if (staged) {
-                    if (lane == 0) bulk_wait_read_all();   // the box is free again
+                    uint8_t* box = last_tile ? smem + (q * (BN / 32) + c) * kBoxBytes
+                                             : smem + C::kStagingOff + q * kBoxBytes;
+                    if (!last_tile && lane == 0) bulk_wait_read_all();   // the box is free again
                     __syncwarp();
                     tmem_load_wait(r);
                     const int col0 = T.col0 + c * 32;

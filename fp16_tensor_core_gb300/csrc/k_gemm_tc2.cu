@@ -285,7 +285,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         constexpr int kSlotBytes = kSlotF4 * 16;
         constexpr int kCopyPiece = 16384;           // bulk copies of 16 KB
         static_assert(kSlotBytes % kCopyPiece == 0, "partial tile in whole pieces");
-        static_assert(STAGES * C::kStageBytes >= kSlotBytes, "a partial tile fits in the ring");
+        static_assert(STAGES * C::kStageBytes >= kSlotBytes + 4 * (BN / 32) * kBoxBytes,
+                      "a partial tile and every output box of a tile fit in the ring");
         // every other part's partial tile fits in the idle ring: staged loads
         const bool staged_parts =
             static_cast<int64_t>(p.tail_split - 1) * kSlotBytes <= STAGES * C::kStageBytes;
@@ -297,9 +298,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // is on its last item: its CTAs then start on SMs as these exit
             // (it still waits for this grid before touching memory).
             PairItem nx;
-            if (p.early_release && warp == 4 && lane == 0 &&
-                !pair_item(i + 1, pair, npairs, num_tiles, num_kb, p.tail_split, nx))
-                pdl_launch_dependents();
+            const bool last_item = !pair_item(i + 1, pair, npairs, num_tiles, num_kb, p.tail_split, nx);
+            if (p.early_release && warp == 4 && lane == 0 && last_item) pdl_launch_dependents();
             // The four warps continue or leave together (the split tail
             // below synchronises them on a named barrier).
             const bool got = wait_bounded_cluster(&acc_full[acc], acc_phase, ctl);
@@ -399,18 +399,24 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             if (it.part > 0 || !ready) {
                 // nothing to store (a later part, or a wait that ran out)
             } else if (p.staged) {
-                // Every tile: the warp's 32 x 32 boxes go through its staging
-                // box in shared memory and out by bulk tensor stores.  One
-                // store in flight per warp: the next box is written once the
-                // previous store has read the buffer (its tensor-memory load
-                // is already under way).
-                uint8_t* box = smem + C::kStagingOff + q * kBoxBytes;
+                // Every tile: the warp's 32 x 32 boxes go through shared
+                // memory and out by bulk tensor stores.  While later tiles'
+                // main loops run, one staging box per warp (the next box is
+                // written once the previous store has read the buffer); on
+                // the CTA's last item, whose ring of stages is idle, every
+                // box has a place of its own in the ring (after any staged
+                // partial tiles), so the stores go out back to back.
+                const int ring_base = (it.part == 0 && staged_parts)
+                                          ? (p.tail_split - 1) * kSlotBytes : 0;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     __syncwarp();
                     tmem_load_32cols(tbase + c * 32, r);
-                    if (lane == 0) bulk_wait_read_all();
+                    uint8_t* box = last_item
+                        ? smem + ring_base + (q * (BN / 32) + c) * kBoxBytes
+                        : smem + C::kStagingOff + q * kBoxBytes;
+                    if (!last_item && lane == 0) bulk_wait_read_all();
                     __syncwarp();
                     tmem_load_wait(r);
                     add_parts(c, r);
