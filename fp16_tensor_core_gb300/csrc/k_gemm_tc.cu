@@ -331,6 +331,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tmem_load_wait(r);
                     const int col0 = T.col0 + c * 32;
                     amax_bits = max(amax_bits, stage_box(p, box, row, T.row_end, col0, r, alpha, lane));
+                    if (last_tile) continue;   // stored together below
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && row0 < T.row_end && col0 < p.N) {
@@ -340,6 +341,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 } else {
                     tmem_load_wait(r);
                     amax_bits = max(amax_bits, store_chunk(p, row, T.row_end, T.col0 + c * 32, r, alpha));
+                }
+            }
+            if (staged && last_tile) {
+                // every box of the warp is in the idle ring: one fence, then
+                // all of its stores
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && row0 < T.row_end) {
+                    for (int c = 0; c < BN / 32 && T.col0 + c * 32 < p.N; ++c)
+                        tma_store_2d(&tmap_d, smem + (q * (BN / 32) + c) * kBoxBytes, T.col0 + c * 32,
+                                     row0);
+                    bulk_commit();
                 }
             }
             tc_fence_before_sync();

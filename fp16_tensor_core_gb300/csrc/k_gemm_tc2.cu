@@ -422,10 +422,23 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     add_parts(c, r);
                     const int col0 = nt * BN + c * 32;
                     amax_bits = max(amax_bits, stage_box(p, box, row, p.M, col0, r, alpha, lane));
+                    if (last_item) continue;   // stored together below
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && row0 < p.M && col0 < p.N) {
                         tma_store_2d(&tmap_d, box, col0, row0);
+                        bulk_commit();
+                    }
+                }
+                if (last_item) {
+                    // every box of the warp is in the ring: one fence, then
+                    // all of its stores
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.M) {
+                        for (int c = 0; c < BN / 32 && nt * BN + c * 32 < p.N; ++c)
+                            tma_store_2d(&tmap_d, smem + ring_base + (q * (BN / 32) + c) * kBoxBytes,
+                                         nt * BN + c * 32, row0);
                         bulk_commit();
                     }
                 }
