@@ -87,7 +87,7 @@ Knobs read_knobs() {
     if (env_int("DG_MMA_GEMV_WARPS", 2, 8, &v) && (v == 2 || v == 3 || v == 4 || v == 8))
         k.mma_gemv_warps = static_cast<int>(v);
     if (const char* e = std::getenv("DG_STAGED_EPI")) k.staged_epilogue = e[0] != '0';
-    if (const char* e = std::getenv("DG_SPLIT_TAIL")) k.split_tail = e[0] != '0';
+    if (const char* e = std::getenv("DG_SPLIT_TAIL")) k.split_tail = e[0] == '1';
     if (const char* e = std::getenv("DG_EARLY_RELEASE")) k.early_release = e[0] != '0';
     return k;
 }

@@ -58,7 +58,7 @@ struct Knobs {
     int mma_gemv = -1;          // DG_MMA_GEMV: 0 off, 1 for every M <= 16, else planned
     int mma_gemv_warps = 0;     // DG_MMA_GEMV_WARPS (2, 3, 4, 8): warps per CTA of that path
     bool staged_epilogue = true;  // DG_STAGED_EPI=0: tiled epilogues store rows directly
-    bool split_tail = true;       // DG_SPLIT_TAIL=0: CTA pairs run a partial last wave whole
+    bool split_tail = false;      // DG_SPLIT_TAIL=1: CTA pairs split a partial last wave along K
     bool early_release = true;    // DG_EARLY_RELEASE=0: tiled kernels release the next one at exit
 };
 const Knobs& knobs();

@@ -364,13 +364,12 @@ def _plan_paths_and_tiles(sm):
     big = dg.dg_gemm_plan(8192, 8192, 8192, sm_count=sm)
     assert small["block_n"] < big["block_n"]
     assert big["grid"] == sm and big["block_m"] == 256 and big["block_n"] == 256
-    # 4096^3: 256 pair tiles of 256 x 256, three full waves over 76 pairs and
-    # a last wave of 28 tiles that the kernel splits along K
+    # 4096^3: 304 pair tiles of 256 x 224, exactly four waves over 76 pairs
     sq = dg.dg_gemm_plan(4096, 4096, 4096, sm_count=sm)
-    assert (sq["block_m"], sq["block_n"], sq["tiles"]) == (256, 256, 256)
-    with knobs(DG_SPLIT_TAIL="0"):   # without the split: 304 tiles of 256 x 224, four waves
-        sq = dg.dg_gemm_plan(4096, 4096, 4096, sm_count=sm)
-        assert (sq["block_m"], sq["block_n"], sq["tiles"]) == (256, 224, 304)
+    assert (sq["block_m"], sq["block_n"], sq["tiles"]) == (256, 224, 304)
+    with knobs(DG_SPLIT_TAIL="1"):   # with the split tail: 256 tiles of 256 x 256, the
+        sq = dg.dg_gemm_plan(4096, 4096, 4096, sm_count=sm)   # last 28 split along K
+        assert (sq["block_m"], sq["block_n"], sq["tiles"]) == (256, 256, 256)
 
 
 def test_plan_argument_errors(L):

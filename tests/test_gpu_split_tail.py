@@ -1,7 +1,8 @@
-"""CTA-pair GEMM with a split tail: when the tiles do not fill the last wave
-of pairs, the kernel cuts each remaining tile into 2-4 K ranges over the
-otherwise idle pairs; the pair holding the first range adds the others'
-FP32 partial tiles in range order and stores the tile.  Checked against
+"""CTA-pair GEMM with a split tail (DG_SPLIT_TAIL=1; measured no faster than
+whole tiles on GB300, so off by default): when the tiles do not fill the
+last wave of pairs, the kernel cuts each remaining tile into 2-4 K ranges
+over the otherwise idle pairs; the pair holding the first range adds the
+others' FP32 partial tiles in range order and stores the tile.  Checked against
 the oracle on every output ([FP8-guide] §3.1's K-blocked accumulation, §3.3
 edges), for 2, 3 and 4 ranges per tile (which of them a shape gets depends
 on how many pairs the GPU runs at once, so several shapes are used), ragged
@@ -36,7 +37,7 @@ def _lib():
     from fp16_tensor_core_gb300 import build
     build.build()
     dg.dg_init()
-    with knobs(DG_2CTA="1", DG_FORCE_BLOCK_N="256"):
+    with knobs(DG_2CTA="1", DG_FORCE_BLOCK_N="256", DG_SPLIT_TAIL="1"):
         yield
     assert dg.dg_sync_status() == dg.DG_OK
 
