@@ -38,11 +38,6 @@ FLOP_PER_STEP = 2.0 * M * N * K
 WORKLOAD = "fp8_8192_e4m3out"
 CPU_SAMPLE_ROWS = 3072  # ~10-20 s of oracle work on 16 cores
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
-# Kernel sources whose change invalidates recorded ncu traffic (the tiled
-# GEMMs, the split-K kernel and the GEMV).
-GEMM_SOURCES = [os.path.join(ROOT, "fp16_tensor_core_gb300", "csrc", f)
-                for f in ("k_gemm_tc2.cu", "k_gemm_tc.cu", "k_gemm_skinny.cu", "k_gemv.cu",
-                          "gemm_common.cuh", "dg_ptx.cuh")]
 # Nominal dense FP8 tensor rate of one GB300 (NVIDIA's figure without 2:4
 # sparsity), for context beside the measured-peak fraction.
 NOMINAL_FP8_TFLOPS = 4500.0
@@ -61,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--kernel", default=None, help="time one kernel workload alone")
     ap.add_argument("--graph", action="store_true",
                     help="with --kernel: also time the launches replayed from a CUDA graph")
+    ap.add_argument("--record-traffic", nargs="+", default=None, metavar="WORKLOAD=CSV",
+                    help="write profiles/traffic.json from ncu CSV logs (no GPU work)")
     ap.add_argument("--settle-seconds", type=float, default=1.5,
                     help="untimed busy period before the timed steps (clock sampling)")
     return ap.parse_args(argv)
@@ -110,24 +107,24 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
-def gemm_source_hash() -> str:
+def source_hash(files) -> str:
+    """First 16 hex digits of the SHA-256 of the named kernel sources."""
     h = hashlib.sha256()
-    for p in GEMM_SOURCES:
-        with open(p, "rb") as f:
+    for name in files:
+        with open(os.path.join(ROOT, "fp16_tensor_core_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str = WORKLOAD):
     """DRAM bytes per launch of `workload`'s kernel from the committed ncu
-    summary, if it was taken on the current kernel sources; else None."""
+    summary, if it was taken on the kernel's current sources; else None."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as f:
         rec = json.load(f)
-    entries = rec.get("entries", [rec])
-    for e in entries:
-        if e.get("workload") == workload and e.get("source_sha256_16") == gemm_source_hash():
+    for e in rec.get("entries", []):
+        if e.get("workload") == workload and e.get("source_sha256_16") == source_hash(e["sources"]):
             return e.get("dram_bytes_per_launch")
     return None
 
@@ -832,8 +829,65 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# Kernels behind the workloads whose DRAM traffic is recorded: (name pattern
+# in the ncu CSV, sources the counters depend on, algorithmic bytes per
+# launch, description).
+TRAFFIC_KERNELS = {
+    "fp8_gemm_8192_e4m3out": ("gemm_tc_pair_kernel",
+                              ["k_gemm_tc2.cu", "gemm_common.cuh", "dg_ptx.cuh"],
+                              3 * 8192 * 8192, "E4M3 8192^3, E4M3 out, 256 x 256 CTA-pair tiles"),
+    "qkv_gemv_1x12288x4096": ("gemv_mma_kernel", ["k_gemv_mma.cu", "dg_ptx.cuh"],
+                              12288 * 4096 + 4096 + 12288 * 2,
+                              "E4M3 1 x 12288 x 4096 (decode QKV), warp-MMA GEMV"),
+    "qkv_m8_8x12288x4096": ("gemv_mma_kernel", ["k_gemv_mma.cu", "dg_ptx.cuh"],
+                            12288 * 4096 + 8 * 4096 + 8 * 12288 * 2,
+                            "E4M3 8 x 12288 x 4096, warp-MMA GEMV"),
+    "qkv_m16_16x12288x4096": ("gemm_skinny_kernel",
+                              ["k_gemm_skinny.cu", "gemm_common.cuh", "dg_ptx.cuh"],
+                              12288 * 4096 + 16 * 4096 + 16 * 12288 * 2,
+                              "E4M3 16 x 12288 x 4096, split-K tcgen05"),
+}
+
+
+def record_traffic(pairs):
+    """`--record-traffic workload=csv ...`: writes profiles/traffic.json from
+    the CSV logs of one-pass ncu captures (dram__bytes_read.sum,
+    dram__bytes_write.sum, gpu__time_duration.sum) of `--kernel workload`,
+    with the hash of the sources each was taken on."""
+    import csv
+    out = {"note": "one captured launch per workload after its warm-up launches; DRAM bytes "
+                   "read + written per launch",
+           "entries": []}
+    for arg in pairs:
+        workload, path = arg.split("=", 1)
+        pattern, sources, algo, desc = TRAFFIC_KERNELS[workload]
+        with open(path) as f:
+            rows = list(csv.reader(line for line in f if not line.startswith("==")))
+        vals = {}
+        for r in rows[1:]:
+            d = dict(zip(rows[0], r))
+            if pattern in d.get("Kernel Name", ""):
+                vals[d["Metric Name"]] = float(d["Metric Value"].replace(",", ""))
+        rd, wr = int(vals["dram__bytes_read.sum"]), int(vals["dram__bytes_write.sum"])
+        out["entries"].append({
+            "workload": workload, "kernel": pattern, "description": desc, "sources": sources,
+            "source_sha256_16": source_hash(sources), "dram_bytes_read": rd, "dram_bytes_write": wr,
+            "dram_bytes_per_launch": rd + wr, "algorithmic_bytes_per_launch": algo,
+            "duration_ns_under_ncu": vals.get("gpu__time_duration.sum"),
+            "command": f"python bench.py --kernel {workload} --steps 2 --warmup 1 && ncu --metrics "
+                       "dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+                       f"--clock-control none -k regex:{pattern} -s 1 -c 1 --csv --log-file "
+                       f"traffic.csv python bench.py --kernel {workload} --steps 2 --warmup 1"})
+    with open(PROFILE_TRAFFIC, "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.record_traffic:
+        record_traffic(args.record_traffic)
+        return
     if args.impl == "reference":
         run_reference(args)
     elif args.kernel:
