@@ -116,7 +116,7 @@ def source_hash(files) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str = WORKLOAD):
+def recorded_traffic(workload: str):
     """DRAM bytes per launch of `workload`'s kernel from the committed ncu
     summary, if it was taken on the kernel's current sources; else None."""
     if not os.path.exists(PROFILE_TRAFFIC):
@@ -720,7 +720,7 @@ def run_own(args):
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     plan = dg.dg_gemm_plan(M, N, K, dg.DG_E4M3, dg.DG_E4M3)
     achieved = FLOP_PER_STEP / (gemm_ms * 1e-3) / 1e12
-    traffic = recorded_traffic()
+    traffic = recorded_traffic("fp8_gemm_8192_e4m3out")
     line = {
         "metric": "FP8 GEMM TFLOPS (and GB/s at M=1) on 1 GB300, % of roofline",
         "value": value,
