@@ -106,10 +106,27 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
-// Whole-cluster barrier (every thread of every CTA of the cluster).
+// Whole-cluster barrier (every thread of every CTA of the cluster).  The
+// aligned form: only where every warp is converged (kernel start).
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The same barrier in the non-aligned form, which counts threads one by one:
+// for the end of a kernel, where a warp whose lane 0 ran a role alone may
+// reach it diverged (__syncwarp does not reconverge a warp, and the aligned
+// form is undefined for a diverged warp).
+__device__ __forceinline__ void cluster_sync_all_diverged() {
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// CTA-wide barrier in the non-aligned form (see cluster_sync_all_diverged):
+// every thread of the CTA, arriving one by one.  __syncthreads is the
+// aligned form.
+__device__ __forceinline__ void cta_sync_diverged() {
+    asm volatile("barrier.sync 0;" ::: "memory");
 }
 
 // The shared::cluster address of this CTA's shared object `p` as seen in the

@@ -620,8 +620,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
     }
 
+    // Warps whose lane 0 ran a role alone may arrive diverged: the barrier
+    // before tensor memory is freed is the non-aligned one.
     tc_fence_before_sync();
-    __syncthreads();
+    cta_sync_diverged();
     tc_fence_after_sync();
     if (warp == 2) tmem_dealloc<C::kTmemCols>(tmem_base);
 }

@@ -366,8 +366,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         publish_amax(p, amax_bits);
     }
 
+    // Warps 0 and 1 may arrive diverged (their lane 0 ran a role alone): the
+    // barrier before tensor memory is freed is the non-aligned one.
     tc_fence_before_sync();
-    __syncthreads();
+    cta_sync_diverged();
     tc_fence_after_sync();
     if (warp == 2) tmem_dealloc<C::kTmemCols>(tmem_base);
 }

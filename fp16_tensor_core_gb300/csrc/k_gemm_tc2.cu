@@ -475,14 +475,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         publish_amax(p, amax_bits);
     }
 
+    // Warps 0 and 1 may arrive diverged (their lane 0 ran a role alone), so
+    // the barriers before tensor memory is freed and the CTAs exit are the
+    // non-aligned ones.
     tc_fence_before_sync();
-    __syncwarp();
-    __syncthreads();
+    cta_sync_diverged();
     tc_fence_after_sync();
     if (warp == 2) tmem_dealloc_pair<C::kTmemCols>(tmem_base);
     // No arrival from one CTA may land in the other after it has exited.
-    __syncwarp();
-    cluster_sync_all();
+    cluster_sync_all_diverged();
 }
 
 template <typename Kern>
