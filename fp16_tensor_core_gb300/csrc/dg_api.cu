@@ -89,6 +89,7 @@ Knobs read_knobs() {
     if (const char* e = std::getenv("DG_STAGED_EPI")) k.staged_epilogue = e[0] != '0';
     if (const char* e = std::getenv("DG_SPLIT_TAIL")) k.split_tail = e[0] == '1';
     if (const char* e = std::getenv("DG_EARLY_RELEASE")) k.early_release = e[0] != '0';
+    if (const char* e = std::getenv("DG_SPLITK_ROWS")) k.splitk_rows = e[0] == '1' ? 1 : 0;
     return k;
 }
 
@@ -473,6 +474,11 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
                     L.tail_ws_bytes = splitk_partial_bytes(st->sm_count);
                     L.tail_counts = ws.counts;
                 }
+            }
+            if (plan.path == 4 && plan.block_n < kSkinnyTileRows) {
+                // row ranges: one CTA per range over the whole of K, no
+                // partial tiles, so no workspace
+                return from_cuda(launch_gemm_skinny(L, nullptr, nullptr, kSplitkMaxCols, s));
             }
             if (plan.path == 4) {
                 SplitkWs ws;

@@ -60,6 +60,10 @@ struct Knobs {
     bool staged_epilogue = true;  // DG_STAGED_EPI=0: tiled epilogues store rows directly
     bool split_tail = false;      // DG_SPLIT_TAIL=1: CTA pairs split a partial last wave along K
     bool early_release = true;    // DG_EARLY_RELEASE=0: tiled kernels release the next one at exit
+    // DG_SPLITK_ROWS=1: split-K plans take row ranges (one CTA per
+    // ceil(N / SMs) rows of B over the whole of K, no split, no workspace)
+    // wherever they fit; default 128-row tiles.
+    int splitk_rows = 0;
 };
 const Knobs& knobs();
 

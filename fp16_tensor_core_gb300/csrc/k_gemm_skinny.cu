@@ -33,6 +33,16 @@
 // fit, else four segments' quads at a time from L2; for its last tile, warps
 // 0-3 (done with their own roles) take the odd 16-column chunks.  With at
 // least two CTAs per tile the grid is a whole multiple of the tile count.
+// Row ranges (DG_SPLITK_ROWS=1): when N fits 128 rows per SM, a tile may
+// instead be a range of tile_rows = ceil(N / SMs) rows, one CTA per range
+// over the whole of K (grid = tiles): every SM streams the same share of B
+// with no tile split, so no partial tile, workspace or finishing pass.  TMA
+// loads tile_rows rows of B per K block; the MMA still spans 128 rows, and
+// the accumulator rows past tile_rows (stale shared memory) are never
+// stored.  Measured on GB300 no faster than 128-row tiles at the decode QKV
+// shape (16 x 12288 x 4096: 11.48 against 11.58 us) and much slower for
+// short ranges over a long K (16 x 4096 x 11008, 27 rows per CTA: 22.1
+// against 11.2 us, too few bytes per box in flight), so not the default.
 // Launch overlap: before its
 // dependency wait a CTA prefetches its first ring of B into L2, and right
 // after it the grid lets the next kernel take over SMs as CTAs exit, so the
@@ -105,7 +115,8 @@ struct SkParams {
     uint32_t* amax_out;
     float* partials;       // [2 * gridDim.x][NC / 4][128] float4: column quads
     uint32_t* counts;      // [tiles]
-    int tiles;             // ceil(N / 128)
+    int tiles;             // ceil(N / tile_rows)
+    int tile_rows;         // rows of B per tile: 128, or a row range (<= 128)
     int kblocks;           // ceil(K / BK)
     int prefetch_kblocks;  // B boxes of its range a CTA moves into L2 up front
 };
@@ -257,7 +268,7 @@ __device__ __forceinline__ void finish_chunks(const SkParams& p, uint8_t* smem, 
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = sum[j];
         }
-        if (n < p.N) {
+        if (r < p.tile_rows && n < p.N) {
             const int jn = min(16, p.M - c0);   // rows of A in this chunk
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -338,7 +349,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
         // kernel finishes (a prefetch only moves lines into L2).
         int t = t_begin, kb = kb_begin;
         for (int i = 0; i < p.prefetch_kblocks && i < n_units; ++i) {
-            tma_prefetch_l2_2d(&tmap_w, kb * kBK, t * kRows);
+            tma_prefetch_l2_2d(&tmap_w, kb * kBK, t * p.tile_rows);
             if (++kb == KB) { kb = 0; ++t; }
         }
     }
@@ -356,6 +367,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
         uint32_t issued_phase = 0;
         bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
         bool ok = true;
+        // bytes of one K block: tile_rows rows of B (the box) and NC rows of A
+        const uint32_t kb_bytes = static_cast<uint32_t>(p.tile_rows * kBKBytes + kXBytes);
         int t = t_begin, kb0 = kb_begin;
         for (int64_t left = n_units; left > 0 && ok; ++t, kb0 = 0) {
             const int kb_end = static_cast<int>(min(static_cast<int64_t>(KB), kb0 + left));
@@ -366,12 +379,12 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 if (skip) {
                     skip = false;   // leave this stage unloaded
                 } else {
-                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nk * kKBBytes));
+                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nk) * kb_bytes);
 #pragma unroll
                     for (int i = 0; i < KPS; ++i) {
                         if (i < nk) {
                             tma_load_2d(sW + stage * C::kStageW + i * kWBytes, &tmap_w, &full[stage],
-                                        (kb + i) * kBK, t * kRows);
+                                        (kb + i) * kBK, t * p.tile_rows);
                             tma_load_2d(sX + stage * C::kStageX + i * kXBytes, &tmap_x, &full[stage],
                                         (kb + i) * kBK, 0);
                         }
@@ -467,7 +480,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
             // only chunks that hold rows of A (c0 < M) are read.
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                   static_cast<uint32_t>(acc * NC);
-            const int n = t * kRows + r;
+            const int n = t * p.tile_rows + r;
             float first[16];   // chunk 0, kept from the partial pass
             bool finish = true;
             int my_slot = 0;
@@ -605,7 +618,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     const int quads = (min(p.M, NC) + 3) >> 2;
                     const float none[16] = {};   // chunk 0 is not among the odd ones
                     uint32_t amax_bits = 0u;
-                    finish_chunks<NC>(p, smem, tacc, r, t * kRows + r, 16, 32,
+                    finish_chunks<NC>(p, smem, tacc, r, t * p.tile_rows + r, 16, 32,
                                       static_cast<int>(blockIdx.x), c_first, c_last, first_slot,
                                       staged, quads, none, alpha, amax_bits);
                     if (p.amax_out != nullptr) {
@@ -656,7 +669,9 @@ cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cuda
         }
     }
     CUtensorMap tw, tx;
-    if (!make_map(&tw, L.B, L.N, L.K, kFp16In, kRows) || !make_map(&tx, L.A, L.M, L.K, kFp16In, NC))
+    const int tile_rows = L.plan->block_n;
+    if (!make_map(&tw, L.B, L.N, L.K, kFp16In, tile_rows) ||
+        !make_map(&tx, L.A, L.M, L.K, kFp16In, NC))
         return cudaErrorInvalidValue;
     SkParams prm;
     prm.D = L.D;
@@ -674,6 +689,7 @@ cudaError_t launch_sk(const TcLaunch& L, float* partials, uint32_t* counts, cuda
     prm.partials = partials;
     prm.counts = counts;
     prm.tiles = L.plan->tiles;
+    prm.tile_rows = tile_rows;
     const int bk = kFp16In ? 64 : 128;
     prm.kblocks = (L.K + bk - 1) / bk;
     prm.prefetch_kblocks = splitk_prefetch_kblocks(C::kRing);
@@ -724,6 +740,16 @@ void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg
     p->block_n = kRows;
     p->block_k = bk;
     p->stages = ring_kblocks(nc) / splitk_kps();
+    // Row ranges (see the file comment): N within 128 rows per SM.
+    const int64_t range = (N + sm_count - 1) / sm_count;
+    const int rows_knob = knobs().splitk_rows;
+    if (range <= kRows && knobs().splitk_grid == 0 && rows_knob == 1) {
+        p->block_n = static_cast<int>(range);
+        p->tiles = static_cast<int>((N + range - 1) / range);
+        p->grid = p->tiles;
+        p->smem_bytes = smem_for_nc(nc);
+        return;
+    }
     p->tiles = static_cast<int>(tiles);
     // With room for at least two CTAs per tile, launch a whole multiple of
     // the tile count, so every CTA covers the same fraction of one tile (one
@@ -740,8 +766,14 @@ void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg
 
 cudaError_t launch_gemm_skinny(const TcLaunch& L, float* partials, uint32_t* counts, int max_cols,
                                cudaStream_t s) {
-    if (L.M < 1 || L.M > kSplitkMaxCols || nc_for(L.M) > max_cols ||
-        L.plan->tiles > kSkinnyMaxTiles || partials == nullptr || counts == nullptr)
+    const int rows = L.plan->block_n;
+    if (L.M < 1 || L.M > kSplitkMaxCols || nc_for(L.M) > max_cols || rows < 1 || rows > kRows ||
+        L.plan->tiles > kSkinnyMaxTiles ||
+        static_cast<int64_t>(L.plan->tiles) * rows < L.N)
+        return cudaErrorInvalidValue;
+    // 128-row tiles may be split over CTAs (workspace needed); row ranges are
+    // one CTA each (grid = tiles), never split.
+    if (rows == kRows ? (partials == nullptr || counts == nullptr) : L.plan->grid != L.plan->tiles)
         return cudaErrorInvalidValue;
     return L.fp16_in ? launch_in<true>(L, partials, counts, s)
                      : launch_in<false>(L, partials, counts, s);

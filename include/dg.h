@@ -293,7 +293,10 @@ typedef struct {
                        M <= 128 where it is estimated faster (operands
                        swapped: block_m = 16, 32, 64 or 128 padded rows of
                        A, block_n = 128 rows of B per tile, K blocks of all
-                       tiles spread over grid CTAs), 5 warp-MMA GEMV for
+                       tiles spread over grid CTAs; with DG_SPLITK_ROWS=1
+                       and N <= 128 x SMs, block_n = ceil(N / SMs) rows of
+                       B per CTA over the whole of K, grid = tiles, no
+                       workspace), 5 warp-MMA GEMV for
                        M <= 16 (block_n = 16 rows of B per CTA, the K sum
                        split over `stages` warps, block_k = K elements per
                        warp step)                                           */

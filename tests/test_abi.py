@@ -259,9 +259,33 @@ def test_plan_decode_shapes_default_to_warp_mma(L):
 
 def test_plan_paths_and_tiles(L):
     """The CUDA-core GEMV, split-K and tiled choices, with the warp-MMA GEMV
-    turned off (the kernels stay selectable and are tested on their own)."""
-    with knobs(DG_MMA_GEMV="0"):
+    and split-K row ranges turned off (the kernels stay selectable and are
+    tested on their own)."""
+    with knobs(DG_MMA_GEMV="0", DG_SPLITK_ROWS="0"):
         _plan_paths_and_tiles(152)
+
+
+def test_plan_splitk_row_ranges(L):
+    """With DG_SPLITK_ROWS=1, split-K plans with N within 128 rows per SM
+    take row ranges: ceil(N / SMs) rows of B per CTA over the whole of K, one
+    CTA per range (grid = tiles); wider N keeps 128-row tiles, and so does
+    every plan by default."""
+    sm = 152
+    with knobs(DG_MMA_GEMV="0", DG_SPLITK_ROWS="1"):
+        for m, n, rows, tiles in ((16, 12288, 81, 152), (3, 12288, 81, 152), (16, 4096, 27, 152),
+                                  (5, 1000, 7, 143), (3, 17, 1, 17), (16, 19456, 128, 152)):
+            p = dg.dg_gemm_plan(m, n, 4096, sm_count=sm)
+            assert p["path"] == 4 and p["block_n"] == rows, (m, n, p)
+            assert p["tiles"] == tiles and p["grid"] == tiles, (m, n, p)
+            assert (tiles - 1) * rows < n <= tiles * rows
+        p = dg.dg_gemm_plan(16, 19457, 4096, sm_count=sm)   # 129 rows per SM: 128-row tiles
+        assert p["path"] == 4 and p["block_n"] == 128 and p["tiles"] == 153
+        p = dg.dg_gemm_plan(64, 4096, 4096, sm_count=sm)
+        assert p["path"] == 4 and p["block_m"] == 64 and p["block_n"] == 27
+        assert p["grid"] == p["tiles"] == 152
+    # the decode default at M = 9..16 (E4M3, large N x K): 128-row split-K tiles
+    p = dg.dg_gemm_plan(16, 12288, 4096, sm_count=sm)
+    assert p["path"] == 4 and p["block_n"] == 128 and p["tiles"] == 96
 
 
 def _plan_paths_and_tiles(sm):
