@@ -88,6 +88,7 @@ Knobs read_knobs() {
         k.mma_gemv_warps = static_cast<int>(v);
     if (const char* e = std::getenv("DG_STAGED_EPI")) k.staged_epilogue = e[0] != '0';
     if (const char* e = std::getenv("DG_SPLIT_TAIL")) k.split_tail = e[0] == '1';
+    if (const char* e = std::getenv("DG_STREAM_K")) k.stream_k = e[0] == '1';
     if (const char* e = std::getenv("DG_EARLY_RELEASE")) k.early_release = e[0] != '0';
     if (const char* e = std::getenv("DG_SPLITK_ROWS")) k.splitk_rows = e[0] == '1' ? 1 : 0;
     return k;
@@ -464,11 +465,13 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
             L.group_off = nullptr;
             L.groups = 0;
             if (plan.path == 5) return from_cuda(launch_gemv_mma(L, s));
-            if (plan.path == 3 && plan.block_m == 256 && knobs().split_tail) {
-                // CTA pairs may split a partial last wave along K through the
-                // stream's split-K workspace (none: the tail runs whole).
+            if (plan.path == 3 && plan.block_m == 256 &&
+                (knobs().split_tail || knobs().stream_k)) {
+                // CTA pairs may split tiles along K through the stream's
+                // split-K workspace (none, e.g. while a new stream is being
+                // captured: every tile runs whole).
                 SplitkWs ws;
-                if (splitk_workspace(st, s, &ws, /*may_allocate=*/false) == DG_OK &&
+                if (splitk_workspace(st, s, &ws, /*may_allocate=*/knobs().stream_k) == DG_OK &&
                     ws.partials != nullptr) {
                     L.tail_ws = ws.partials;
                     L.tail_ws_bytes = splitk_partial_bytes(st->sm_count);

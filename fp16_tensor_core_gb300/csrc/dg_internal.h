@@ -59,6 +59,8 @@ struct Knobs {
     int mma_gemv_warps = 0;     // DG_MMA_GEMV_WARPS (2, 3, 4, 8): warps per CTA of that path
     bool staged_epilogue = true;  // DG_STAGED_EPI=0: tiled epilogues store rows directly
     bool split_tail = false;      // DG_SPLIT_TAIL=1: CTA pairs split a partial last wave along K
+    // DG_STREAM_K=1: CTA pairs take equal ranges of (tile, K block) units
+    bool stream_k = false;
     bool early_release = true;    // DG_EARLY_RELEASE=0: tiled kernels release the next one at exit
     // DG_SPLITK_ROWS=1: split-K plans take row ranges (one CTA per
     // ceil(N / SMs) rows of B over the whole of K, no split, no workspace)

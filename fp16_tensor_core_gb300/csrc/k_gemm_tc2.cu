@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <mutex>
 
 #include "dg_internal.h"
@@ -78,11 +79,26 @@ struct PairCfg {
 };
 
 // One work item of a pair: a tile t and its K blocks [kb0, kb1); part -1 is
-// a whole tile, part s >= 0 the s-th K range of a split tail tile (part 0
+// a whole tile, part s >= 0 the s-th K range of a split tile (part 0
 // finishes the tile: it adds the other parts' partial tiles in part order).
 struct PairItem {
-    int t, kb0, kb1, part, r;   // r: index of a split tile among the tail tiles
+    int t, kb0, kb1, part, r;   // r: index of a split tile (its slots, its counter)
 };
+
+// Params::tail_split value of the stream-K schedule.  The first
+// floor(tiles / pairs) - 1 rounds run whole tiles round-robin, as without it
+// (neighbouring pairs on neighbouring tiles, which share A and B in L2); the
+// (tile, K block) units of the remaining tiles (between one and two rounds'
+// worth) are cut into one equal contiguous range per pair, so every pair
+// ends after the same MMA work.  A tile cut at the boundary between pairs
+// b - 1 and b is split in two (index r = b): pair b runs its later K range
+// first and publishes it, pair b - 1 runs its first K range last and
+// finishes the tile.  Each pair's range spans at least one tile, so no tile
+// is cut twice; the host chooses it only with at least two tiles per pair.
+constexpr int kStreamK = -1;
+
+// K ranges a split tile is cut into under a schedule.
+__host__ __device__ constexpr int parts_of(int split) { return split == kStreamK ? 2 : split; }
 
 // Item i of pair `pair` (false when the pair has no item i).  Without a
 // split tail, tiles pair, pair + npairs, ...; with one (split >= 2), pairs
@@ -96,6 +112,34 @@ __device__ __forceinline__ bool pair_item(int i, int pair, int npairs, int num_t
     it.kb1 = num_kb;
     it.part = -1;
     it.r = 0;
+    if (split == kStreamK) {
+        const int rounds = num_tiles / npairs - 1;   // whole-tile rounds first
+        if (i < rounds) {
+            it.t = pair + i * npairs;
+            return true;
+        }
+        const int base = rounds * npairs;             // first tile of the stream-K part
+        const int64_t units = static_cast<int64_t>(num_tiles - base) * num_kb;
+        const int64_t u0 = static_cast<int64_t>(pair) * units / npairs;
+        const int64_t u1 = static_cast<int64_t>(pair + 1) * units / npairs;
+        const int t0 = static_cast<int>(u0 / num_kb);
+        const int k0 = static_cast<int>(u0 - static_cast<int64_t>(t0) * num_kb);
+        const int t1 = static_cast<int>((u1 - 1) / num_kb);              // last tile touched
+        const int k1 = static_cast<int>(u1 - static_cast<int64_t>(t1) * num_kb);   // its end
+        const int j = i - rounds;
+        if (u1 <= u0 || t0 + j > t1) return false;
+        it.t = base + t0 + j;
+        if (j == 0 && k0 > 0) {              // later part of the tile cut at u0
+            it.part = 1;
+            it.kb0 = k0;
+            it.r = pair;
+        } else if (t0 + j == t1 && k1 < num_kb) {   // first part of the tile cut at u1
+            it.part = 0;
+            it.kb1 = k1;
+            it.r = pair + 1;
+        }
+        return true;
+    }
     if (split < 2) {
         it.t = pair + i * npairs;
         return it.t < num_tiles;
@@ -288,8 +332,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         static_assert(STAGES * C::kStageBytes >= kSlotBytes + 4 * (BN / 32) * kBoxBytes,
                       "a partial tile and every output box of a tile fit in the ring");
         // every other part's partial tile fits in the idle ring: staged loads
+        const int nparts = parts_of(p.tail_split);   // K ranges of a split tile
         const bool staged_parts =
-            static_cast<int64_t>(p.tail_split - 1) * kSlotBytes <= STAGES * C::kStageBytes;
+            static_cast<int64_t>(nparts - 1) * kSlotBytes <= STAGES * C::kStageBytes;
         PairItem it;
         for (int i = 0; pair_item(i, pair, npairs, num_tiles, num_kb, p.tail_split, it); ++i) {
             int mt, nt;
@@ -314,7 +359,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // ([BN / 4][128] float4: a warp's 32 rows are one 512-byte run).
             auto slot_of = [&](int s) {
                 return reinterpret_cast<float4*>(p.tail_ws) +
-                       static_cast<int64_t>((it.r * (p.tail_split - 1) + s - 1) * 2 +
+                       static_cast<int64_t>((it.r * (nparts - 1) + s - 1) * 2 +
                                             static_cast<int>(rank)) * kSlotF4;
             };
             uint32_t* const counter = p.tail_counts + it.r * 2 + static_cast<int>(rank);
@@ -347,7 +392,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 // other parts have published theirs.
                 bool arrived = true;
                 if (threadIdx.x == 128) {
-                    const uint32_t want = static_cast<uint32_t>(p.tail_split - 1);
+                    const uint32_t want = static_cast<uint32_t>(nparts - 1);
                     const uint64_t t0 = global_timer_ns();
                     while (ld_acquire_gpu(counter) < want) {
                         if (*ctl.abort_flag || global_timer_ns() - t0 > ctl.timeout_ns) {
@@ -364,9 +409,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     // part order, on one barrier (used once per CTA)
                     if (threadIdx.x == 128) {
                         fence_proxy_async_global();
-                        mbar_arrive_expect_tx(fix_bar, static_cast<uint32_t>(p.tail_split - 1) *
+                        mbar_arrive_expect_tx(fix_bar, static_cast<uint32_t>(nparts - 1) *
                                                            kSlotBytes);
-                        for (int s2 = 1; s2 < p.tail_split; ++s2)
+                        for (int s2 = 1; s2 < nparts; ++s2)
                             for (int piece = 0; piece < kSlotBytes; piece += kCopyPiece)
                                 bulk_load_g2s(smem + (s2 - 1) * kSlotBytes + piece,
                                               reinterpret_cast<const uint8_t*>(slot_of(s2)) + piece,
@@ -381,7 +426,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // the first part's accumulator, from the ring when staged.
             auto add_parts = [&](int c, uint32_t (&r)[32]) {
                 if (it.part != 0) return;
-                for (int s = 1; s < p.tail_split; ++s) {
+                for (int s = 1; s < nparts; ++s) {
                     const float4* w = staged_parts
                         ? reinterpret_cast<const float4*>(smem + (s - 1) * kSlotBytes)
                         : slot_of(s);
@@ -407,7 +452,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 // box has a place of its own in the ring (after any staged
                 // partial tiles), so the stores go out back to back.
                 const int ring_base = (it.part == 0 && staged_parts)
-                                          ? (p.tail_split - 1) * kSlotBytes : 0;
+                                          ? (nparts - 1) * kSlotBytes : 0;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
@@ -554,7 +599,22 @@ cudaError_t launch_pair_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s
     // workspace holds their partial tiles.
     const int pairs = L.plan->tiles < clusters ? L.plan->tiles : clusters;
     prm2.tail_split = 1;
-    if (knobs().split_tail && L.tail_ws != nullptr && L.tail_counts != nullptr && pairs > 0) {
+    // Stream-K: equal ranges of (tile, K block) units per pair, when every
+    // pair covers at least two tiles' worth (a tile is cut at most once), the
+    // tiles do not already divide evenly, and the workspace holds a partial
+    // tile per boundary and CTA.
+    const int64_t sk_need = static_cast<int64_t>(2) * pairs * BN * kHalfBM * sizeof(float);
+    if (knobs().stream_k && L.tail_ws != nullptr && L.tail_counts != nullptr && pairs > 0 &&
+        L.plan->tiles >= 2 * pairs && L.plan->tiles % pairs != 0 &&
+        sk_need <= static_cast<int64_t>(L.tail_ws_bytes) && 2 * pairs <= kSkinnyMaxTiles) {
+        prm2.tail_split = kStreamK;
+        prm2.tail_ws = L.tail_ws;
+        prm2.tail_counts = L.tail_counts;
+        if (knobs().log)
+            std::fprintf(stderr, "[dg] pair GEMM %dx%dx%d: stream-K over %d pairs, %d tiles\n",
+                         L.M, L.N, L.K, pairs, L.plan->tiles);
+    } else if (knobs().split_tail && L.tail_ws != nullptr && L.tail_counts != nullptr &&
+               pairs > 0) {
         const int rem = L.plan->tiles % pairs;
         const int num_kb = (L.K + C::kBK - 1) / C::kBK;
         int split = rem > 0 ? pairs / rem : 0;
