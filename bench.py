@@ -850,14 +850,20 @@ TRAFFIC_KERNELS = {
 
 
 def record_traffic(pairs):
-    """`--record-traffic workload=csv ...`: writes profiles/traffic.json from
-    the CSV logs of one-pass ncu captures (dram__bytes_read.sum,
+    """`--record-traffic workload=csv ...`: records in profiles/traffic.json,
+    from the CSV logs of one-pass ncu captures (dram__bytes_read.sum,
     dram__bytes_write.sum, gpu__time_duration.sum) of `--kernel workload`,
-    with the hash of the sources each was taken on."""
+    each workload's DRAM bytes with the hash of the sources it was taken on.
+    Entries of other workloads are kept."""
     import csv
     out = {"note": "one captured launch per workload after its warm-up launches; DRAM bytes "
                    "read + written per launch",
            "entries": []}
+    if os.path.exists(PROFILE_TRAFFIC):
+        with open(PROFILE_TRAFFIC) as f:
+            out["entries"] = json.load(f).get("entries", [])
+    recorded = [arg.split("=", 1)[0] for arg in pairs]
+    out["entries"] = [e for e in out["entries"] if e.get("workload") not in recorded]
     for arg in pairs:
         workload, path = arg.split("=", 1)
         pattern, sources, algo, desc = TRAFFIC_KERNELS[workload]
@@ -878,6 +884,7 @@ def record_traffic(pairs):
                        "dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
                        f"--clock-control none -k regex:{pattern} -s 1 -c 1 --csv --log-file "
                        f"traffic.csv python bench.py --kernel {workload} --steps 2 --warmup 1"})
+    out["entries"].sort(key=lambda e: e["workload"])
     with open(PROFILE_TRAFFIC, "w") as f:
         json.dump(out, f, indent=1)
         f.write("\n")
