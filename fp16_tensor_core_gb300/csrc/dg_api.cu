@@ -91,6 +91,8 @@ Knobs read_knobs() {
     if (const char* e = std::getenv("DG_STREAM_K")) k.stream_k = e[0] == '1';
     if (const char* e = std::getenv("DG_EARLY_RELEASE")) k.early_release = e[0] != '0';
     if (const char* e = std::getenv("DG_SPLITK_ROWS")) k.splitk_rows = e[0] == '1' ? 1 : 0;
+    if (env_int("DG_SPLITK_TILE_ROWS", 16, 128, &v) && v % 8 == 0)
+        k.splitk_tile_rows = static_cast<int>(v);
     return k;
 }
 
@@ -311,7 +313,8 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     // every M <= 128.
     const bool splitk_off = kn.splitk == 0;
     const bool splitk_forced = kn.splitk == 1;
-    const bool splitk_fits = (N + kSkinnyTileRows - 1) / kSkinnyTileRows <= kSkinnyMaxTiles;
+    const int64_t sk_rows = kn.splitk_tile_rows;
+    const bool splitk_fits = (N + sk_rows - 1) / sk_rows <= kSkinnyMaxTiles;
     if (!splitk_off && splitk_fits && M <= kSkinnyMaxM) {
         p->path = 4;
         plan_skinny(M, N, K, fp16_in, sm_count, p);
@@ -478,9 +481,9 @@ dg_status run_gemm(const void* A, const void* B, void* D, int64_t M, int64_t N, 
                     L.tail_counts = ws.counts;
                 }
             }
-            if (plan.path == 4 && plan.block_n < kSkinnyTileRows) {
-                // row ranges: one CTA per range over the whole of K, no
-                // partial tiles, so no workspace
+            if (plan.path == 4 && plan.grid == plan.tiles) {
+                // one CTA per tile (row ranges, or as many tiles as CTAs):
+                // no partial tiles, so no workspace
                 return from_cuda(launch_gemm_skinny(L, nullptr, nullptr, kSplitkMaxCols, s));
             }
             if (plan.path == 4) {

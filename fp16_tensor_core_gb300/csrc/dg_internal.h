@@ -66,6 +66,7 @@ struct Knobs {
     // ceil(N / SMs) rows of B over the whole of K, no split, no workspace)
     // wherever they fit; default 128-row tiles.
     int splitk_rows = 0;
+    int splitk_tile_rows = 128;   // DG_SPLITK_TILE_ROWS=<16..128, multiple of 8> (sweeps)
 };
 const Knobs& knobs();
 

@@ -734,10 +734,13 @@ cudaError_t launch_in(const TcLaunch& L, float* partials, uint32_t* counts, cuda
 void plan_skinny(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_plan* p) {
     const int bk = fp16_in ? 64 : 128;
     const int nc = nc_for(M);
-    const int64_t tiles = (N + kRows - 1) / kRows;
+    // rows of B per tile: 128, or DG_SPLITK_TILE_ROWS (sweeps; the MMA still
+    // spans 128 rows and the rows past the tile are not stored)
+    const int tile_rows = knobs().splitk_tile_rows;
+    const int64_t tiles = (N + tile_rows - 1) / tile_rows;
     const int64_t units = tiles * ((K + bk - 1) / bk);
     p->block_m = nc;
-    p->block_n = kRows;
+    p->block_n = tile_rows;
     p->block_k = bk;
     p->stages = ring_kblocks(nc) / splitk_kps();
     // Row ranges (see the file comment): N within 128 rows per SM.
@@ -771,9 +774,9 @@ cudaError_t launch_gemm_skinny(const TcLaunch& L, float* partials, uint32_t* cou
         L.plan->tiles > kSkinnyMaxTiles ||
         static_cast<int64_t>(L.plan->tiles) * rows < L.N)
         return cudaErrorInvalidValue;
-    // 128-row tiles may be split over CTAs (workspace needed); row ranges are
-    // one CTA each (grid = tiles), never split.
-    if (rows == kRows ? (partials == nullptr || counts == nullptr) : L.plan->grid != L.plan->tiles)
+    // Tiles may be split over CTAs (workspace needed) unless there is one CTA
+    // per tile (grid = tiles: each CTA's range is exactly one tile).
+    if (L.plan->grid != L.plan->tiles && (partials == nullptr || counts == nullptr))
         return cudaErrorInvalidValue;
     return L.fp16_in ? launch_in<true>(L, partials, counts, s)
                      : launch_in<false>(L, partials, counts, s);

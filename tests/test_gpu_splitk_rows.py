@@ -151,3 +151,28 @@ def test_repeatable_and_graph_capture_on_a_fresh_stream():
     torch.cuda.synchronize()
     assert dg.dg_sync_status() == dg.DG_OK
     assert torch.equal(Dg, D0)
+
+
+@pytest.mark.parametrize("rows", ["64", "32"])
+@pytest.mark.parametrize("M,N,K", [(16, 12288, 4096), (5, 1000, 1040), (12, 4096, 11008)])
+def test_short_split_tiles(rows, M, N, K):
+    """Split-K over tiles shorter than 128 rows (DG_SPLITK_TILE_ROWS): tiles
+    split between CTAs whose accumulators hold rows past the tile (stale
+    shared memory), which the finishing pass adds but never stores."""
+    with knobs(DG_SPLITK_ROWS="0", DG_SPLITK_TILE_ROWS=rows):
+        p = dg.dg_gemm_plan(M, N, K)
+        assert p["path"] == 4 and p["block_n"] == int(rows) and p["grid"] != p["tiles"], p
+        qa_ref, qb_ref, sa, sb = _quantised(M, N, K)
+        sat, sbt = _scales(sa, sb)
+        buf, D = guarded(M * N, torch.int16, 0x7FFF)
+        am = scalar()
+        dg.dg_fp8_gemm_amax(dev(qa_ref), dev(qb_ref), D, sat, sbt, None, dg.DG_BF16, am,
+                            M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf, M * N, 0x7FFF)
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N)), R, S, sa, sb)
+    ref = float(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))))
+    i = np.argmax(np.abs(R))
+    tol = 8e-3 * ref + 1e-4 * S.reshape(-1)[i] * float(sa) * float(sb)
+    assert abs(am[0].item() - ref) <= tol, (am[0].item(), ref, tol)
