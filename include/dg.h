@@ -25,7 +25,11 @@
  *            keeps its workspace until dg_release_stream(stream) or exit.
  *            At most 16 streams per device hold an allocated one at a time;
  *            past that, split-K shapes on further streams run on the tiled
- *            tensor-core kernel (no workspace, same tolerance).
+ *            tensor-core kernel (no workspace, same tolerance).  A graph
+ *            captured on a stream refers to that stream's workspace: do not
+ *            replay it concurrently with another replay of itself or with
+ *            split-K work (or DG_SPLIT_TAIL / DG_STREAM_K pair GEMMs) on the
+ *            capturing stream; replays in stream order are fine.
  * Layout.    Dense, row-major, no leading-dimension arguments: A is M x K,
  *            B is N x K (both K contiguous, the "TN" form), D is M x N.
  * Alignment. Every data pointer must be 16-byte aligned, every FP32 device
