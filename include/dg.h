@@ -340,7 +340,40 @@ dg_status dg_release_stream(dg_stream_t stream);
 /* Re-reads the DG_* tuning variables of the environment (tile, path and
  * launch switches used for sweeps and tests).  They are otherwise read
  * once, at the library's first call; no call reads the environment
- * again.  Applies to calls made afterwards. */
+ * again.  Applies to calls made afterwards.  None changes what is
+ * computed, only which kernel and launch shape compute it (the results
+ * stay within the same tolerance; values outside the ranges below are
+ * ignored):
+ *   DG_LOG=1              one stderr line per GEMM call (path and tile)
+ *   DG_PDL=0              no programmatic dependent launch (launch overlap)
+ *   DG_MMA_GEMV=0|1       warp-MMA GEMV off / for every M <= 16 (plan path 5)
+ *   DG_MMA_GEMV_WARPS=n   its warps per CTA (2, 3, 4 or 8)
+ *   DG_GEMV_MAX_M=n       largest M on the CUDA-core GEMV (0..16; default 2)
+ *   DG_GEMV_ROWS=n        its rows of B per CTA at M <= 2 (4, 8 or 16)
+ *   DG_SPLITK=0|1         split-K off / for every M <= 128
+ *   DG_SPLITK_GRID=n      CTAs of a split-K launch
+ *   DG_SPLITK_KPS=1|2     K blocks per split-K pipeline stage (default 2)
+ *   DG_SPLITK_PREFETCH=n  B boxes a split-K CTA moves into L2 before its
+ *                         dependency wait (0..256; default one ring)
+ *   DG_SPLITK_ROWS=1      split-K in row ranges: ceil(N / SMs) rows of B
+ *                         per CTA over the whole of K, no workspace
+ *   DG_SPLITK_TILE_ROWS=n rows of B per split-K tile (16..128, a multiple
+ *                         of 8; default 128)
+ *   DG_2CTA=0|1           CTA pairs off / for every M >= 256
+ *   DG_FORCE_BLOCK_N=n    tile width of the tiled kernels (64..256)
+ *   DG_GROUP_M=n          raster group of M tiles (1..4096)
+ *   DG_ONE_WAVE=0         no one-wave tile rule; DG_ONE_WAVE_KB=n its
+ *                         K-block limit (default 64)
+ *   DG_STAGED_EPI=0       tiled epilogues store rows directly instead of
+ *                         through staging boxes and bulk tensor stores
+ *   DG_EARLY_RELEASE=0    tiled kernels release the next launch at exit
+ *                         instead of once every CTA is on its last tile
+ *   DG_SPLIT_TAIL=1       CTA pairs split the tiles of a partial last
+ *                         round along K over the idle pairs
+ *   DG_STREAM_K=1         CTA pairs run whole-tile rounds, then equal
+ *                         (tile, K block) ranges over the last rounds
+ * DG_SPLIT_TAIL and DG_STREAM_K use the stream's split-K workspace (see
+ * Memory above); without one the tiles run whole. */
 void dg_reload_env(void);
 
 /* Upper bound, in microseconds, on any single in-kernel wait (default
