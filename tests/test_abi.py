@@ -427,3 +427,15 @@ def test_plain_c_client_builds_and_runs(L, tmp_path):
                     src, "-o", str(exe), "-L", lib_dir, "-ldg", f"-Wl,-rpath,{lib_dir}"], check=True)
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0 and "c abi ok" in r.stdout, (r.returncode, r.stdout, r.stderr)
+
+
+def test_tuning_variables_documented():
+    """Every DG_* environment variable the library reads is listed in
+    include/dg.h, and every one listed there is read."""
+    api = open(os.path.join(ROOT, "fp16_tensor_core_gb300", "csrc", "dg_api.cu")).read()
+    read = set(re.findall(r'(?:getenv|env_int)\("(DG_[A-Z0-9_]+)"', api))
+    header = open(os.path.join(ROOT, "include", "dg.h")).read()
+    start = header.index("void dg_reload_env(void);")
+    block = header[header.rindex("/*", 0, start):start]
+    listed = set(re.findall(r"\b(DG_[A-Z0-9_]+)=", block))
+    assert read and read == listed, (sorted(read - listed), sorted(listed - read))
