@@ -231,7 +231,7 @@ class Workload:
         if ev is not None:
             ev[1].record(stream)
 
-    KERNELS_PER_STEP = 9  # 2 x (amax init + amax + scale), 2 x quantise, 1 GEMM
+    KERNELS_PER_STEP = 7  # 2 x (amax init + amax with its scale), 2 x quantise, 1 GEMM
 
 
 def time_kernel(torch, stream, fn, iters: int, warmup: int = 3) -> float:
@@ -749,7 +749,7 @@ def run_own(args):
             "inputs": "FP32 A, B ~ N(0,1) seed 0, resident in HBM; sD from tests/golden/sd_8192.json",
             "l2": "inputs larger than L2 (2 x 268 MB FP32 per step), no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "launch": "9 stream launches per step (graph_replay: the same step as one CUDA-graph replay)",
+            "launch": "7 stream launches per step (graph_replay: the same step as one CUDA-graph replay)",
         },
         "roofline": {
             "bound": "tensor",

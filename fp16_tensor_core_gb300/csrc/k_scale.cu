@@ -36,8 +36,55 @@ __device__ __forceinline__ uint32_t abs_bits4(float4 v) {
     return max(max(abs_bits(v.x), abs_bits(v.y)), max(abs_bits(v.z), abs_bits(v.w)));
 }
 
+// scale = amax / 448 (one IEEE binary32 division), 1 for an all-zero tensor.
+__device__ __forceinline__ float scale_of_amax(float a) {
+    return (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+}
+
+// Power-of-two scale ([FP8-guide] §2.1): the smallest p = 2^e (e >= -149,
+// so p is a binary32 value) with 448 * p >= amax, compared exactly in
+// double; 1 for amax == 0, NaN for NaN, +Inf for +Inf.  Dividing by p is
+// then exact: the quantiser only shifts exponents.
+__device__ __forceinline__ float scale_pow2_of_amax(float a) {
+    float p;
+    if (a != a) {
+        p = a;
+    } else if (a == 0.0f) {
+        p = 1.0f;
+    } else if (a > 3.4028234663852886e38f) {
+        p = a;
+    } else {
+        const int ebits = static_cast<int>((__float_as_uint(a) >> 23) & 0xFFu);
+        int e = ebits == 0 ? -149 : max(-149, ebits - 127 - 10);
+        const double ad = static_cast<double>(a);
+        // 448 * 2^e for e >= -149 is an exact double; at most a few steps.
+        for (int it = 0; it < 400; ++it) {
+            const double pe = __longlong_as_double(static_cast<long long>(e + 1023) << 52);
+            if (448.0 * pe >= ad) break;
+            ++e;
+        }
+        p = static_cast<float>(__longlong_as_double(static_cast<long long>(e + 1023) << 52));
+    }
+    return p;
+}
+
+// Scale from the finished reduction, by the CTA that completes it: each CTA,
+// after its atomicMax, counts its arrival in the scale word (zeroed before
+// the launch); the last one reads the final maximum and writes the scale
+// over the count.  One thread per CTA.
+__device__ __forceinline__ void finish_scale(uint32_t* amax_bits, float* scale_out, bool pow2) {
+    __threadfence();   // this CTA's maximum is visible before its arrival
+    uint32_t* count = reinterpret_cast<uint32_t*>(scale_out);
+    if (atomicAdd(count, 1u) == gridDim.x - 1) {
+        __threadfence();
+        const float a = __uint_as_float(atomicOr(amax_bits, 0u));
+        *scale_out = pow2 ? scale_pow2_of_amax(a) : scale_of_amax(a);
+    }
+}
+
 __global__ void __launch_bounds__(kAmaxThreads)
-amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_bits) {
+amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_bits,
+            float* __restrict__ scale_out, int pow2) {
     pdl_wait();
     const int64_t n4 = n >> 2;
     const float4* x4 = reinterpret_cast<const float4*>(x);
@@ -64,49 +111,28 @@ amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_b
         m = lane < kAmaxThreads / 32 ? partial[lane] : 0u;
         m = __reduce_max_sync(0xFFFFFFFFu, m);
         if (lane == 0 && m != 0u) atomicMax(out_bits, m);
+        if (lane == 0 && scale_out != nullptr) finish_scale(out_bits, scale_out, pow2 != 0);
     }
 }
 
-// Power-of-two scale ([FP8-guide] §2.1): the smallest p = 2^e (e >= -149,
-// so p is a binary32 value) with 448 * p >= amax, compared exactly in
-// double; 1 for amax == 0, NaN for NaN, +Inf for +Inf.  Dividing by p is
-// then exact: the quantiser only shifts exponents.
+// Power-of-two scale from a finished reduction (see scale_pow2_of_amax).
 __global__ void scale_pow2_kernel(const float* __restrict__ amax, float* __restrict__ scale) {
     pdl_wait();
-    const float a = *amax;
-    float p;
-    if (a != a) {
-        p = a;
-    } else if (a == 0.0f) {
-        p = 1.0f;
-    } else if (a > 3.4028234663852886e38f) {
-        p = a;
-    } else {
-        const int ebits = static_cast<int>((__float_as_uint(a) >> 23) & 0xFFu);
-        int e = ebits == 0 ? -149 : max(-149, ebits - 127 - 10);
-        const double ad = static_cast<double>(a);
-        // 448 * 2^e for e >= -149 is an exact double; at most a few steps.
-        for (int it = 0; it < 400; ++it) {
-            const double pe = __longlong_as_double(static_cast<long long>(e + 1023) << 52);
-            if (448.0 * pe >= ad) break;
-            ++e;
-        }
-        p = static_cast<float>(__longlong_as_double(static_cast<long long>(e + 1023) << 52));
-    }
-    *scale = p;
+    *scale = scale_pow2_of_amax(*amax);
 }
 
-// Zeroes the running maximum before the reduction.
-__global__ void amax_init_kernel(uint32_t* __restrict__ out_bits) {
+// Zeroes the running maximum before the reduction (and the arrival count in
+// the scale word when the reduction's last CTA writes the scale).
+__global__ void amax_init_kernel(uint32_t* __restrict__ out_bits, uint32_t* __restrict__ count) {
     pdl_wait();
     *out_bits = 0u;
+    if (count != nullptr) *count = 0u;
 }
 
-// scale = amax / 448 (one IEEE binary32 division), 1 for an all-zero tensor.
+// scale = amax / 448 from a finished reduction (see scale_of_amax).
 __global__ void scale_kernel(const float* __restrict__ amax, float* __restrict__ scale) {
     pdl_wait();
-    const float a = *amax;
-    *scale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+    *scale = scale_of_amax(*amax);
 }
 
 __device__ __forceinline__ uint32_t quant4(float4 v, float s) {
@@ -123,7 +149,8 @@ __device__ __forceinline__ uint32_t quant4(float4 v, float s) {
 template <bool kAmax>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict__ scale_p,
-                uint8_t* __restrict__ q, uint32_t* __restrict__ amax_bits) {
+                uint8_t* __restrict__ q, uint32_t* __restrict__ amax_bits,
+                float* __restrict__ next_scale) {
     pdl_wait();
     const float s = *scale_p;
     const int lane = threadIdx.x & 31;
@@ -164,6 +191,7 @@ quantize_kernel(const float* __restrict__ x, int64_t n, const float* __restrict_
             m = lane < kQuantThreads / 32 ? partial[lane] : 0u;
             m = __reduce_max_sync(0xFFFFFFFFu, m);
             if (lane == 0 && m != 0u) atomicMax(amax_bits, m);
+            if (lane == 0 && next_scale != nullptr) finish_scale(amax_bits, next_scale, false);
         }
     }
 }
@@ -276,7 +304,8 @@ cudaError_t launch_convert_f16(const float* x, int64_t n, const float* factor, u
 cudaError_t launch_convert_f16_amax(const float* x, int64_t n, const float* factor, uint16_t* out,
                                     float* amax_out, int sm_count, cudaStream_t s) {
     uint32_t* bits = reinterpret_cast<uint32_t*>(amax_out);
-    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits,
+                                  static_cast<uint32_t*>(nullptr));
     if (e != cudaSuccess || n <= 0) return e;
     const int64_t blocks = slab_grid(n, sm_count);
     return launch_kernel(convert_f16_kernel<true>, dim3(static_cast<unsigned>(blocks)),
@@ -286,7 +315,11 @@ cudaError_t launch_convert_f16_amax(const float* x, int64_t n, const float* fact
 cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
                         int sm_count, cudaStream_t s, bool pow2) {
     uint32_t* bits = reinterpret_cast<uint32_t*>(amax_out);
-    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
+    // The reduction's last CTA writes the scale (two launches, not three)
+    // unless there is no reduction or the scale and amax words coincide.
+    float* fold = (n > 0 && scale_out != nullptr && scale_out != amax_out) ? scale_out : nullptr;
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits,
+                                  reinterpret_cast<uint32_t*>(fold));
     if (e != cudaSuccess) return e;
     if (n > 0) {
         const int64_t n4 = (n + 3) >> 2;
@@ -295,16 +328,18 @@ cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
         e = launch_kernel(amax_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kAmaxThreads), 0, s,
-                          x, n, bits);
+                          x, n, bits, fold, pow2 ? 1 : 0);
         if (e != cudaSuccess) return e;
     }
-    if (scale_out) e = launch_kernel(pow2 ? scale_pow2_kernel : scale_kernel, dim3(1), dim3(1), 0, s,
-                                     static_cast<const float*>(amax_out), scale_out);
+    if (scale_out != nullptr && fold == nullptr)
+        e = launch_kernel(pow2 ? scale_pow2_kernel : scale_kernel, dim3(1), dim3(1), 0, s,
+                          static_cast<const float*>(amax_out), scale_out);
     return e;
 }
 
 cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s) {
-    return launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
+    return launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits,
+                         static_cast<uint32_t*>(nullptr));
 }
 
 cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_t* q,
@@ -312,22 +347,29 @@ cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale, 
     if (n <= 0) return cudaSuccess;
     const int64_t blocks = slab_grid(n, sm_count);
     return launch_kernel(quantize_kernel<false>, dim3(static_cast<unsigned>(blocks)),
-                         dim3(kQuantThreads), 0, s, x, n, scale, q, static_cast<uint32_t*>(nullptr));
+                         dim3(kQuantThreads), 0, s, x, n, scale, q, static_cast<uint32_t*>(nullptr),
+                         static_cast<float*>(nullptr));
 }
 
 cudaError_t launch_quantize_e4m3_amax(const float* x, int64_t n, const float* scale, uint8_t* q,
                                       float* amax_out, float* next_scale_out, int sm_count,
                                       cudaStream_t s) {
     uint32_t* bits = reinterpret_cast<uint32_t*>(amax_out);
-    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits);
+    // The pass's last CTA writes the next scale (two launches, not three)
+    // unless the next scale overwrites the scale this pass reads (in place)
+    // or the amax word.
+    float* fold = (n > 0 && next_scale_out != nullptr && next_scale_out != scale &&
+                   next_scale_out != amax_out) ? next_scale_out : nullptr;
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits,
+                                  reinterpret_cast<uint32_t*>(fold));
     if (e != cudaSuccess) return e;
     if (n > 0) {
         const int64_t blocks = slab_grid(n, sm_count);
         e = launch_kernel(quantize_kernel<true>, dim3(static_cast<unsigned>(blocks)),
-                          dim3(kQuantThreads), 0, s, x, n, scale, q, bits);
+                          dim3(kQuantThreads), 0, s, x, n, scale, q, bits, fold);
         if (e != cudaSuccess) return e;
     }
-    if (next_scale_out != nullptr)
+    if (next_scale_out != nullptr && fold == nullptr)
         e = launch_kernel(scale_kernel, dim3(1), dim3(1), 0, s,
                           static_cast<const float*>(amax_out), next_scale_out);
     return e;

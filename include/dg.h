@@ -82,9 +82,12 @@ typedef enum {
  *              n == 0.
  *   scale_out  FP32[1], device, may be NULL: amax / 448 as one binary32
  *              division, or 1 when amax == 0.
- * Three kernel launches on the stream: a one-thread kernel that zeroes
- * amax_out, the reduction, and (when scale_out is set) a one-thread kernel
- * that forms the scale. */
+ * Two kernel launches on the stream: a one-thread kernel that zeroes
+ * amax_out (and scale_out, which counts the reduction's CTAs until the
+ * last one writes the scale over the count), and the reduction.  When
+ * n == 0 or scale_out == amax_out, a third one-thread kernel forms the
+ * scale after the reduction instead.  scale_out holds no scale while the
+ * call runs. */
 dg_status dg_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
                   dg_stream_t stream);
 
@@ -192,9 +195,10 @@ dg_status dg_fp8_gemm_grouped(const uint8_t* A, const uint8_t* B, void* D,
  * dg_quantize_e4m3.  [FP8-guide] §3.2: the calibration run records each
  * tensor's largest magnitude and the scale comes from it; here the record
  * of one call scales the next, so amax and quantisation share one read.
- * next_scale_out may be the same buffer as scale (it is written after the
- * quantiser has finished); amax_out must not be scale.  Pointers as
- * dg_quantize_e4m3 and dg_amax. */
+ * next_scale_out may be the same buffer as scale (it is then written by a
+ * one-thread kernel after the pass; otherwise the pass's last CTA writes
+ * it, the word counting the CTAs until then); amax_out must not be scale.
+ * Pointers as dg_quantize_e4m3 and dg_amax. */
 dg_status dg_quantize_e4m3_amax(const float* x, int64_t n, const float* scale,
                                 uint8_t* q, float* amax_out,
                                 float* next_scale_out, dg_stream_t stream);
