@@ -367,6 +367,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
         uint32_t issued_phase = 0;
         bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
         bool ok = true;
+        bool first_lap = true;   // every stage starts free: no wait on the first lap
         // bytes of one K block: tile_rows rows of B (the box) and NC rows of A
         const uint32_t kb_bytes = static_cast<uint32_t>(p.tile_rows * kBKBytes + kXBytes);
         int t = t_begin, kb0 = kb_begin;
@@ -375,7 +376,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
             left -= kb_end - kb0;
             for (int kb = kb0; kb < kb_end; kb += KPS) {
                 const int nk = min(KPS, kb_end - kb);
-                if (!wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
+                if (!first_lap && !wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
                 if (skip) {
                     skip = false;   // leave this stage unloaded
                 } else {
@@ -392,7 +393,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 }
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                if (++stage == kStages) { stage = 0; phase ^= 1u; first_lap = false; }
             }
         }
         // Let every issued copy land before the CTA exits (immediate after a

@@ -137,13 +137,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();   // the prologue above overlaps the preceding kernel's tail
 
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     const int num_m = (p.M + kBM - 1) / kBM;
     const int num_n = (p.N + BN - 1) / BN;
     int num_tiles = num_m * num_n;
     const int num_kb = (p.K + C::kBK - 1) / C::kBK;
+    // The prologue overlaps the preceding kernel's tail; the grouped tile
+    // prefix reads the device offsets, so there the wait comes first, while
+    // the plain kernel forms its first tile before it (below).
+    if constexpr (kGrouped) pdl_wait();
     if constexpr (kGrouped) {
         // Tiles of group g: ceil(M_g / 128) x num_n, numbered group by group.
         // The offsets are validated here; invalid ones store nothing.
@@ -203,6 +206,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
         return T;
     };
+    // The producer's first tile depends only on the launch: formed before the
+    // dependency wait while the preceding kernel drains (the empty asm keeps
+    // it there).
+    Tile T0{};
+    if constexpr (!kGrouped) {
+        if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < num_tiles) {
+            int g0 = 0;
+            T0 = tile_of(static_cast<int>(blockIdx.x), g0);
+            asm volatile("" :: "r"(T0.a_row), "r"(T0.b_row), "r"(T0.row_end), "r"(T0.col0) : "memory");
+        }
+        pdl_wait();
+    }
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
@@ -212,11 +227,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
         uint32_t issued_phase = 0;         // parity of each stage's last load
         bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
         bool ok = true;
+        bool first_lap = true;   // every stage starts free: no wait on the first lap
         int gcur = 0;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const Tile T = tile_of(t, gcur);
+            const Tile T = (!kGrouped && t == static_cast<int>(blockIdx.x)) ? T0 : tile_of(t, gcur);
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
+                if (!first_lap && !wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
                 if (skip) {
                     skip = false;           // leave this stage unloaded
                 } else {
@@ -226,7 +242,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 }
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; first_lap = false; }
             }
         }
         // Every load this thread issued must have landed before the CTA can

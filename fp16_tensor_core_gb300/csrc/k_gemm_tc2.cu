@@ -225,7 +225,6 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     cluster_sync_all();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();
 
     const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
     const int num_m = (p.M + kPairBM - 1) / kPairBM;
@@ -233,6 +232,22 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int num_tiles = num_m * num_n;
     const int num_kb = (p.K + C::kBK - 1) / C::kBK;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    // The producer's first item, its tile and the even CTA's barrier address
+    // depend only on the launch: they are formed before the dependency wait,
+    // while the preceding kernel drains (after it they took ~0.5 us of the
+    // launch's critical path); the empty asm keeps them there.
+    PairItem it0{};
+    bool have0 = false;
+    int mt0 = 0, nt0 = 0;
+    uint32_t leader_full = 0;
+    if (warp == 0 && lane == 0) {
+        leader_full = map_to_rank(full, 0);
+        have0 = pair_item(0, pair, npairs, num_tiles, num_kb, p.tail_split, it0);
+        if (have0) tile_coords(it0.t, num_m, num_n, p.group_m, mt0, nt0);
+        asm volatile("" :: "r"(leader_full), "r"(mt0), "r"(nt0), "r"(it0.kb0), "r"(it0.kb1),
+                     "r"(have0 ? 1 : 0) : "memory");
+    }
+    pdl_wait();
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -241,15 +256,17 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         uint32_t issued_mask = 0, issued_phase = 0;
         bool skip = p.skip_first_load != 0 && blockIdx.x == 0;
         bool ok = true;
-        const uint32_t leader_full = map_to_rank(full, 0);
-        PairItem it;
-        for (int i = 0; ok && pair_item(i, pair, npairs, num_tiles, num_kb, p.tail_split, it); ++i) {
-            int mt, nt;
-            tile_coords(it.t, num_m, num_n, p.group_m, mt, nt);
+        bool first_lap = true;   // every stage starts free: no wait on the first lap
+        PairItem it = it0;
+        for (int i = 0;
+             ok && (i == 0 ? have0 : pair_item(i, pair, npairs, num_tiles, num_kb, p.tail_split, it));
+             ++i) {
+            int mt = mt0, nt = nt0;
+            if (i > 0) tile_coords(it.t, num_m, num_n, p.group_m, mt, nt);
             const int a_row = mt * kPairBM + static_cast<int>(rank) * kHalfBM;
             const int b_row = nt * BN + static_cast<int>(rank) * C::kBRows;
             for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                if (!wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
+                if (!first_lap && !wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
                 if (skip) {
                     skip = false;            // leave this stage unloaded
                 } else {
@@ -260,7 +277,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 }
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; first_lap = false; }
             }
         }
         // The even CTA's barriers cover both CTAs' boxes: once every stage it
