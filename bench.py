@@ -423,8 +423,8 @@ def kernel_cases(torch, dg):
         D = torch.empty((S, S), dtype=torch.bfloat16, device=dev)
 
         def fn(i, s):
-            dg.dg_convert_f16_amax(A, A16, f[1:2], am_a, stream=s)
-            dg.dg_convert_f16_amax(B, B16, f[1:2], am_b, stream=s)
+            # both operands converted (and their maxima recorded) in one pass
+            dg.dg_convert_f16_amax_pair(A, B, A16, B16, f[1:2], am_a, am_b, stream=s)
             dg.dg_hgemm_scaled(A16, B16, D, f[2:3], f[3:4], dg.DG_BF16, stream=s)
             dg.dg_fp16_range_scale(am_a, am_b, f, stream=s)
         return fn, 2.0 * S ** 3, 0.0, "tensor_fp16", "FP32 operands 2 x 67 MB (> L2 together with the FP16 copies)"

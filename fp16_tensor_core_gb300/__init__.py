@@ -23,7 +23,7 @@ __all__ = [
     "dg_hgemm", "dg_hgemm_scaled", "dg_fp16_range_scale", "dg_convert_f16",
     "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
     "dg_debug_skip_first_load", "dg_status_string", "dg_version", "dg_release_stream",
-    "dg_reload_env", "dg_convert_f16_amax", "EXPORTED_SYMBOLS",
+    "dg_reload_env", "dg_convert_f16_amax", "dg_convert_f16_amax_pair", "EXPORTED_SYMBOLS",
 ]
 
 DG_OK, DG_ERR_INVALID_VALUE, DG_ERR_MISALIGNED, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_TIMEOUT = range(6)
@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp16_range_scale", "dg_convert_f16", "dg_gemm_plan",
     "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
     "dg_status_string", "dg_version", "dg_release_stream", "dg_reload_env", "dg_convert_f16_amax",
+    "dg_convert_f16_amax_pair",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -87,6 +88,7 @@ def lib():
             L.dg_fp16_range_scale.argtypes = [vp, vp, vp, vp]
             L.dg_convert_f16.argtypes = [vp, i64, vp, vp, vp]
             L.dg_convert_f16_amax.argtypes = [vp, i64, vp, vp, vp, vp]
+            L.dg_convert_f16_amax_pair.argtypes = [vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]
             L.dg_gemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(_Plan)]
             L.dg_init.argtypes = []
@@ -105,7 +107,7 @@ def lib():
                          "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_gemm_plan", "dg_init",
                          "dg_sync_status", "dg_version", "dg_hgemm_scaled", "dg_fp16_range_scale",
                          "dg_convert_f16", "dg_quantize_e4m3_amax", "dg_release_stream",
-                         "dg_convert_f16_amax"):
+                         "dg_convert_f16_amax", "dg_convert_f16_amax_pair"):
                 getattr(L, name).restype = st
             _lib = L
     return _lib
@@ -261,6 +263,13 @@ def dg_convert_f16_amax(x, out, factor, amax_out, stream=None) -> None:
     (the next call's factors come from dg_fp16_range_scale on such maxima)."""
     _check(lib().dg_convert_f16_amax(_ptr(x), x.numel(), _ptr(factor), _ptr(out), _ptr(amax_out),
                                      _stream(stream)), "dg_convert_f16_amax")
+
+
+def dg_convert_f16_amax_pair(a, b, out_a, out_b, factor, amax_a, amax_b, stream=None) -> None:
+    """dg_convert_f16_amax for both HGEMM operands in one pass (one factor)."""
+    _check(lib().dg_convert_f16_amax_pair(_ptr(a), a.numel(), _ptr(b), b.numel(), _ptr(factor),
+                                          _ptr(out_a), _ptr(out_b), _ptr(amax_a), _ptr(amax_b),
+                                          _stream(stream)), "dg_convert_f16_amax_pair")
 
 
 def dg_gemm_plan(M, N, K, in_dtype=DG_E4M3, out_dtype=DG_BF16, sm_count=0) -> dict:

@@ -712,6 +712,26 @@ dg_status dg_convert_f16_amax(const float* x, int64_t n, const float* factor, ui
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dg_status dg_convert_f16_amax_pair(const float* a, int64_t na, const float* b, int64_t nb,
+                                   const float* factor, uint16_t* out_a, uint16_t* out_b,
+                                   float* amax_a, float* amax_b, dg_stream_t stream) {
+    if (na < 0 || nb < 0 || amax_a == nullptr || amax_b == nullptr ||
+        (na > 0 && (a == nullptr || out_a == nullptr)) || (nb > 0 && (b == nullptr || out_b == nullptr)))
+        return DG_ERR_INVALID_VALUE;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(out_a) || !aligned16(out_b) ||
+        !aligned4(factor) || !aligned4(amax_a) || !aligned4(amax_b))
+        return DG_ERR_MISALIGNED;
+    // both words are zeroed before the pass reads the factor, and each
+    // collects one tensor's maximum
+    if (amax_a == amax_b || amax_a == factor || amax_b == factor) return DG_ERR_INVALID_VALUE;
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_convert_f16_amax_pair(a, na, b, nb, factor, out_a, out_b, amax_a, amax_b,
+                                                  st->sm_count,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dg_status dg_gemm_plan(int64_t M, int64_t N, int64_t K, dg_dtype in, dg_dtype out,
                        int sm_count, dg_plan* plan) {
     if (plan == nullptr) return DG_ERR_INVALID_VALUE;

@@ -125,6 +125,10 @@ cudaError_t launch_convert_f16(const float* x, int64_t n, const float* factor, u
 // pass (zeroing kernel first).
 cudaError_t launch_convert_f16_amax(const float* x, int64_t n, const float* factor, uint16_t* out,
                                     float* amax_out, int sm_count, cudaStream_t s);
+cudaError_t launch_convert_f16_amax_pair(const float* a, int64_t na, const float* b, int64_t nb,
+                                         const float* factor, uint16_t* out_a, uint16_t* out_b,
+                                         float* amax_a, float* amax_b, int sm_count,
+                                         cudaStream_t s);
 // Sets *bits = 0 on stream s (one-thread kernel).
 cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s);
 

@@ -275,6 +275,73 @@ convert_f16_kernel(const float* __restrict__ x, int64_t n, const float* __restri
     }
 }
 
+// Both operands of the scaled HGEMM in one launch ([DG-FP16] §3.3 multiplies
+// each by the same factor): the 512-element slabs of a, then of b, are dealt
+// to warps as one sequence (a warp's slab lies wholly in one tensor), each
+// CTA keeps one running max |x| per tensor and adds both to the words;
+// the ragged tails go to blocks 0 and 1 (0 alone for a one-CTA grid).
+__global__ void __launch_bounds__(kQuantThreads)
+convert_f16_pair_kernel(const float* __restrict__ xa, int64_t na, uint16_t* __restrict__ oa,
+                        uint32_t* __restrict__ ma, const float* __restrict__ xb, int64_t nb,
+                        uint16_t* __restrict__ ob, uint32_t* __restrict__ mb,
+                        const float* __restrict__ factor_p) {
+    pdl_wait();
+    const float f = factor_p != nullptr ? *factor_p : 1.0f;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t sa = na >> 9, sb = nb >> 9;
+    uint32_t m_a = 0u, m_b = 0u;
+    for (int64_t slab = warp; slab < sa + sb; slab += nwarps) {
+        const bool in_a = slab < sa;   // the same for the whole warp
+        const float4* x4 = reinterpret_cast<const float4*>(in_a ? xa : xb);
+        uint2* o4 = reinterpret_cast<uint2*>(in_a ? oa : ob);
+        const int64_t b = (in_a ? slab : slab - sa) * 128 + lane;
+        const float4 v0 = ld_stream_f4(x4 + b);
+        const float4 v1 = ld_stream_f4(x4 + b + 32);
+        const float4 v2 = ld_stream_f4(x4 + b + 64);
+        const float4 v3 = ld_stream_f4(x4 + b + 96);
+        o4[b] = half4(v0, f);
+        o4[b + 32] = half4(v1, f);
+        o4[b + 64] = half4(v2, f);
+        o4[b + 96] = half4(v3, f);
+        const uint32_t mm = max(max(abs_bits4(v0), abs_bits4(v1)), max(abs_bits4(v2), abs_bits4(v3)));
+        if (in_a) m_a = max(m_a, mm); else m_b = max(m_b, mm);
+    }
+    const unsigned tail_b = gridDim.x > 1 ? 1u : 0u;
+    if (blockIdx.x == 0) {
+        for (int64_t i = (sa << 9) + threadIdx.x; i < na; i += blockDim.x) {
+            const float v = xa[i];
+            oa[i] = static_cast<uint16_t>(f32x2_to_f16x2(__fmul_rn(v, f), 0.0f) & 0xFFFFu);
+            m_a = max(m_a, abs_bits(v));
+        }
+    }
+    if (blockIdx.x == tail_b) {
+        for (int64_t i = (sb << 9) + threadIdx.x; i < nb; i += blockDim.x) {
+            const float v = xb[i];
+            ob[i] = static_cast<uint16_t>(f32x2_to_f16x2(__fmul_rn(v, f), 0.0f) & 0xFFFFu);
+            m_b = max(m_b, abs_bits(v));
+        }
+    }
+    __shared__ uint32_t part_a[kQuantThreads / 32], part_b[kQuantThreads / 32];
+    m_a = __reduce_max_sync(0xFFFFFFFFu, m_a);
+    m_b = __reduce_max_sync(0xFFFFFFFFu, m_b);
+    const int w = threadIdx.x >> 5;
+    if (lane == 0) {
+        part_a[w] = m_a;
+        part_b[w] = m_b;
+    }
+    __syncthreads();
+    if (w == 0) {
+        m_a = lane < kQuantThreads / 32 ? part_a[lane] : 0u;
+        m_b = lane < kQuantThreads / 32 ? part_b[lane] : 0u;
+        m_a = __reduce_max_sync(0xFFFFFFFFu, m_a);
+        m_b = __reduce_max_sync(0xFFFFFFFFu, m_b);
+        if (lane == 0 && m_a != 0u) atomicMax(ma, m_a);
+        if (lane == 0 && m_b != 0u) atomicMax(mb, m_b);
+    }
+}
+
 // Grid of the slab kernels (quantiser, FP16 conversion): one 512-element
 // slab per warp, at most 8 CTAs of kQuantThreads per SM, at least one CTA.
 int64_t slab_grid(int64_t n, int sm_count) {
@@ -310,6 +377,22 @@ cudaError_t launch_convert_f16_amax(const float* x, int64_t n, const float* fact
     const int64_t blocks = slab_grid(n, sm_count);
     return launch_kernel(convert_f16_kernel<true>, dim3(static_cast<unsigned>(blocks)),
                          dim3(kQuantThreads), 0, s, x, n, factor, out, bits);
+}
+
+cudaError_t launch_convert_f16_amax_pair(const float* a, int64_t na, const float* b, int64_t nb,
+                                         const float* factor, uint16_t* out_a, uint16_t* out_b,
+                                         float* amax_a, float* amax_b, int sm_count,
+                                         cudaStream_t s) {
+    uint32_t* bits_a = reinterpret_cast<uint32_t*>(amax_a);
+    uint32_t* bits_b = reinterpret_cast<uint32_t*>(amax_b);
+    // one one-thread kernel zeroes both maxima (the second word as the
+    // "count" argument, which it also sets to zero)
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits_a, bits_b);
+    if (e != cudaSuccess || na + nb <= 0) return e;
+    const int64_t blocks = slab_grid(na + nb, sm_count);
+    return launch_kernel(convert_f16_pair_kernel, dim3(static_cast<unsigned>(blocks)),
+                         dim3(kQuantThreads), 0, s, a, na, out_a, bits_a, b, nb, out_b, bits_b,
+                         factor);
 }
 
 cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale_out,

@@ -289,6 +289,20 @@ dg_status dg_convert_f16_amax(const float* x, int64_t n, const float* factor,
                               uint16_t* out, float* amax_out,
                               dg_stream_t stream);
 
+/* dg_convert_f16_amax for both operands of the scaled HGEMM in one pass:
+ * out_a[i] = fp16_rn(fl32(a[i] * factor[0])), out_b[i] likewise from b, and
+ * amax_a[0] = max |a|, amax_b[0] = max |b|.  [DG-FP16] §3.3 multiplies both
+ * operands by the same factor (the square root of the range scale); the
+ * next call's factors come from dg_fp16_range_scale(amax_a, amax_b, ...).
+ * Two kernel launches: a one-thread kernel zeroes both maxima, then one
+ * grid converts a and b (half the launches of two dg_convert_f16_amax
+ * calls).  amax_a and amax_b: distinct FP32 device words, 4-byte aligned,
+ * neither the factor word (DG_ERR_INVALID_VALUE).  Other arguments and
+ * errors as dg_convert_f16_amax; na or nb may be 0. */
+dg_status dg_convert_f16_amax_pair(const float* a, int64_t na, const float* b, int64_t nb,
+                                   const float* factor, uint16_t* out_a, uint16_t* out_b,
+                                   float* amax_a, float* amax_b, dg_stream_t stream);
+
 /* Tile / path selection for a GEMM shape, host only (launches nothing).
  * [FP8-guide] §2.2, §3.1, §3.3 (per-shape tile choice, smaller tiles where
  * edge waste is high) and [HGEMM-L2] §3.1-§3.3 (tile and stage count chosen

@@ -193,6 +193,25 @@ def test_convert_f16_amax_argument_errors(L):
     assert c(FAKE, 8, None, FAKE, FAKE + 2, None) == dg.DG_ERR_MISALIGNED
 
 
+def test_convert_f16_amax_pair_argument_errors(L):
+    c = L.dg_convert_f16_amax_pair
+    A, B, F, OA, OB, MA, MB = FAKE, FAKE + 256, FAKE + 512, FAKE + 768, FAKE + 1024, FAKE + 1280, FAKE + 1296
+    assert c(A, -1, B, 8, None, OA, OB, MA, MB, None) == dg.DG_ERR_INVALID_VALUE
+    assert c(A, 8, B, -1, None, OA, OB, MA, MB, None) == dg.DG_ERR_INVALID_VALUE
+    assert c(A, 8, B, 8, None, OA, OB, None, MB, None) == dg.DG_ERR_INVALID_VALUE      # no amax word
+    assert c(A, 8, B, 8, None, OA, OB, MA, None, None) == dg.DG_ERR_INVALID_VALUE
+    assert c(None, 8, B, 8, None, OA, OB, MA, MB, None) == dg.DG_ERR_INVALID_VALUE
+    assert c(A, 8, B, 8, None, OA, None, MA, MB, None) == dg.DG_ERR_INVALID_VALUE
+    assert c(A, 8, B, 8, None, OA, OB, MA, MA, None) == dg.DG_ERR_INVALID_VALUE      # one word for both
+    assert c(A, 8, B, 8, F, OA, OB, F, MB, None) == dg.DG_ERR_INVALID_VALUE          # amax is factor
+    assert c(A, 8, B, 8, F, OA, OB, MA, F, None) == dg.DG_ERR_INVALID_VALUE
+    assert c(A + 4, 8, B, 8, None, OA, OB, MA, MB, None) == dg.DG_ERR_MISALIGNED
+    assert c(A, 8, B + 4, 8, None, OA, OB, MA, MB, None) == dg.DG_ERR_MISALIGNED
+    assert c(A, 8, B, 8, None, OA, OB + 8, MA, MB, None) == dg.DG_ERR_MISALIGNED
+    assert c(A, 8, B, 8, F + 1, OA, OB, MA, MB, None) == dg.DG_ERR_MISALIGNED
+    assert c(A, 8, B, 8, None, OA, OB, MA, MB + 2, None) == dg.DG_ERR_MISALIGNED
+
+
 def test_quantize_amax_argument_errors(L):
     q = L.dg_quantize_e4m3_amax
     assert q(FAKE, 10, None, FAKE, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE    # no scale

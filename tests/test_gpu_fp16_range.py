@@ -128,6 +128,32 @@ def test_convert_with_amax_is_bit_exact(n):
     assert np.float32(am[0].item()).view(np.uint32) == np.float32(oracle.amax(x)).view(np.uint32)
 
 
+@pytest.mark.parametrize("na,nb", [(0, 0), (0, 1000), (511, 0), (100, 77), (4097, (1 << 20) + 7),
+                                   (1 << 20, 1 << 20)])
+def test_convert_pair_is_bit_exact(na, nb):
+    """Both operands in one pass: each tensor's codes and maximum identical to
+    the oracle (and to dg_convert_f16_amax), ragged tails in the same or in
+    different CTAs, empty tensors, stale maxima overwritten."""
+    xa = synth.normal_f32(70 + na % 13, (na,)) * np.float32(500.0)
+    xb = synth.normal_f32(80 + nb % 17, (nb,)) * np.float32(900.0)
+    if na > 10:
+        xa[3] = 8.5e4
+    if nb > 10:
+        xb[nb - 2] = -7.5e4
+    f = scalar()
+    f[0] = 0.61
+    oa = torch.empty(max(na, 1), dtype=torch.int16, device="cuda")[:na]
+    ob = torch.empty(max(nb, 1), dtype=torch.int16, device="cuda")[:nb]
+    ma, mb = scalar(), scalar()
+    ma[0], mb[0] = 3.0e6, 4.0e6   # stale: the call zeroes both first
+    dg.dg_convert_f16_amax_pair(dev(xa), dev(xb), oa, ob, f[0:1], ma, mb)
+    assert dg.dg_sync_status() == dg.DG_OK
+    assert np.array_equal(oa.cpu().numpy().view(np.uint16), oracle.convert_f16(xa, np.float32(0.61)))
+    assert np.array_equal(ob.cpu().numpy().view(np.uint16), oracle.convert_f16(xb, np.float32(0.61)))
+    assert np.float32(ma[0].item()).view(np.uint32) == np.float32(oracle.amax(xa)).view(np.uint32)
+    assert np.float32(mb[0].item()).view(np.uint32) == np.float32(oracle.amax(xb)).view(np.uint32)
+
+
 def test_convert_with_amax_propagates_nan():
     x = synth.normal_f32(3, (5000,))
     x[4321] = np.nan
@@ -138,9 +164,10 @@ def test_convert_with_amax_propagates_nan():
     assert np.isnan(am[0].item())
 
 
+@pytest.mark.parametrize("pair", [False, True])
 @pytest.mark.parametrize("M,N,K,mma", [(2, 300, 512, None), (9, 1000, 1040, "0"), (129, 520, 1040, None),
                                        (384, 1000, 2048, None)])
-def test_recorded_factor_chain(M, N, K, mma):
+def test_recorded_factor_chain(M, N, K, mma, pair):
     """Delayed dynamic-range scaling: each step converts with the factors
     formed from the previous step's maxima, recorded by the conversions
     themselves.  From the second step on (same operands) every factor, FP16
@@ -158,8 +185,11 @@ def test_recorded_factor_chain(M, N, K, mma):
     D = torch.empty((M, N), dtype=torch.int16, device="cuda")
 
     def step():
-        dg.dg_convert_f16_amax(dA, A16, f[1:2], am_a)
-        dg.dg_convert_f16_amax(dB, B16, f[1:2], am_b)
+        if pair:
+            dg.dg_convert_f16_amax_pair(dA, dB, A16, B16, f[1:2], am_a, am_b)
+        else:
+            dg.dg_convert_f16_amax(dA, A16, f[1:2], am_a)
+            dg.dg_convert_f16_amax(dB, B16, f[1:2], am_b)
         dg.dg_hgemm_scaled(A16, B16, D, f[2:3], f[3:4], dg.DG_BF16)
         used = f.clone()
         dg.dg_fp16_range_scale(am_a, am_b, f)      # factors for the next step
