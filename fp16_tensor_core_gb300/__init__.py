@@ -23,7 +23,8 @@ __all__ = [
     "dg_hgemm", "dg_hgemm_scaled", "dg_fp16_range_scale", "dg_convert_f16",
     "dg_gemm_plan", "dg_init", "dg_sync_status", "dg_set_wait_timeout_us",
     "dg_debug_skip_first_load", "dg_status_string", "dg_version", "dg_release_stream",
-    "dg_reload_env", "dg_convert_f16_amax", "dg_convert_f16_amax_pair", "EXPORTED_SYMBOLS",
+    "dg_reload_env", "dg_convert_f16_amax", "dg_convert_f16_amax_pair", "dg_quantize_e4m3_pair",
+    "EXPORTED_SYMBOLS",
 ]
 
 DG_OK, DG_ERR_INVALID_VALUE, DG_ERR_MISALIGNED, DG_ERR_UNSUPPORTED, DG_ERR_CUDA, DG_ERR_TIMEOUT = range(6)
@@ -37,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "dg_fp16_range_scale", "dg_convert_f16", "dg_gemm_plan",
     "dg_init", "dg_sync_status", "dg_set_wait_timeout_us", "dg_debug_skip_first_load",
     "dg_status_string", "dg_version", "dg_release_stream", "dg_reload_env", "dg_convert_f16_amax",
-    "dg_convert_f16_amax_pair",
+    "dg_convert_f16_amax_pair", "dg_quantize_e4m3_pair",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -89,6 +90,7 @@ def lib():
             L.dg_convert_f16.argtypes = [vp, i64, vp, vp, vp]
             L.dg_convert_f16_amax.argtypes = [vp, i64, vp, vp, vp, vp]
             L.dg_convert_f16_amax_pair.argtypes = [vp, i64, vp, i64, vp, vp, vp, vp, vp, vp]
+            L.dg_quantize_e4m3_pair.argtypes = [vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp]
             L.dg_gemm_plan.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(_Plan)]
             L.dg_init.argtypes = []
@@ -107,7 +109,8 @@ def lib():
                          "dg_fp8_gemm_grouped", "dg_fp8_gemm_splitk_static", "dg_gemm_plan", "dg_init",
                          "dg_sync_status", "dg_version", "dg_hgemm_scaled", "dg_fp16_range_scale",
                          "dg_convert_f16", "dg_quantize_e4m3_amax", "dg_release_stream",
-                         "dg_convert_f16_amax", "dg_convert_f16_amax_pair"):
+                         "dg_convert_f16_amax", "dg_convert_f16_amax_pair",
+                         "dg_quantize_e4m3_pair"):
                 getattr(L, name).restype = st
             _lib = L
     return _lib
@@ -168,6 +171,14 @@ def dg_quantize_e4m3(x, scale, q, stream=None) -> None:
         raise ValueError("q must have as many elements as x")
     _check(lib().dg_quantize_e4m3(_ptr(x), x.numel(), _ptr(scale), _ptr(q), _stream(stream)),
            "dg_quantize_e4m3")
+
+
+def dg_quantize_e4m3_pair(a, b, amax_a, amax_b, scale_a, scale_b, qa, qb, stream=None) -> None:
+    """amax, scale and E4M3 codes of both GEMM operands in one call (as
+    dg_amax + dg_quantize_e4m3 on each)."""
+    _check(lib().dg_quantize_e4m3_pair(_ptr(a), a.numel(), _ptr(b), b.numel(), _ptr(amax_a),
+                                       _ptr(amax_b), _ptr(scale_a), _ptr(scale_b), _ptr(qa),
+                                       _ptr(qb), _stream(stream)), "dg_quantize_e4m3_pair")
 
 
 def dg_quantize_e4m3_amax(x, scale, q, amax_out, next_scale_out=None, stream=None) -> None:

@@ -555,6 +555,29 @@ dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dg_status dg_quantize_e4m3_pair(const float* a, int64_t na, const float* b, int64_t nb,
+                                float* amax_a, float* amax_b, float* scale_a, float* scale_b,
+                                uint8_t* qa, uint8_t* qb, dg_stream_t stream) {
+    if (na < 0 || nb < 0 || amax_a == nullptr || amax_b == nullptr || scale_a == nullptr ||
+        scale_b == nullptr || (na > 0 && (a == nullptr || qa == nullptr)) ||
+        (nb > 0 && (b == nullptr || qb == nullptr)))
+        return DG_ERR_INVALID_VALUE;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(qa) || !aligned16(qb) || !aligned4(amax_a) ||
+        !aligned4(amax_b) || !aligned4(scale_a) || !aligned4(scale_b))
+        return DG_ERR_MISALIGNED;
+    // four distinct words: two maxima, two scales (scale_a counts CTAs first)
+    const float* w[4] = {amax_a, amax_b, scale_a, scale_b};
+    for (int i = 0; i < 4; ++i)
+        for (int j = i + 1; j < 4; ++j)
+            if (w[i] == w[j]) return DG_ERR_INVALID_VALUE;
+    DeviceState* st = nullptr;
+    dg_status rc = current_device_state(&st);
+    if (rc != DG_OK) return rc;
+    return from_cuda(launch_quantize_e4m3_pair(a, na, b, nb, amax_a, amax_b, scale_a, scale_b, qa,
+                                               qb, st->sm_count,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dg_status dg_quantize_e4m3_amax(const float* x, int64_t n, const float* scale, uint8_t* q,
                                 float* amax_out, float* next_scale_out, dg_stream_t stream) {
     if (n < 0 || scale == nullptr || amax_out == nullptr ||

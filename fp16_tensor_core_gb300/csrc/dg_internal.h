@@ -129,6 +129,9 @@ cudaError_t launch_convert_f16_amax_pair(const float* a, int64_t na, const float
                                          const float* factor, uint16_t* out_a, uint16_t* out_b,
                                          float* amax_a, float* amax_b, int sm_count,
                                          cudaStream_t s);
+cudaError_t launch_quantize_e4m3_pair(const float* a, int64_t na, const float* b, int64_t nb,
+                                      float* amax_a, float* amax_b, float* scale_a, float* scale_b,
+                                      uint8_t* qa, uint8_t* qb, int sm_count, cudaStream_t s);
 // Sets *bits = 0 on stream s (one-thread kernel).
 cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s);
 

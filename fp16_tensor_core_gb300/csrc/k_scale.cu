@@ -82,10 +82,10 @@ __device__ __forceinline__ void finish_scale(uint32_t* amax_bits, float* scale_o
     }
 }
 
-__global__ void __launch_bounds__(kAmaxThreads)
-amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_bits,
-            float* __restrict__ scale_out, int pow2) {
-    pdl_wait();
+// This thread's max |x| (ordered bits) over its grid-stride share of x; the
+// ragged tail (n mod 4 elements) is read by block `tail_block`.
+__device__ __forceinline__ uint32_t amax_share(const float* __restrict__ x, int64_t n,
+                                               unsigned tail_block) {
     const int64_t n4 = n >> 2;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -99,9 +99,16 @@ amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_b
         m = max(m, max(max(abs_bits4(v0), abs_bits4(v1)), max(abs_bits4(v2), abs_bits4(v3))));
     }
     for (; i < n4; i += stride) m = max(m, abs_bits4(ld_stream_f4(x4 + i)));
-    if (blockIdx.x == 0 && threadIdx.x < static_cast<unsigned>(n & 3))
+    if (blockIdx.x == tail_block && threadIdx.x < static_cast<unsigned>(n & 3))
         m = max(m, abs_bits(x[(n4 << 2) + threadIdx.x]));
+    return m;
+}
 
+__global__ void __launch_bounds__(kAmaxThreads)
+amax_kernel(const float* __restrict__ x, int64_t n, uint32_t* __restrict__ out_bits,
+            float* __restrict__ scale_out, int pow2) {
+    pdl_wait();
+    uint32_t m = amax_share(x, n, 0);
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     __shared__ uint32_t partial[kAmaxThreads / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,10 +130,12 @@ __global__ void scale_pow2_kernel(const float* __restrict__ amax, float* __restr
 
 // Zeroes the running maximum before the reduction (and the arrival count in
 // the scale word when the reduction's last CTA writes the scale).
-__global__ void amax_init_kernel(uint32_t* __restrict__ out_bits, uint32_t* __restrict__ count) {
+__global__ void amax_init_kernel(uint32_t* __restrict__ out_bits, uint32_t* __restrict__ count,
+                                 uint32_t* __restrict__ other) {
     pdl_wait();
     *out_bits = 0u;
     if (count != nullptr) *count = 0u;
+    if (other != nullptr) *other = 0u;
 }
 
 // scale = amax / 448 from a finished reduction (see scale_of_amax).
@@ -140,6 +149,83 @@ __device__ __forceinline__ uint32_t quant4(float4 v, float s) {
     const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s));
     return lo | (hi << 16);
 }
+
+// amax and scale of both GEMM operands in one grid: every thread takes its
+// grid-stride share of a, then of b (so the grid streams on from one tensor
+// to the next without a launch boundary); each CTA adds its two maxima to
+// the words, counts its arrival in scale_a's word (zeroed before), and the
+// last CTA writes both scales, scale_a over the count last.
+__global__ void __launch_bounds__(kAmaxThreads)
+amax_pair_kernel(const float* __restrict__ xa, int64_t na, const float* __restrict__ xb, int64_t nb,
+                 uint32_t* __restrict__ bits_a, uint32_t* __restrict__ bits_b,
+                 float* __restrict__ scale_a, float* __restrict__ scale_b) {
+    pdl_wait();
+    uint32_t ma = amax_share(xa, na, 0);
+    uint32_t mb = amax_share(xb, nb, gridDim.x > 1 ? 1u : 0u);
+    ma = __reduce_max_sync(0xFFFFFFFFu, ma);
+    mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+    __shared__ uint32_t pa[kAmaxThreads / 32], pb[kAmaxThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        pa[warp] = ma;
+        pb[warp] = mb;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        ma = lane < kAmaxThreads / 32 ? pa[lane] : 0u;
+        mb = lane < kAmaxThreads / 32 ? pb[lane] : 0u;
+        ma = __reduce_max_sync(0xFFFFFFFFu, ma);
+        mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+        if (lane == 0) {
+            if (ma != 0u) atomicMax(bits_a, ma);
+            if (mb != 0u) atomicMax(bits_b, mb);
+            __threadfence();   // both maxima visible before the arrival
+            if (atomicAdd(reinterpret_cast<uint32_t*>(scale_a), 1u) == gridDim.x - 1) {
+                __threadfence();
+                *scale_b = scale_of_amax(__uint_as_float(atomicOr(bits_b, 0u)));
+                *scale_a = scale_of_amax(__uint_as_float(atomicOr(bits_a, 0u)));
+            }
+        }
+    }
+}
+
+// Quantisation of both GEMM operands in one grid, each with its own scale:
+// the 512-element slabs of a, then of b, are dealt to warps as one sequence
+// (a warp's slab lies wholly in one tensor); the ragged tails go to blocks 0
+// and 1 (0 alone for a one-CTA grid).
+__global__ void __launch_bounds__(kQuantThreads)
+quantize_pair_kernel(const float* __restrict__ xa, int64_t na, const float* __restrict__ sa_p,
+                     uint8_t* __restrict__ qa, const float* __restrict__ xb, int64_t nb,
+                     const float* __restrict__ sb_p, uint8_t* __restrict__ qb) {
+    pdl_wait();
+    const float sa = *sa_p, sb = *sb_p;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ka = na >> 9, kb = nb >> 9;
+    for (int64_t slab = warp; slab < ka + kb; slab += nwarps) {
+        const bool in_a = slab < ka;   // the same for the whole warp
+        const float4* x4 = reinterpret_cast<const float4*>(in_a ? xa : xb);
+        uint32_t* q4 = reinterpret_cast<uint32_t*>(in_a ? qa : qb);
+        const float s = in_a ? sa : sb;
+        const int64_t b = (in_a ? slab : slab - ka) * 128 + lane;
+        const float4 v0 = ld_stream_f4(x4 + b);
+        const float4 v1 = ld_stream_f4(x4 + b + 32);
+        const float4 v2 = ld_stream_f4(x4 + b + 64);
+        const float4 v3 = ld_stream_f4(x4 + b + 96);
+        q4[b] = quant4(v0, s);
+        q4[b + 32] = quant4(v1, s);
+        q4[b + 64] = quant4(v2, s);
+        q4[b + 96] = quant4(v3, s);
+    }
+    if (blockIdx.x == 0)
+        for (int64_t i = (ka << 9) + threadIdx.x; i < na; i += blockDim.x)
+            qa[i] = static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(xa[i], sa), 0.0f) & 0xFFu);
+    if (blockIdx.x == (gridDim.x > 1 ? 1u : 0u))
+        for (int64_t i = (kb << 9) + threadIdx.x; i < nb; i += blockDim.x)
+            qb[i] = static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(xb[i], sb), 0.0f) & 0xFFu);
+}
+
 
 // Each warp iteration handles 512 consecutive elements: four fully coalesced
 // 512-byte loads (lane j reads float4 j, j+32, j+64, j+96 of the slab) and
@@ -372,7 +458,7 @@ cudaError_t launch_convert_f16_amax(const float* x, int64_t n, const float* fact
                                     float* amax_out, int sm_count, cudaStream_t s) {
     uint32_t* bits = reinterpret_cast<uint32_t*>(amax_out);
     cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits,
-                                  static_cast<uint32_t*>(nullptr));
+                                  static_cast<uint32_t*>(nullptr), static_cast<uint32_t*>(nullptr));
     if (e != cudaSuccess || n <= 0) return e;
     const int64_t blocks = slab_grid(n, sm_count);
     return launch_kernel(convert_f16_kernel<true>, dim3(static_cast<unsigned>(blocks)),
@@ -387,12 +473,35 @@ cudaError_t launch_convert_f16_amax_pair(const float* a, int64_t na, const float
     uint32_t* bits_b = reinterpret_cast<uint32_t*>(amax_b);
     // one one-thread kernel zeroes both maxima (the second word as the
     // "count" argument, which it also sets to zero)
-    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits_a, bits_b);
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits_a, bits_b,
+                                  static_cast<uint32_t*>(nullptr));
     if (e != cudaSuccess || na + nb <= 0) return e;
     const int64_t blocks = slab_grid(na + nb, sm_count);
     return launch_kernel(convert_f16_pair_kernel, dim3(static_cast<unsigned>(blocks)),
                          dim3(kQuantThreads), 0, s, a, na, out_a, bits_a, b, nb, out_b, bits_b,
                          factor);
+}
+
+cudaError_t launch_quantize_e4m3_pair(const float* a, int64_t na, const float* b, int64_t nb,
+                                      float* amax_a, float* amax_b, float* scale_a, float* scale_b,
+                                      uint8_t* qa, uint8_t* qb, int sm_count, cudaStream_t s) {
+    uint32_t* bits_a = reinterpret_cast<uint32_t*>(amax_a);
+    uint32_t* bits_b = reinterpret_cast<uint32_t*>(amax_b);
+    cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits_a, bits_b,
+                                  reinterpret_cast<uint32_t*>(scale_a));
+    if (e != cudaSuccess) return e;
+    const int64_t n4 = ((na + 3) >> 2) + ((nb + 3) >> 2);
+    int64_t blocks = (n4 + kAmaxThreads - 1) / kAmaxThreads;
+    const int64_t cap = static_cast<int64_t>(sm_count) * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    e = launch_kernel(amax_pair_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kAmaxThreads), 0, s,
+                      a, na, b, nb, bits_a, bits_b, scale_a, scale_b);
+    if (e != cudaSuccess || na + nb <= 0) return e;
+    const int64_t qblocks = slab_grid(na + nb, sm_count);
+    return launch_kernel(quantize_pair_kernel, dim3(static_cast<unsigned>(qblocks)),
+                         dim3(kQuantThreads), 0, s, a, na, static_cast<const float*>(scale_a), qa, b,
+                         nb, static_cast<const float*>(scale_b), qb);
 }
 
 cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale_out,
@@ -402,7 +511,7 @@ cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale
     // unless there is no reduction or the scale and amax words coincide.
     float* fold = (n > 0 && scale_out != nullptr && scale_out != amax_out) ? scale_out : nullptr;
     cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits,
-                                  reinterpret_cast<uint32_t*>(fold));
+                                  reinterpret_cast<uint32_t*>(fold), static_cast<uint32_t*>(nullptr));
     if (e != cudaSuccess) return e;
     if (n > 0) {
         const int64_t n4 = (n + 3) >> 2;
@@ -422,7 +531,7 @@ cudaError_t launch_amax(const float* x, int64_t n, float* amax_out, float* scale
 
 cudaError_t launch_zero_word(uint32_t* bits, cudaStream_t s) {
     return launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits,
-                         static_cast<uint32_t*>(nullptr));
+                         static_cast<uint32_t*>(nullptr), static_cast<uint32_t*>(nullptr));
 }
 
 cudaError_t launch_quantize_e4m3(const float* x, int64_t n, const float* scale, uint8_t* q,
@@ -444,7 +553,7 @@ cudaError_t launch_quantize_e4m3_amax(const float* x, int64_t n, const float* sc
     float* fold = (n > 0 && next_scale_out != nullptr && next_scale_out != scale &&
                    next_scale_out != amax_out) ? next_scale_out : nullptr;
     cudaError_t e = launch_kernel(amax_init_kernel, dim3(1), dim3(1), 0, s, bits,
-                                  reinterpret_cast<uint32_t*>(fold));
+                                  reinterpret_cast<uint32_t*>(fold), static_cast<uint32_t*>(nullptr));
     if (e != cudaSuccess) return e;
     if (n > 0) {
         const int64_t blocks = slab_grid(n, sm_count);

@@ -112,6 +112,25 @@ dg_status dg_amax_pow2(const float* x, int64_t n, float* amax_out,
 dg_status dg_quantize_e4m3(const float* x, int64_t n, const float* scale,
                            uint8_t* q, dg_stream_t stream);
 
+/* Both operands of the E4M3 GEMM prepared in one call: amax and scale of a
+ * and of b (as dg_amax), then each quantised with its own scale (as
+ * dg_quantize_e4m3).  [FP8-guide] §3.2 scales each operand by its own
+ * amax / 448 before the GEMM.  Three kernel launches: a one-thread kernel
+ * zeroes the two maxima (and scale_a, which counts the reduction's CTAs
+ * until the last one writes both scales), one grid takes the maxima of a
+ * and then b, one grid quantises a and b.  The results are bit-identical to
+ * dg_amax + dg_quantize_e4m3 on each tensor; the grids stream on from one
+ * tensor to the next without a launch boundary between them.
+ *   a, b          FP32[na], FP32[nb], device, 16-byte aligned (na, nb >= 0)
+ *   amax_a/_b     FP32 device words: max |a|, max |b| (NaN propagates)
+ *   scale_a/_b    FP32 device words: amax / 448, or 1 when amax == 0
+ *   qa, qb        uint8[na], uint8[nb] E4M3 codes, 16-byte aligned
+ * The four words must be distinct and 4-byte aligned (DG_ERR_INVALID_VALUE,
+ * DG_ERR_MISALIGNED). */
+dg_status dg_quantize_e4m3_pair(const float* a, int64_t na, const float* b, int64_t nb,
+                                float* amax_a, float* amax_b, float* scale_a, float* scale_b,
+                                uint8_t* qa, uint8_t* qb, dg_stream_t stream);
+
 /* Per-tensor-scaled E4M3 GEMM.  [FP8-guide] §2.1, §3.2, §3.3:
  *   D[m,n] = out( scale_a * scale_b * sum_k A[m,k] * B[n,k] )
  * with FP8 inputs, FP32 accumulation and the scales applied once to the

@@ -212,6 +212,28 @@ def test_convert_f16_amax_pair_argument_errors(L):
     assert c(A, 8, B, 8, None, OA, OB, MA, MB + 2, None) == dg.DG_ERR_MISALIGNED
 
 
+def test_quantize_pair_argument_errors(L):
+    q = L.dg_quantize_e4m3_pair
+    A, B, QA, QB = FAKE, FAKE + 256, FAKE + 512, FAKE + 768
+    W = [FAKE + 1024 + 16 * i for i in range(4)]
+    assert q(A, -1, B, 8, *W, QA, QB, None) == dg.DG_ERR_INVALID_VALUE
+    assert q(A, 8, B, -1, *W, QA, QB, None) == dg.DG_ERR_INVALID_VALUE
+    for k in range(4):                                       # each word required
+        w = list(W)
+        w[k] = None
+        assert q(A, 8, B, 8, *w, QA, QB, None) == dg.DG_ERR_INVALID_VALUE
+    assert q(None, 8, B, 8, *W, QA, QB, None) == dg.DG_ERR_INVALID_VALUE
+    assert q(A, 8, B, 8, *W, QA, None, None) == dg.DG_ERR_INVALID_VALUE
+    for i in range(4):                                       # the four words distinct
+        for j in range(i + 1, 4):
+            w = list(W)
+            w[j] = w[i]
+            assert q(A, 8, B, 8, *w, QA, QB, None) == dg.DG_ERR_INVALID_VALUE, (i, j)
+    assert q(A + 4, 8, B, 8, *W, QA, QB, None) == dg.DG_ERR_MISALIGNED
+    assert q(A, 8, B, 8, *W, QA, QB + 4, None) == dg.DG_ERR_MISALIGNED
+    assert q(A, 8, B, 8, W[0] + 2, *W[1:], QA, QB, None) == dg.DG_ERR_MISALIGNED
+
+
 def test_quantize_amax_argument_errors(L):
     q = L.dg_quantize_e4m3_amax
     assert q(FAKE, 10, None, FAKE, FAKE, None, None) == dg.DG_ERR_INVALID_VALUE    # no scale
