@@ -236,7 +236,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (skip) {
                     skip = false;           // leave this stage unloaded
                 } else {
-                    mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                    mbar_arrive_expect_tx(&full[stage], p.a_box_bytes + C::kBBytes);
                     tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kb * C::kBK, T.a_row);
                     tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kb * C::kBK, T.b_row);
                     issued_mask |= 1u << stage;
@@ -412,9 +412,20 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     }
     CUtensorMap ta, tb, td;
     const int b_rows = kGrouped ? L.N * L.groups : L.N;   // grouped: B is (G*N) x K
-    if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kBM) || !make_map(&tb, L.B, b_rows, L.K, kFp16In, BN))
+    // A box rows: M rounded up to 8 when A has at most 32 rows, else 128.
+    // A 128-row box over so short a tensor slows every load (17 x 11008 x
+    // 4096 E4M3: 17.3 us against 12.5 with a 24-row box; M = 32 runs 12.5
+    // with either).  DG_TC_A_BOX=0 keeps 128 rows, =2 narrows every A of
+    // fewer than 128 rows (sweeps).
+    int a_rows = kBM;
+    const int a_box = knobs().tc_a_box;
+    if (!kGrouped && ((a_box == 1 && L.M <= 32) || (a_box == 2 && L.M < kBM)))
+        a_rows = (L.M + 7) / 8 * 8;
+    if (!make_map(&ta, L.A, L.M, L.K, kFp16In, a_rows) ||
+        !make_map(&tb, L.B, b_rows, L.K, kFp16In, BN))
         return cudaErrorInvalidValue;
     Params prm2 = prm;
+    prm2.a_box_bytes = a_rows * kBKBytes;
     // Output map of the staged epilogue (else the epilogue stores directly).
     if (!prm2.staged || !make_out_map(&td, L)) {
         prm2.staged = 0;
@@ -428,6 +439,7 @@ template <bool kFp16In>
 cudaError_t launch_in(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     switch (L.plan->block_n) {
         case 64: return launch_cfg<64, stages_for(64), kFp16In>(L, prm, s);
+        case 96: return launch_cfg<96, stages_for(96), kFp16In>(L, prm, s);
         case 128: return launch_cfg<128, stages_for(128), kFp16In>(L, prm, s);
         case 160: return launch_cfg<160, stages_for(160), kFp16In>(L, prm, s);
         case 192: return launch_cfg<192, stages_for(192), kFp16In>(L, prm, s);
@@ -439,6 +451,7 @@ cudaError_t launch_in(const TcLaunch& L, const Params& prm, cudaStream_t s) {
 int smem_for(int bn) {
     switch (bn) {
         case 64: return Cfg<64, stages_for(64), false>::kSmemBytes;
+        case 96: return Cfg<96, stages_for(96), false>::kSmemBytes;
         case 128: return Cfg<128, stages_for(128), false>::kSmemBytes;
         case 160: return Cfg<160, stages_for(160), false>::kSmemBytes;
         case 192: return Cfg<192, stages_for(192), false>::kSmemBytes;
@@ -461,12 +474,15 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     // for BN/2 cycles, so narrow tiles need more shared-memory bandwidth per
     // flop (8192/BN + 64 B/clk).  Measured on GB300 (8192^3 E4M3): BN 256 ->
     // 1.0, 128 -> 0.72, 64 -> 0.36; the widths in between are interpolated
-    // along that demand curve.
-    const int cand[6] = {256, 224, 192, 160, 128, 64};
-    const double eff[6] = {1.0, 0.95, 0.88, 0.80, 0.72, 0.36};
+    // along that demand curve.  The 96-wide tile (last-but-one candidate)
+    // takes part only in the one-wave rule below.
+    constexpr int kCand = 7;
+    const int cand[kCand] = {256, 224, 192, 160, 128, 96, 64};
+    const double eff[kCand] = {1.0, 0.95, 0.88, 0.80, 0.72, 0.0, 0.36};
     int best = 256;
     double best_cost = 0.0;
-    for (int i = 0; i < 6; ++i) {
+    for (int i = 0; i < kCand; ++i) {
+        if (cand[i] == 96) continue;
         const int bn = cand[i];
         const int64_t tiles = num_m * ((N + bn - 1) / bn);
         const int64_t waves = (tiles + sm_count - 1) / sm_count;
@@ -488,7 +504,7 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     const Knobs& kn = knobs();
     bool one_wave = false;
     if (kn.one_wave && kblocks <= kn.one_wave_kb) {
-        for (int i = 5; i >= 0; --i) {   // narrowest first
+        for (int i = kCand - 1; i >= 0; --i) {   // narrowest first
             if (num_m * ((N + cand[i] - 1) / cand[i]) <= sm_count) {
                 // past 32 K blocks a wide tile is MMA-bound enough for the
                 // pairs' efficiency to win (2048^2 x 8192: 26.1 us as pairs
@@ -501,10 +517,11 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
             }
         }
     }
-    // DG_FORCE_BLOCK_N=64|128|160|192|224|256 pins the tile width (sweeps).
+    // DG_FORCE_BLOCK_N=64|96|128|160|192|224|256 pins the tile width (sweeps).
     {
         const int v = kn.force_block_n;
-        if (v == 64 || v == 128 || v == 160 || v == 192 || v == 224 || v == 256) best = v;
+        for (int i = 0; i < kCand; ++i)
+            if (v == cand[i]) best = v;
     }
     const int64_t tiles = num_m * ((N + best - 1) / best);
     p->block_m = kBM;
@@ -592,6 +609,7 @@ Params make_params(const TcLaunch& L) {
     if (knobs().group_m != 0) prm.group_m = knobs().group_m;
     prm.group_off = L.group_off;
     prm.groups = L.groups;
+    prm.a_box_bytes = kBM * kBKBytes;   // the single-CTA launcher may narrow it
     return prm;
 }
 

@@ -413,7 +413,7 @@ def _plan_paths_and_tiles(sm):
     for m in (17, 63, 65, 129, 256, 4096, 8192):
         p = dg.dg_gemm_plan(m, 1000, 1040, sm_count=sm)
         assert p["path"] == 3
-        assert p["block_n"] in (64, 128, 160, 192, 224, 256)
+        assert p["block_n"] in (64, 96, 128, 160, 192, 224, 256)
         if p["block_m"] == 256:            # CTA pairs: M >= 256, even grid
             assert m >= 256 and p["grid"] % 2 == 0 and p["grid"] <= 2 * p["tiles"]
         else:
@@ -421,6 +421,11 @@ def _plan_paths_and_tiles(sm):
         assert p["grid"] <= sm
         assert p["smem_bytes"] <= 232448
         assert p["block_k"] == 128
+    # decode batches on the QKV shape: 128 tiles of 128 x 96 keep 128 SMs
+    # streaming B (128 x 128 tiles would keep 96)
+    for m in (32, 64, 128):
+        p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
+        assert (p["path"], p["block_m"], p["block_n"], p["tiles"], p["grid"]) == (3, 128, 96, 128, 128)
     # FP16 operands: 64 K elements (128 bytes) per stage
     assert dg.dg_gemm_plan(4096, 4096, 4096, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16,
                            sm_count=sm)["block_k"] == 64

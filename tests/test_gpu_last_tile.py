@@ -4,7 +4,7 @@
 Each CTA's last tile gives every 32 x 32 output box its own place in the
 drained operand ring and stores them together; earlier tiles go through one
 staging box per warp.  Shapes cover whole and ragged last tiles, several
-tiles per CTA, widths of 224 and 160 columns (7 and 5 chunks), rows past M
+tiles per CTA, widths of 224, 160 and 96 columns (7, 5 and 3 chunks), rows past M
 in the odd CTA of a pair, both kernels, BF16 and E4M3 output (E4M3 rows of
 1000 bytes are not 16-byte multiples and take the direct stores), the
 output-amax report and the grouped kernel.  Every element is compared.
@@ -33,7 +33,7 @@ def _lib():
 
 
 @pytest.mark.parametrize("kernel,bn", [("1", None), ("0", None), ("1", "224"), ("1", "160"),
-                                       ("0", "224"), ("0", "160")])
+                                       ("0", "224"), ("0", "160"), ("0", "96")])
 @pytest.mark.parametrize("M,N,K", [
     (300, 1000, 272),    # ragged N, odd CTA's rows past M, one tile per CTA
     (640, 2240, 1040),   # several tiles per CTA, K tail
@@ -96,3 +96,38 @@ def test_grouped_widths(N):
             continue
         R, S = oracle.gemm_e4m3(qa_h[r0:r1], qb_h[g * N:(g + 1) * N])
         check_bf16_like(bf16_bits_to_f64(h[r0:r1]), R, S, 1.0, 0.5, f"group {g}")
+
+
+@pytest.mark.parametrize("M,N,K,fp16", [
+    (48, 11008, 1040, False),   # 115 tiles of 128 x 96, the last 64 wide; K tail
+    (32, 12288, 4096, False),   # the decode QKV projection at a batch of 32
+    (17, 14336, 1040, True),    # FP16 operands
+])
+def test_one_wave_96_wide(M, N, K, fp16):
+    """Shapes whose every tile fits one wave only at 96 columns take the
+    96-wide single-CTA tile from the default planner; every element against
+    the oracle."""
+    plan = dg.dg_gemm_plan(M, N, K, dg.DG_FP16 if fp16 else dg.DG_E4M3, dg.DG_BF16)
+    assert (plan["path"], plan["block_m"], plan["block_n"]) == (3, 128, 96), plan
+    assert plan["tiles"] == (N + 95) // 96 <= plan["grid"], plan
+    buf, D = guarded(M * N, torch.int16, 0x7FFF)
+    if fp16:
+        ha, hb = synth.make_inputs("fp16_4096", M=M, N=N, K=K)   # binary16 bit patterns
+        dg.dg_hgemm(dev(ha.view(np.int16)), dev(hb.view(np.int16)), D, dg.DG_BF16, M=M, N=N, K=K)
+        assert dg.dg_sync_status() == dg.DG_OK
+        R, S = oracle.hgemm(ha, hb)
+        check_guards(buf, M * N, 0x7FFF)
+        check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N)), R, S,
+                        1.0, 1.0)
+        return
+    A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+    qa, _, sa = gpu_quantize(A)
+    qb, _, sb = gpu_quantize(B)
+    qa_ref, sa_ref, _ = oracle.quantize_tensor(A)
+    qb_ref, sb_ref, _ = oracle.quantize_tensor(B)
+    dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    check_guards(buf, M * N, 0x7FFF)
+    check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N)), R, S,
+                    sa_ref, sb_ref)
