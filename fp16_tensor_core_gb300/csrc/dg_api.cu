@@ -93,7 +93,7 @@ Knobs read_knobs() {
     if (const char* e = std::getenv("DG_SPLITK_ROWS")) k.splitk_rows = e[0] == '1' ? 1 : 0;
     if (env_int("DG_SPLITK_TILE_ROWS", 16, 128, &v) && v % 8 == 0)
         k.splitk_tile_rows = static_cast<int>(v);
-    if (env_int("DG_TC_A_BOX", 0, 2, &v)) k.tc_a_box = static_cast<int>(v);
+    if (env_int("DG_TC_SHORT_BOX", 0, 2, &v)) k.tc_short_box = static_cast<int>(v);
     return k;
 }
 

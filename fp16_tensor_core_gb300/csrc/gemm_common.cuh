@@ -40,10 +40,12 @@ struct Params {
     int tail_split;
     float* tail_ws;         // partial tiles: [slot][2 CTAs][BN / 4][128] float4
     uint32_t* tail_counts;  // per tail tile and CTA: arrivals of the later parts
-    // Single-CTA kernel: bytes of one A box (128 rows x 128 bytes, or fewer
-    // rows when A has at most 32; the MMA still reads 128 rows, and the
-    // rows past the box only reach output rows past M, which are not stored).
+    // Single-CTA kernel: bytes of one A box and one B box (128 and BN rows
+    // x 128 bytes, or fewer rows for an operand of at most 32 rows; the MMA
+    // still reads 128 and BN rows, and the rows past a box only reach
+    // output rows past M or columns past N, which are not stored).
     int a_box_bytes;
+    int b_box_bytes;
 };
 
 constexpr int kMaxGroups = 1024;

@@ -236,7 +236,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (skip) {
                     skip = false;           // leave this stage unloaded
                 } else {
-                    mbar_arrive_expect_tx(&full[stage], p.a_box_bytes + C::kBBytes);
+                    mbar_arrive_expect_tx(&full[stage], p.a_box_bytes + p.b_box_bytes);
                     tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kb * C::kBK, T.a_row);
                     tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kb * C::kBK, T.b_row);
                     issued_mask |= 1u << stage;
@@ -412,20 +412,25 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     }
     CUtensorMap ta, tb, td;
     const int b_rows = kGrouped ? L.N * L.groups : L.N;   // grouped: B is (G*N) x K
-    // A box rows: M rounded up to 8 when A has at most 32 rows, else 128.
-    // A 128-row box over so short a tensor slows every load (17 x 11008 x
-    // 4096 E4M3: 17.3 us against 12.5 with a 24-row box; M = 32 runs 12.5
-    // with either).  DG_TC_A_BOX=0 keeps 128 rows, =2 narrows every A of
-    // fewer than 128 rows (sweeps).
-    int a_rows = kBM;
-    const int a_box = knobs().tc_a_box;
-    if (!kGrouped && ((a_box == 1 && L.M <= 32) || (a_box == 2 && L.M < kBM)))
-        a_rows = (L.M + 7) / 8 * 8;
+    // Box rows: an operand of at most 32 rows is loaded in boxes of its
+    // rows rounded up to 8, else 128 (A) and BN (B) rows.  A box that tall
+    // over so short a tensor slows every load (17 x 11008 x 4096 E4M3:
+    // 17.3 us against 12.5 with a 24-row A box; M = 32 runs 12.5 with
+    // either).  DG_TC_SHORT_BOX=0 keeps the full boxes, =2 also narrows
+    // every operand shorter than its box (sweeps).  Grouped B rows are
+    // slices of one tall tensor: full boxes.
+    const int sb = knobs().tc_short_box;
+    auto box_rows = [&](int rows, int full) {
+        return ((sb == 1 && rows <= 32) || (sb == 2 && rows < full)) ? (rows + 7) / 8 * 8 : full;
+    };
+    const int a_rows = kGrouped ? kBM : box_rows(L.M, kBM);
+    const int b_box = kGrouped ? BN : box_rows(L.N, BN);
     if (!make_map(&ta, L.A, L.M, L.K, kFp16In, a_rows) ||
-        !make_map(&tb, L.B, b_rows, L.K, kFp16In, BN))
+        !make_map(&tb, L.B, b_rows, L.K, kFp16In, b_box))
         return cudaErrorInvalidValue;
     Params prm2 = prm;
     prm2.a_box_bytes = a_rows * kBKBytes;
+    prm2.b_box_bytes = b_box * kBKBytes;
     // Output map of the staged epilogue (else the epilogue stores directly).
     if (!prm2.staged || !make_out_map(&td, L)) {
         prm2.staged = 0;
@@ -609,7 +614,8 @@ Params make_params(const TcLaunch& L) {
     if (knobs().group_m != 0) prm.group_m = knobs().group_m;
     prm.group_off = L.group_off;
     prm.groups = L.groups;
-    prm.a_box_bytes = kBM * kBKBytes;   // the single-CTA launcher may narrow it
+    prm.a_box_bytes = kBM * kBKBytes;   // the single-CTA launcher may narrow these
+    prm.b_box_bytes = L.plan->block_n * kBKBytes;
     return prm;
 }
 

@@ -1,13 +1,16 @@
-"""The single-CTA tiled kernel for short A, with each A box height (128
-rows; M rounded up to 8 for M <= 32, the default; the same for every
-M < 128), against the oracle.
+"""The single-CTA tiled kernel for short operands, with each box height
+(full: 128 rows of A, BN of B; the operand's rows rounded up to 8 when it
+has at most 32, the default; the same whenever it is shorter than its
+box), against the oracle.
 
-The MMA always reads 128 rows of A from shared memory; with a shorter box
-the rows past it hold whatever the stage held before, and only output rows
-past M depend on them, which are neither stored nor counted in the output
-amax.  Shapes: M = 1..100 forced onto the tiled path (GEMV, warp-MMA GEMV and
-split-K off), ragged N and a K tail, E4M3 and FP16 operands, BF16 and E4M3
-output with the amax report; guard sentinels around D.
+The MMA always reads 128 rows of A and BN of B from shared memory; with a
+shorter box the rows past it hold whatever the stage held before, and only
+output rows past M or columns past N depend on them, which are neither
+stored nor counted in the output amax.  Shapes: M = 1..100 forced onto the
+tiled path (GEMV, warp-MMA GEMV and split-K off), N = 8..32 (the 64-wide
+tile over a short B), both short, ragged edges and a K tail, E4M3 and FP16
+operands, BF16 and E4M3 output with the amax report; guard sentinels
+around D.
 """
 import numpy as np
 import pytest
@@ -35,10 +38,12 @@ def _lib():
 
 
 @pytest.mark.parametrize("box", ["0", "1", "2"])
-@pytest.mark.parametrize("M", [1, 8, 17, 31, 32, 33, 100])
+@pytest.mark.parametrize("M,N", [(1, 1000), (8, 1000), (17, 1000), (31, 1000), (32, 1000),
+                                 (33, 1000), (100, 1000), (300, 8), (300, 17), (700, 31),
+                                 (300, 32), (17, 9)])
 @pytest.mark.parametrize("out", [dg.DG_BF16, dg.DG_E4M3])
-def test_e4m3_small_m(box, M, out):
-    N, K = 1000, 1040
+def test_e4m3_small_m(box, M, N, out):
+    K = 1040
     A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
     qa, _, sa = gpu_quantize(A)
     qb, _, sb = gpu_quantize(B)
@@ -54,7 +59,7 @@ def test_e4m3_small_m(box, M, out):
     else:
         buf, D = guarded(M * N, torch.int16, 0x7FFF)
     am = scalar()
-    with knobs(DG_TC_A_BOX=box, **TILED):
+    with knobs(DG_TC_SHORT_BOX=box, **TILED):
         plan = dg.dg_gemm_plan(M, N, K, dg.DG_E4M3, out)
         assert (plan["path"], plan["block_m"]) == (3, 128), plan
         dg.dg_fp8_gemm_amax(qa, qb, D, sa, sb, sd, out, am, M=M, N=N, K=K)
@@ -72,12 +77,12 @@ def test_e4m3_small_m(box, M, out):
 
 
 @pytest.mark.parametrize("box", ["0", "1", "2"])
-@pytest.mark.parametrize("M", [3, 24, 57])
-def test_fp16_small_m(box, M):
-    N, K = 777, 1000
+@pytest.mark.parametrize("M,N", [(3, 777), (24, 777), (57, 777), (500, 24)])
+def test_fp16_small_m(box, M, N):
+    K = 1000
     A, B = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
     buf, D = guarded(M * N, torch.int16, 0x7FFF)
-    with knobs(DG_TC_A_BOX=box, **TILED):
+    with knobs(DG_TC_SHORT_BOX=box, **TILED):
         plan = dg.dg_gemm_plan(M, N, K, dg.DG_FP16, dg.DG_BF16)
         assert (plan["path"], plan["block_m"]) == (3, 128), plan
         dg.dg_hgemm(dev(A.view(np.int16)), dev(B.view(np.int16)), D, dg.DG_BF16, M=M, N=N, K=K)
