@@ -312,21 +312,49 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     // plan would keep fewer than 3/4 of the SMs busy and the time estimate
     // below favours it.  DG_SPLITK=0 turns it off, DG_SPLITK=1 uses it for
     // every M <= 128.
+    //
+    // Over a short K the tiled kernel wins instead once its tiles fill at
+    // least half the SMs in one wave: a CTA then streams its few K blocks
+    // straight into one tile, with no cross-CTA fix-up.  Measured on GB300
+    // (E4M3, graph-replayed, us, split-K -> tiled): 16 x 12288 x 1040 8.24
+    // -> 6.78, 9 x 12288 x 1040 8.20 -> 6.69, 16 x 14336 x 1040 8.70 ->
+    // 7.13, 16 x 11008 x 2048 8.44 -> 8.03; split-K stays ahead at 32 K
+    // blocks (16 x 12288 x 4096 11.6 against 12.8) and with fewer tiles
+    // (16 x 4096 x 1040: 5.5 either way).
     const bool splitk_off = kn.splitk == 0;
     const bool splitk_forced = kn.splitk == 1;
     const int64_t sk_rows = kn.splitk_tile_rows;
     const bool splitk_fits = (N + sk_rows - 1) / sk_rows <= kSkinnyMaxTiles;
+    const int64_t tiles = ((M + 127) / 128) * ((N + 63) / 64);
+    if (tiles > INT_MAX) return DG_ERR_UNSUPPORTED;
+    auto short_k_one_wave = [&](const dg_plan& t) {
+        const int64_t kb = (K + t.block_k - 1) / t.block_k;
+        return t.tiles <= t.grid && kb <= 16 && 2 * static_cast<int64_t>(t.tiles) >= sm_count;
+    };
     if (!splitk_off && splitk_fits && M <= kSkinnyMaxM) {
+        if (!splitk_forced) {
+            dg_plan t{};
+            t.path = 3;
+            plan_tc(M, N, K, fp16_in, sm_count, &t);
+            if (short_k_one_wave(t)) {
+                *p = t;
+                return DG_OK;
+            }
+        }
         p->path = 4;
         plan_skinny(M, N, K, fp16_in, sm_count, p);
         return DG_OK;
     }
-    const int64_t tiles = ((M + 127) / 128) * ((N + 63) / 64);
-    if (tiles > INT_MAX) return DG_ERR_UNSUPPORTED;
     p->path = 3;
     plan_tc(M, N, K, fp16_in, sm_count, p);
-    if (!splitk_off && splitk_fits && M <= kSplitkMaxCols &&
-        (splitk_forced || 4 * static_cast<int64_t>(p->grid) < 3 * static_cast<int64_t>(sm_count))) {
+    // Split-K is weighed only where the tiled plan keeps fewer than 3/4 of
+    // the SMs busy.  Weighing it against the 96-wide one-wave plans too
+    // (the 128-wide plans they replaced were weighed) was measured: 3-4%
+    // gained at 17 / 32 x 11008 x 4096 E4M3, 8-20% lost at FP16 17 x 11008
+    // x 1040, 32 x 12288 x 1040, 48 x 11008 x 4096 and E4M3 48 x 11008 x
+    // 8192, where the split-K estimate is too low.
+    const bool weigh = 4 * static_cast<int64_t>(p->grid) < 3 * static_cast<int64_t>(sm_count);
+    if (!splitk_off && splitk_fits && M <= kSplitkMaxCols && (splitk_forced || weigh)) {
         dg_plan sk{};
         sk.path = 4;
         plan_skinny(M, N, K, fp16_in, sm_count, &sk);

@@ -426,6 +426,14 @@ def _plan_paths_and_tiles(sm):
     for m in (32, 64, 128):
         p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
         assert (p["path"], p["block_m"], p["block_n"], p["tiles"], p["grid"]) == (3, 128, 96, 128, 128)
+    # 9..16 rows over a short K with many tiles: the one-wave tiled kernel;
+    # over a long K, or with few tiles, split-K
+    p = dg.dg_gemm_plan(16, 12288, 1040, sm_count=sm)
+    assert (p["path"], p["block_n"], p["tiles"]) == (3, 96, 128), p
+    assert dg.dg_gemm_plan(16, 12288, 4096, sm_count=sm)["path"] == 4
+    assert dg.dg_gemm_plan(16, 4096, 1040, sm_count=sm)["path"] == 4
+    # a 96-wide one-wave plan keeps the tiled kernel over a long K too
+    assert dg.dg_gemm_plan(17, 11008, 4096, sm_count=sm)["block_n"] == 96
     # FP16 operands: 64 K elements (128 bytes) per stage
     assert dg.dg_gemm_plan(4096, 4096, 4096, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16,
                            sm_count=sm)["block_k"] == 64

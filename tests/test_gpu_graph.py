@@ -30,7 +30,7 @@ def chain(A, B, bufs, out):
 
 @pytest.mark.parametrize("M,N,K,out", [
     (1, 1000, 1040, dg.DG_BF16),      # warp-MMA GEMV
-    (16, 12288, 512, dg.DG_BF16),     # split-K
+    (16, 4096, 1040, dg.DG_BF16),     # split-K (32 tiles, each over four CTAs)
     (129, 1000, 1040, dg.DG_BF16),    # single CTA
     (640, 1536, 2048, dg.DG_E4M3),    # CTA pairs, E4M3 out
 ])

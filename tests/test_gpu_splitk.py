@@ -30,7 +30,10 @@ def _lib():
     from fp16_tensor_core_gb300 import build
     build.build()
     dg.dg_init()
-    with knobs(DG_MMA_GEMV="0"):   # M <= 16 on this kernel, not the warp-MMA GEMV
+    # M <= 16 on this kernel, not the warp-MMA GEMV, and split-K for every
+    # M <= 128 (over a short K with many tiles the default planner would take
+    # the one-wave tiled kernel for some of these shapes)
+    with knobs(DG_MMA_GEMV="0", DG_SPLITK="1"):
         yield
     assert dg.dg_sync_status() == dg.DG_OK
 
@@ -84,57 +87,45 @@ def test_splitk_bf16_matches_oracle(M, N, K):
 def test_splitk_wide_bf16_matches_oracle(M, N, K):
     """17 <= M <= 128: MMA N = 32 / 64 / 128 columns of A per CTA, the
     partial slots and the fixup walked 16 columns at a time."""
-    os.environ["DG_SPLITK"] = "1"
-    dg.dg_reload_env()
-    try:
-        p = _plan(M, N, K)
-        assert p["block_m"] == (32 if M <= 32 else 64 if M <= 64 else 128), p
-        qa, qb, sa, sb, qa_ref, qb_ref, sa_ref, sb_ref = _fp8_case(M, N, K)
-        buf, D = guarded(M * N, torch.int16, 0x7FFF)
-        dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, M=M, N=N, K=K)
-        assert dg.dg_sync_status() == dg.DG_OK
-        check_guards(buf, M * N, 0x7FFF)
-        R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
-        d = bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N))
-        check_bf16_like(d, R, S, sa_ref, sb_ref)
-    finally:
-        os.environ.pop("DG_SPLITK", None)
-        dg.dg_reload_env()
+    p = _plan(M, N, K)
+    assert p["block_m"] == (32 if M <= 32 else 64 if M <= 64 else 128), p
+    qa, qb, sa, sb, qa_ref, qb_ref, sa_ref, sb_ref = _fp8_case(M, N, K)
+    buf, D = guarded(M * N, torch.int16, 0x7FFF)
+    dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf, M * N, 0x7FFF)
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    d = bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N))
+    check_bf16_like(d, R, S, sa_ref, sb_ref)
 
 
 @pytest.mark.parametrize("M,N,K", [(48, 1000, 2080), (120, 640, 1040)])
 def test_splitk_wide_e4m3_out_and_fp16(M, N, K):
-    os.environ["DG_SPLITK"] = "1"
-    dg.dg_reload_env()
-    try:
-        _plan(M, N, K)
-        A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
-        qa_ref, sa, _ = oracle.quantize_tensor(A)
-        qb_ref, sb, _ = oracle.quantize_tensor(B)
-        R = oracle.gemm_e4m3(qa_ref, qb_ref, with_abs=False)
-        sd = np.float32(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))) / 448.0)
-        qa, _, sa_d = gpu_quantize(A)
-        qb, _, sb_d = gpu_quantize(B)
-        sdt = scalar()
-        sdt[0] = float(sd)
-        buf, D = guarded(M * N, torch.uint8, 0x7F)
-        dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, sdt, dg.DG_E4M3, M=M, N=N, K=K)
-        assert dg.dg_sync_status() == dg.DG_OK
-        check_guards(buf, M * N, 0x7F)
-        check_e4m3(D.cpu().numpy().reshape(M, N), R, sa, sb, sd)
-        _plan(M, N, K, dg.DG_FP16)
-        A16, B16 = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
-        buf16, D16 = guarded(M * N, torch.int16, 0x7FFF)
-        dg.dg_hgemm(dev(A16.view(np.int16)), dev(B16.view(np.int16)), D16, dg.DG_FP16,
-                    M=M, N=N, K=K)
-        assert dg.dg_sync_status() == dg.DG_OK
-        check_guards(buf16, M * N, 0x7FFF)
-        R16, S16 = oracle.hgemm(A16, B16)
-        check_bf16_like(fp16_bits_to_f64(D16.cpu().numpy().view(np.uint16).reshape(M, N)),
-                        R16, S16, 1.0, 1.0, "FP16")
-    finally:
-        os.environ.pop("DG_SPLITK", None)
-        dg.dg_reload_env()
+    _plan(M, N, K)
+    A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+    qa_ref, sa, _ = oracle.quantize_tensor(A)
+    qb_ref, sb, _ = oracle.quantize_tensor(B)
+    R = oracle.gemm_e4m3(qa_ref, qb_ref, with_abs=False)
+    sd = np.float32(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))) / 448.0)
+    qa, _, sa_d = gpu_quantize(A)
+    qb, _, sb_d = gpu_quantize(B)
+    sdt = scalar()
+    sdt[0] = float(sd)
+    buf, D = guarded(M * N, torch.uint8, 0x7F)
+    dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, sdt, dg.DG_E4M3, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf, M * N, 0x7F)
+    check_e4m3(D.cpu().numpy().reshape(M, N), R, sa, sb, sd)
+    _plan(M, N, K, dg.DG_FP16)
+    A16, B16 = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
+    buf16, D16 = guarded(M * N, torch.int16, 0x7FFF)
+    dg.dg_hgemm(dev(A16.view(np.int16)), dev(B16.view(np.int16)), D16, dg.DG_FP16,
+                M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf16, M * N, 0x7FFF)
+    R16, S16 = oracle.hgemm(A16, B16)
+    check_bf16_like(fp16_bits_to_f64(D16.cpu().numpy().view(np.uint16).reshape(M, N)),
+                    R16, S16, 1.0, 1.0, "FP16")
 
 
 @pytest.mark.parametrize("M,N,K", [(48, 4096, 2048), (24, 2048, 1040)])
@@ -143,43 +134,37 @@ def test_splitk_staged_fixup_all_outputs(M, N, K):
     shared memory (32 or 16 tiles, a whole multiple of CTAs per tile, every
     partial tile fits in the ring): BF16 and E4M3 out from E4M3 inputs and
     FP16 out from FP16 inputs."""
-    os.environ["DG_SPLITK"] = "1"
-    dg.dg_reload_env()
-    try:
-        p = _plan(M, N, K)
-        assert p["grid"] % p["tiles"] == 0 and p["grid"] // p["tiles"] >= 2, p
-        A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
-        qa_ref, sa, _ = oracle.quantize_tensor(A)
-        qb_ref, sb, _ = oracle.quantize_tensor(B)
-        qa, _, sa_d = gpu_quantize(A)
-        qb, _, sb_d = gpu_quantize(B)
-        R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
-        buf, D = guarded(M * N, torch.int16, 0x7FFF)
-        dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, None, dg.DG_BF16, M=M, N=N, K=K)
-        assert dg.dg_sync_status() == dg.DG_OK
-        check_guards(buf, M * N, 0x7FFF)
-        check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N)), R, S, sa, sb)
-        sd = np.float32(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))) / 448.0)
-        sdt = scalar()
-        sdt[0] = float(sd)
-        buf8, D8 = guarded(M * N, torch.uint8, 0x7F)
-        dg.dg_fp8_gemm(qa, qb, D8, sa_d, sb_d, sdt, dg.DG_E4M3, M=M, N=N, K=K)
-        assert dg.dg_sync_status() == dg.DG_OK
-        check_guards(buf8, M * N, 0x7F)
-        check_e4m3(D8.cpu().numpy().reshape(M, N), R, sa, sb, sd)
-        p16 = _plan(M, N, K, dg.DG_FP16)
-        assert p16["grid"] % p16["tiles"] == 0, p16
-        A16, B16 = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
-        buf16, D16 = guarded(M * N, torch.int16, 0x7FFF)
-        dg.dg_hgemm(dev(A16.view(np.int16)), dev(B16.view(np.int16)), D16, dg.DG_FP16, M=M, N=N, K=K)
-        assert dg.dg_sync_status() == dg.DG_OK
-        check_guards(buf16, M * N, 0x7FFF)
-        R16, S16 = oracle.hgemm(A16, B16)
-        check_bf16_like(fp16_bits_to_f64(D16.cpu().numpy().view(np.uint16).reshape(M, N)), R16, S16,
-                        1.0, 1.0, "FP16")
-    finally:
-        os.environ.pop("DG_SPLITK", None)
-        dg.dg_reload_env()
+    p = _plan(M, N, K)
+    assert p["grid"] % p["tiles"] == 0 and p["grid"] // p["tiles"] >= 2, p
+    A, B = synth.make_inputs("fp8_sweep_m65", M=M, N=N, K=K)
+    qa_ref, sa, _ = oracle.quantize_tensor(A)
+    qb_ref, sb, _ = oracle.quantize_tensor(B)
+    qa, _, sa_d = gpu_quantize(A)
+    qb, _, sb_d = gpu_quantize(B)
+    R, S = oracle.gemm_e4m3(qa_ref, qb_ref)
+    buf, D = guarded(M * N, torch.int16, 0x7FFF)
+    dg.dg_fp8_gemm(qa, qb, D, sa_d, sb_d, None, dg.DG_BF16, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf, M * N, 0x7FFF)
+    check_bf16_like(bf16_bits_to_f64(D.cpu().numpy().view(np.uint16).reshape(M, N)), R, S, sa, sb)
+    sd = np.float32(np.max(np.abs(oracle.epilogue_scale(R, sa, sb))) / 448.0)
+    sdt = scalar()
+    sdt[0] = float(sd)
+    buf8, D8 = guarded(M * N, torch.uint8, 0x7F)
+    dg.dg_fp8_gemm(qa, qb, D8, sa_d, sb_d, sdt, dg.DG_E4M3, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf8, M * N, 0x7F)
+    check_e4m3(D8.cpu().numpy().reshape(M, N), R, sa, sb, sd)
+    p16 = _plan(M, N, K, dg.DG_FP16)
+    assert p16["grid"] % p16["tiles"] == 0, p16
+    A16, B16 = synth.make_inputs("fp16_4096", M=M, N=N, K=K)
+    buf16, D16 = guarded(M * N, torch.int16, 0x7FFF)
+    dg.dg_hgemm(dev(A16.view(np.int16)), dev(B16.view(np.int16)), D16, dg.DG_FP16, M=M, N=N, K=K)
+    assert dg.dg_sync_status() == dg.DG_OK
+    check_guards(buf16, M * N, 0x7FFF)
+    R16, S16 = oracle.hgemm(A16, B16)
+    check_bf16_like(fp16_bits_to_f64(D16.cpu().numpy().view(np.uint16).reshape(M, N)), R16, S16,
+                    1.0, 1.0, "FP16")
 
 
 def test_splitk_m1_when_forced():
@@ -306,38 +291,32 @@ def test_splitk_staged_fixup_repeatable_back_to_back(M, N, K):
     partial tiles into shared memory with bulk copies after their acquiring
     arrival atomic; a missing ordering would show as an occasional stale
     partial, so a different sum."""
-    os.environ["DG_SPLITK"] = "1"
-    dg.dg_reload_env()
-    try:
-        p = _plan(M, N, K)
-        assert p["grid"] % p["tiles"] == 0
-        qa, qb, sa, sb, *_ = _fp8_case(M, N, K)
-        ref = torch.empty((M, N), dtype=torch.int16, device="cuda")
-        dg.dg_fp8_gemm(qa, qb, ref, sa, sb, None, dg.DG_BF16)
-        assert dg.dg_sync_status() == dg.DG_OK
-        outs = [torch.empty_like(ref) for _ in range(8)]
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
+    p = _plan(M, N, K)
+    assert p["grid"] % p["tiles"] == 0
+    qa, qb, sa, sb, *_ = _fp8_case(M, N, K)
+    ref = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    dg.dg_fp8_gemm(qa, qb, ref, sa, sb, None, dg.DG_BF16)
+    assert dg.dg_sync_status() == dg.DG_OK
+    outs = [torch.empty_like(ref) for _ in range(8)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for D in outs:
+            dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for D in outs:
+            dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, stream=s)
+    for r in range(50):
+        g.replay()
+        if r % 10 == 9:
+            torch.cuda.synchronize()
             for D in outs:
-                dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, stream=s)
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for D in outs:
-                dg.dg_fp8_gemm(qa, qb, D, sa, sb, None, dg.DG_BF16, stream=s)
-        for r in range(50):
-            g.replay()
-            if r % 10 == 9:
-                torch.cuda.synchronize()
-                for D in outs:
-                    assert torch.equal(D, ref)
-        torch.cuda.synchronize()
-        assert dg.dg_sync_status() == dg.DG_OK
-    finally:
-        os.environ.pop("DG_SPLITK", None)
-        dg.dg_reload_env()
+                assert torch.equal(D, ref)
+    torch.cuda.synchronize()
+    assert dg.dg_sync_status() == dg.DG_OK
 
 
 def test_splitk_timeout_then_recovers():

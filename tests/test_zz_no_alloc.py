@@ -53,6 +53,7 @@ def _inputs(M, N, K):
 def test_static_workspace_matches_regular_entry(M, N, K, out):
     os.environ["DG_GEMV_MAX_M"] = "0"     # the regular entry takes the split-K path for M = 1 too
     os.environ["DG_MMA_GEMV"] = "0"
+    os.environ["DG_SPLITK"] = "1"         # and for 16 x 12288 x 512 (else the one-wave tiled kernel)
     dg.dg_reload_env()
     try:
         assert dg.dg_gemm_plan(M, N, K, dg.DG_E4M3, out)["path"] == 4
@@ -73,6 +74,7 @@ def test_static_workspace_matches_regular_entry(M, N, K, out):
     finally:
         os.environ.pop("DG_GEMV_MAX_M", None)
         os.environ.pop("DG_MMA_GEMV", None)
+        os.environ.pop("DG_SPLITK", None)
         dg.dg_reload_env()
 
 
