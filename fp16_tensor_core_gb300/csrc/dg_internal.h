@@ -67,7 +67,7 @@ struct Knobs {
     // wherever they fit; default 128-row tiles.
     int splitk_rows = 0;
     int splitk_tile_rows = 128;   // DG_SPLITK_TILE_ROWS=<16..128, multiple of 8> (sweeps)
-    int tc_short_box = 1;         // DG_TC_SHORT_BOX (0, 1, 2): box rows of short operands
+    int tc_short_box = 2;         // DG_TC_SHORT_BOX (0, 1, 2): box rows of short operands
 };
 const Knobs& knobs();
 

@@ -41,11 +41,18 @@ struct Params {
     float* tail_ws;         // partial tiles: [slot][2 CTAs][BN / 4][128] float4
     uint32_t* tail_counts;  // per tail tile and CTA: arrivals of the later parts
     // Single-CTA kernel: bytes of one A box and one B box (128 and BN rows
-    // x 128 bytes, or fewer rows for an operand of at most 32 rows; the MMA
-    // still reads 128 and BN rows, and the rows past a box only reach
-    // output rows past M or columns past N, which are not stored).
+    // x 128 bytes), and of the shorter boxes of the edge tiles: tiles whose
+    // A rows start at a_edge_row or later (B rows at b_edge_row or later)
+    // load through the edge maps, boxes of the rows left rounded up to 8
+    // (INT_MAX: no edge).  The MMA still reads 128 and BN rows; the rows
+    // past a box only reach output rows past M or columns past N, which are
+    // not stored.
     int a_box_bytes;
     int b_box_bytes;
+    int a_edge_bytes;
+    int b_edge_bytes;
+    int a_edge_row;
+    int b_edge_row;
 };
 
 constexpr int kMaxGroups = 1024;

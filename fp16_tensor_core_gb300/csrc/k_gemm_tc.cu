@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <mutex>
 
 #include "dg_internal.h"
@@ -93,7 +94,9 @@ template <int BN, int STAGES, bool kFp16In, bool kGrouped = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_b,
-               const __grid_constant__ CUtensorMap tmap_d, const Params p) {
+               const __grid_constant__ CUtensorMap tmap_d,
+               const __grid_constant__ CUtensorMap tmap_a_edge,
+               const __grid_constant__ CUtensorMap tmap_b_edge, const Params p) {
     using C = Cfg<BN, STAGES, kFp16In, kGrouped>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -128,6 +131,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
+        tma_prefetch_desc(&tmap_a_edge);
+        tma_prefetch_desc(&tmap_b_edge);
     }
     if (warp == 2) {
         tmem_alloc<C::kTmemCols>(tmem_slot);
@@ -236,9 +241,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (skip) {
                     skip = false;           // leave this stage unloaded
                 } else {
-                    mbar_arrive_expect_tx(&full[stage], p.a_box_bytes + p.b_box_bytes);
-                    tma_load_2d(sA + stage * C::kABytes, &tmap_a, &full[stage], kb * C::kBK, T.a_row);
-                    tma_load_2d(sB + stage * C::kBBytes, &tmap_b, &full[stage], kb * C::kBK, T.b_row);
+                    // edge tiles load shorter boxes through their own maps
+                    const bool ae = T.a_row >= p.a_edge_row, be = T.b_row >= p.b_edge_row;
+                    mbar_arrive_expect_tx(&full[stage], (ae ? p.a_edge_bytes : p.a_box_bytes) +
+                                                            (be ? p.b_edge_bytes : p.b_box_bytes));
+                    tma_load_2d(sA + stage * C::kABytes, ae ? &tmap_a_edge : &tmap_a, &full[stage],
+                                kb * C::kBK, T.a_row);
+                    tma_load_2d(sB + stage * C::kBBytes, be ? &tmap_b_edge : &tmap_b, &full[stage],
+                                kb * C::kBK, T.b_row);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 }
@@ -412,32 +422,47 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     }
     CUtensorMap ta, tb, td;
     const int b_rows = kGrouped ? L.N * L.groups : L.N;   // grouped: B is (G*N) x K
-    // Box rows: an operand of at most 32 rows is loaded in boxes of its
-    // rows rounded up to 8, else 128 (A) and BN (B) rows.  A box that tall
-    // over so short a tensor slows every load (17 x 11008 x 4096 E4M3:
-    // 17.3 us against 12.5 with a 24-row A box; M = 32 runs 12.5 with
-    // either).  DG_TC_SHORT_BOX=0 keeps the full boxes, =2 also narrows
-    // every operand shorter than its box (sweeps).  Grouped B rows are
-    // slices of one tall tensor: full boxes.
+    // Edge boxes: the last tile of an operand that ends inside a tile (128
+    // rows of A, BN of B) loads boxes of the rows left rounded up to 8, so
+    // no box reaches far past the tensor's end.  Those rows still cross
+    // into the SM and slow every load: E4M3 17 x 11008 x 4096 17.3 -> 12.5
+    // us, 33 x 12288 x 1040 9.9 -> 7.0, 48 x 11008 x 1040 9.3 -> 7.2 with
+    // the short box; no change at 4096-deep K for 33..120 rows.
+    // DG_TC_SHORT_BOX=0 keeps full boxes everywhere, =1 narrows only an
+    // operand of at most 32 rows (sweeps).  Grouped B rows are slices of
+    // one tall tensor: full boxes.
     const int sb = knobs().tc_short_box;
-    auto box_rows = [&](int rows, int full) {
-        return ((sb == 1 && rows <= 32) || (sb == 2 && rows < full)) ? (rows + 7) / 8 * 8 : full;
+    auto edge = [&](int rows, int full, int* edge_row, int* edge_box) {
+        const int left = rows % full;
+        *edge_row = INT_MAX;
+        *edge_box = full;
+        if (kGrouped || left == 0 || sb == 0 || (sb == 1 && rows > 32)) return;
+        *edge_row = rows - left;
+        *edge_box = (left + 7) / 8 * 8;
     };
-    const int a_rows = kGrouped ? kBM : box_rows(L.M, kBM);
-    const int b_box = kGrouped ? BN : box_rows(L.N, BN);
-    if (!make_map(&ta, L.A, L.M, L.K, kFp16In, a_rows) ||
-        !make_map(&tb, L.B, b_rows, L.K, kFp16In, b_box))
+    int a_edge_row, a_edge_box, b_edge_row, b_edge_box;
+    edge(L.M, kBM, &a_edge_row, &a_edge_box);
+    edge(L.N, BN, &b_edge_row, &b_edge_box);
+    CUtensorMap tae, tbe;
+    if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kBM) ||
+        !make_map(&tb, L.B, b_rows, L.K, kFp16In, BN) ||
+        !make_map(&tae, L.A, L.M, L.K, kFp16In, a_edge_box) ||
+        !make_map(&tbe, L.B, b_rows, L.K, kFp16In, b_edge_box))
         return cudaErrorInvalidValue;
     Params prm2 = prm;
-    prm2.a_box_bytes = a_rows * kBKBytes;
-    prm2.b_box_bytes = b_box * kBKBytes;
+    prm2.a_box_bytes = kBM * kBKBytes;
+    prm2.b_box_bytes = BN * kBKBytes;
+    prm2.a_edge_bytes = a_edge_box * kBKBytes;
+    prm2.b_edge_bytes = b_edge_box * kBKBytes;
+    prm2.a_edge_row = a_edge_row;
+    prm2.b_edge_row = b_edge_row;
     // Output map of the staged epilogue (else the epilogue stores directly).
     if (!prm2.staged || !make_out_map(&td, L)) {
         prm2.staged = 0;
         td = ta;
     }
     return launch_kernel(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped>, dim3(L.plan->grid),
-                         dim3(kThreads), C::kSmemBytes, s, ta, tb, td, prm2);
+                         dim3(kThreads), C::kSmemBytes, s, ta, tb, td, tae, tbe, prm2);
 }
 
 template <bool kFp16In>
@@ -614,8 +639,12 @@ Params make_params(const TcLaunch& L) {
     if (knobs().group_m != 0) prm.group_m = knobs().group_m;
     prm.group_off = L.group_off;
     prm.groups = L.groups;
-    prm.a_box_bytes = kBM * kBKBytes;   // the single-CTA launcher may narrow these
+    prm.a_box_bytes = kBM * kBKBytes;   // the single-CTA launcher sets the edge boxes
     prm.b_box_bytes = L.plan->block_n * kBKBytes;
+    prm.a_edge_bytes = prm.a_box_bytes;
+    prm.b_edge_bytes = prm.b_box_bytes;
+    prm.a_edge_row = INT_MAX;
+    prm.b_edge_row = INT_MAX;
     return prm;
 }
 

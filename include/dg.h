@@ -401,8 +401,8 @@ dg_status dg_release_stream(dg_stream_t stream);
  *   DG_GROUP_M=n          raster group of M tiles (1..4096)
  *   DG_TC_SHORT_BOX=0|1|2 single-CTA tiled kernel: operand boxes of full
  *                         height / of the operand's rows rounded up to 8
- *                         when it has at most 32 (default) / whenever it
- *                         is shorter than its box
+ *                         when it has at most 32 / whenever it is shorter
+ *                         than its box (default)
  *   DG_ONE_WAVE=0         no one-wave tile rule; DG_ONE_WAVE_KB=n its
  *                         K-block limit (default 64)
  *   DG_STAGED_EPI=0       tiled epilogues store rows directly instead of

@@ -1,14 +1,15 @@
-"""The single-CTA tiled kernel for short operands, with each box height
-(full: 128 rows of A, BN of B; the operand's rows rounded up to 8 when it
-has at most 32, the default; the same whenever it is shorter than its
-box), against the oracle.
+"""The single-CTA tiled kernel for short operands and ragged edges, with
+each box height (full: 128 rows of A, BN of B; the operand's rows rounded
+up to 8 when it has at most 32; the last tile's rows rounded up to 8
+whenever an operand ends inside a tile, the default), against the oracle.
 
 The MMA always reads 128 rows of A and BN of B from shared memory; with a
 shorter box the rows past it hold whatever the stage held before, and only
 output rows past M or columns past N depend on them, which are neither
 stored nor counted in the output amax.  Shapes: M = 1..100 forced onto the
 tiled path (GEMV, warp-MMA GEMV and split-K off), N = 8..32 (the 64-wide
-tile over a short B), both short, ragged edges and a K tail, E4M3 and FP16
+tile over a short B), both short, M = 129 and 300 (an edge tile of 1 and
+44 rows) with ragged N, and a K tail, E4M3 and FP16
 operands, BF16 and E4M3 output with the amax report; guard sentinels
 around D.
 """
@@ -40,7 +41,7 @@ def _lib():
 @pytest.mark.parametrize("box", ["0", "1", "2"])
 @pytest.mark.parametrize("M,N", [(1, 1000), (8, 1000), (17, 1000), (31, 1000), (32, 1000),
                                  (33, 1000), (100, 1000), (300, 8), (300, 17), (700, 31),
-                                 (300, 32), (17, 9)])
+                                 (300, 32), (17, 9), (129, 1000), (300, 777)])
 @pytest.mark.parametrize("out", [dg.DG_BF16, dg.DG_E4M3])
 def test_e4m3_small_m(box, M, N, out):
     K = 1040
