@@ -102,11 +102,13 @@ def test_grouped_widths(N):
     (48, 11008, 1040, False),   # 115 tiles of 128 x 96, the last 64 wide; K tail
     (32, 12288, 4096, False),   # the decode QKV projection at a batch of 32
     (17, 14336, 1040, True),    # FP16 operands
+    (16, 12288, 1040, False),   # 16 rows over a short K: tiled instead of split-K
+    (12, 11008, 2048, False),
 ])
 def test_one_wave_96_wide(M, N, K, fp16):
     """Shapes whose every tile fits one wave only at 96 columns take the
-    96-wide single-CTA tile from the default planner; every element against
-    the oracle."""
+    96-wide single-CTA tile from the default planner (at 9..16 rows only over
+    a short K); every element against the oracle."""
     plan = dg.dg_gemm_plan(M, N, K, dg.DG_FP16 if fp16 else dg.DG_E4M3, dg.DG_BF16)
     assert (plan["path"], plan["block_m"], plan["block_n"]) == (3, 128, 96), plan
     assert plan["tiles"] == (N + 95) // 96 <= plan["grid"], plan
