@@ -443,11 +443,16 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     int a_edge_row, a_edge_box, b_edge_row, b_edge_box;
     edge(L.M, kBM, &a_edge_row, &a_edge_box);
     edge(L.N, BN, &b_edge_row, &b_edge_box);
+    // (an operand without an edge tile passes its full map twice: no
+    // second encoding on the host)
     CUtensorMap tae, tbe;
     if (!make_map(&ta, L.A, L.M, L.K, kFp16In, kBM) ||
-        !make_map(&tb, L.B, b_rows, L.K, kFp16In, BN) ||
-        !make_map(&tae, L.A, L.M, L.K, kFp16In, a_edge_box) ||
-        !make_map(&tbe, L.B, b_rows, L.K, kFp16In, b_edge_box))
+        !make_map(&tb, L.B, b_rows, L.K, kFp16In, BN))
+        return cudaErrorInvalidValue;
+    tae = ta;
+    tbe = tb;
+    if ((a_edge_row != INT_MAX && !make_map(&tae, L.A, L.M, L.K, kFp16In, a_edge_box)) ||
+        (b_edge_row != INT_MAX && !make_map(&tbe, L.B, b_rows, L.K, kFp16In, b_edge_box)))
         return cudaErrorInvalidValue;
     Params prm2 = prm;
     prm2.a_box_bytes = kBM * kBKBytes;
