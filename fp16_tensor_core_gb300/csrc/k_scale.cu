@@ -190,9 +190,9 @@ amax_pair_kernel(const float* __restrict__ xa, int64_t na, const float* __restri
 }
 
 // Quantisation of both GEMM operands in one grid, each with its own scale:
-// the 512-element slabs of a, then of b, are dealt to warps as one sequence
-// (a warp's slab lies wholly in one tensor); the ragged tails go to blocks 0
-// and 1 (0 alone for a one-CTA grid).
+// the 512-element slabs of a, then of b, are dealt to warps as one sequence,
+// taken from its end (a warp's slab lies wholly in one tensor); the ragged
+// tails go to blocks 0 and 1 (0 alone for a one-CTA grid).
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_pair_kernel(const float* __restrict__ xa, int64_t na, const float* __restrict__ sa_p,
                      uint8_t* __restrict__ qa, const float* __restrict__ xb, int64_t nb,
@@ -203,7 +203,11 @@ quantize_pair_kernel(const float* __restrict__ xa, int64_t na, const float* __re
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t ka = na >> 9, kb = nb >> 9;
-    for (int64_t slab = warp; slab < ka + kb; slab += nwarps) {
+    // Slabs from the end of b backwards: the amax pass before this one
+    // streamed a then b front to back, so the first slabs taken here are
+    // the ones it read last, still in L2.
+    for (int64_t k = warp; k < ka + kb; k += nwarps) {
+        const int64_t slab = ka + kb - 1 - k;
         const bool in_a = slab < ka;   // the same for the whole warp
         const float4* x4 = reinterpret_cast<const float4*>(in_a ? xa : xb);
         uint32_t* q4 = reinterpret_cast<uint32_t*>(in_a ? qa : qb);
