@@ -144,14 +144,18 @@ dg_status dg_quantize_e4m3_pair(const float* a, int64_t na, const float* b, int6
  *   scale_d  FP32[1], device; required iff out == DG_E4M3, else ignored.
  *   M, N, K  >= 0 and < 2^31.  M == 0 or N == 0 is a no-op; K == 0 writes
  *            zeros.  K must be a multiple of 16 (row pitch alignment).
- * M <= 2 runs a bandwidth-bound GEMV with the K sum split across a warp
- * ([DG-FP16] §2.1 and §4.1, the decode QKV projection); 3 <= M <= 16 a
- * split-K tensor-core kernel (operands swapped, K spread over every SM);
- * larger M the tiled tensor-core kernel with a tile chosen per shape
- * (dg_gemm_plan), or for 17 <= M <= 128 the split-K kernel where the tiled
- * one would leave SMs idle and a time estimate favours split-K (few rows of
- * A against a long K).  K tails are zero-filled by the tensor-memory loads and M/N
- * edges are predicated stores ([FP8-guide] §3.3).
+ * Paths (dg_gemm_plan reports the one taken): M <= 8 a bandwidth-bound
+ * GEMV that streams B into registers and sums K on warp-level MMAs (up to
+ * M = 16 for FP16 operands or small N * K; the CUDA-core GEMV for M = 1 when
+ * N is too large for one wave of its CTAs) ([DG-FP16] §2.1 and §4.1, the
+ * decode QKV projection); 9 <= M <= 16 a split-K tensor-core kernel
+ * (operands swapped, K spread over every SM), or over a short K the tiled
+ * kernel when its tiles fill at least half the SMs in one wave; larger M
+ * the tiled tensor-core kernel with a tile chosen per shape, or for
+ * 17 <= M <= 128 the split-K kernel where the tiled one would leave SMs
+ * idle and a time estimate favours split-K (few rows of A against a long
+ * K).  K tails are zero-filled by the tensor-memory loads and M/N edges are
+ * predicated or clipped stores ([FP8-guide] §3.3).
  */
 dg_status dg_fp8_gemm(const uint8_t* A, const uint8_t* B, void* D, int64_t M,
                       int64_t N, int64_t K, const float* scale_a,
