@@ -334,7 +334,8 @@ dg_status dg_convert_f16_amax_pair(const float* a, int64_t na, const float* b, i
  */
 typedef struct {
     int path;       /* 0 no-op, 1 zero-fill (K == 0), 2 GEMV, 3 tensor core,
-                       4 split-K tensor core for M <= 16, and for
+                       4 split-K tensor core for M <= 16 (unless a short K
+                       lets one wave of tiles fill half the SMs), and for
                        M <= 128 where it is estimated faster (operands
                        swapped: block_m = 16, 32, 64 or 128 padded rows of
                        A, block_n = 128 rows of B per tile, K blocks of all
