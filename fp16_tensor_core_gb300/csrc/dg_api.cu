@@ -94,6 +94,7 @@ Knobs read_knobs() {
     if (env_int("DG_SPLITK_TILE_ROWS", 16, 128, &v) && v % 8 == 0)
         k.splitk_tile_rows = static_cast<int>(v);
     if (env_int("DG_TC_SHORT_BOX", 0, 2, &v)) k.tc_short_box = static_cast<int>(v);
+    if (env_int("DG_TC_KPS", 1, 2, &v)) k.tc_kps = static_cast<int>(v);
     return k;
 }
 
@@ -193,7 +194,8 @@ void log_plan(const char* what, int64_t M, int64_t N, int64_t K, const dg_plan& 
 //    the partial tiles: ~0.86 us plus ~0.058 us per segment.
 double tiled_estimate_us(int64_t M, int64_t N, int64_t K, bool fp16_in, const dg_plan& p) {
     const double elem = fp16_in ? 2.0 : 1.0;
-    const int64_t kblocks = (K + p.block_k - 1) / p.block_k;
+    const int64_t kb = fp16_in ? 64 : 128;   // one K block (a stage may hold two)
+    const int64_t kblocks = (K + kb - 1) / kb;
     const int64_t waves = (p.tiles + p.grid - 1) / p.grid;
     const double all_mb = static_cast<double>(M + N) * static_cast<double>(K) * elem / 1e6;
     const double tile_rows = static_cast<double>(std::min<int64_t>(M, p.block_m));
@@ -328,7 +330,8 @@ dg_status make_plan(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count,
     const int64_t tiles = ((M + 127) / 128) * ((N + 63) / 64);
     if (tiles > INT_MAX) return DG_ERR_UNSUPPORTED;
     auto short_k_one_wave = [&](const dg_plan& t) {
-        const int64_t kb = (K + t.block_k - 1) / t.block_k;
+        const int64_t bk = fp16_in ? 64 : 128;   // one K block (a stage may hold two)
+        const int64_t kb = (K + bk - 1) / bk;
         return t.tiles <= t.grid && kb <= 16 && 2 * static_cast<int64_t>(t.tiles) >= sm_count;
     };
     if (!splitk_off && splitk_fits && M <= kSkinnyMaxM) {

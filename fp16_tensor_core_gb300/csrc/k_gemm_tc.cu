@@ -56,18 +56,23 @@ constexpr int kStagingBytes = 4 * kBoxBytes;
 
 // Stage count = what fits in 227 KB beside the barrier block (1 KB, keeping
 // the staging boxes 1024-byte aligned), the staging boxes and the grouped
-// variant's tile prefix, at most 8.
-constexpr int stages_for(int bn, bool grouped = false) {
+// variant's tile prefix, at most 8 (4 with two K blocks per stage).
+constexpr int stages_for(int bn, bool grouped = false, int kps = 1) {
     const int st = (kSmemLimit - 1024 - 1024 - kStagingBytes - (grouped ? kGroupSmem : 0)) /
-                   (kBM * kBKBytes + bn * kBKBytes);
-    return st > 8 ? 8 : st;
+                   (kps * (kBM * kBKBytes + bn * kBKBytes));
+    return st > 8 / kps ? 8 / kps : st;
 }
 
-template <int BN, int STAGES, bool kFp16In, bool kGrouped = false>
+// KPS: K blocks per pipeline stage (1, or 2: each stage holds two adjacent
+// 128-byte K blocks of every row, so a row's 256 bytes are requested
+// together).
+template <int BN, int STAGES, bool kFp16In, bool kGrouped = false, int KPS = 1>
 struct Cfg {
-    static constexpr int kBK = kFp16In ? 64 : 128;        // K elements per stage
-    static constexpr int kABytes = kBM * kBKBytes;        // 16 KB
-    static constexpr int kBBytes = BN * kBKBytes;
+    static constexpr int kBK = kFp16In ? 64 : 128;        // K elements per K block
+    static constexpr int kABox = kBM * kBKBytes;          // 16 KB
+    static constexpr int kBBox = BN * kBKBytes;
+    static constexpr int kABytes = KPS * kABox;
+    static constexpr int kBBytes = KPS * kBBox;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // two accumulators
     static constexpr int kBarBytes = 256;
@@ -90,14 +95,14 @@ struct Tile {
     int a_row, b_row, row_end, col0, g;
 };
 
-template <int BN, int STAGES, bool kFp16In, bool kGrouped = false>
+template <int BN, int STAGES, bool kFp16In, bool kGrouped = false, int KPS = 1>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_d,
                const __grid_constant__ CUtensorMap tmap_a_edge,
                const __grid_constant__ CUtensorMap tmap_b_edge, const Params p) {
-    using C = Cfg<BN, STAGES, kFp16In, kGrouped>;
+    using C = Cfg<BN, STAGES, kFp16In, kGrouped, KPS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -147,7 +152,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int num_m = (p.M + kBM - 1) / kBM;
     const int num_n = (p.N + BN - 1) / BN;
     int num_tiles = num_m * num_n;
-    const int num_kb = (p.K + C::kBK - 1) / C::kBK;
+    // pipeline steps per tile (KPS K blocks each; a block past K loads zeros)
+    const int num_kb = ((p.K + C::kBK - 1) / C::kBK + KPS - 1) / KPS;
     // The prologue overlaps the preceding kernel's tail; the grouped tile
     // prefix reads the device offsets, so there the wait comes first, while
     // the plain kernel forms its first tile before it (below).
@@ -243,12 +249,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 } else {
                     // edge tiles load shorter boxes through their own maps
                     const bool ae = T.a_row >= p.a_edge_row, be = T.b_row >= p.b_edge_row;
-                    mbar_arrive_expect_tx(&full[stage], (ae ? p.a_edge_bytes : p.a_box_bytes) +
-                                                            (be ? p.b_edge_bytes : p.b_box_bytes));
-                    tma_load_2d(sA + stage * C::kABytes, ae ? &tmap_a_edge : &tmap_a, &full[stage],
-                                kb * C::kBK, T.a_row);
-                    tma_load_2d(sB + stage * C::kBBytes, be ? &tmap_b_edge : &tmap_b, &full[stage],
-                                kb * C::kBK, T.b_row);
+                    mbar_arrive_expect_tx(&full[stage], KPS * ((ae ? p.a_edge_bytes : p.a_box_bytes) +
+                                                               (be ? p.b_edge_bytes : p.b_box_bytes)));
+#pragma unroll
+                    for (int j = 0; j < KPS; ++j) {
+                        const int x = (kb * KPS + j) * C::kBK;
+                        tma_load_2d(sA + stage * C::kABytes + j * C::kABox,
+                                    ae ? &tmap_a_edge : &tmap_a, &full[stage], x, T.a_row);
+                        tma_load_2d(sB + stage * C::kBBytes + j * C::kBBox,
+                                    be ? &tmap_b_edge : &tmap_b, &full[stage], x, T.b_row);
+                    }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 }
@@ -277,17 +287,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!wait_bounded(&full[stage], phase, ctl)) { ok = false; break; }
                 tc_fence_after_sync();
-                const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
-                const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
 #pragma unroll
-                for (int kk = 0; kk < kBKBytes / 32; ++kk) {
-                    const uint64_t ad = sdesc_k_major_sw128(a0 + kk * 32);
-                    const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
-                    const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-                    if constexpr (kFp16In)
-                        mma_f16(d_tmem, ad, bd, C::kIdesc, accum);
-                    else
-                        mma_f8f6f4(d_tmem, ad, bd, C::kIdesc, accum);
+                for (int j = 0; j < KPS; ++j) {
+                    const uint32_t a0 = smem_addr(sA + stage * C::kABytes + j * C::kABox);
+                    const uint32_t b0 = smem_addr(sB + stage * C::kBBytes + j * C::kBBox);
+#pragma unroll
+                    for (int kk = 0; kk < kBKBytes / 32; ++kk) {
+                        const uint64_t ad = sdesc_k_major_sw128(a0 + kk * 32);
+                        const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
+                        const uint32_t accum = (kb > 0 || j > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (kFp16In)
+                            mma_f16(d_tmem, ad, bd, C::kIdesc, accum);
+                        else
+                            mma_f8f6f4(d_tmem, ad, bd, C::kIdesc, accum);
+                    }
                 }
                 issued_any = true;
                 mma_commit(&empty[stage]);   // frees the stage when these MMAs finish
@@ -402,9 +415,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
 // ------------------------------------------------------------- host side
 
-template <int BN, int STAGES, bool kFp16In, bool kGrouped = false>
+template <int BN, int STAGES, bool kFp16In, bool kGrouped = false, int KPS = 1>
 cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
-    using C = Cfg<BN, STAGES, kFp16In, kGrouped>;
+    using C = Cfg<BN, STAGES, kFp16In, kGrouped, KPS>;
     static std::mutex mu;
     static bool attr_done[64] = {};
     int dev = 0;
@@ -414,7 +427,7 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
         std::lock_guard<std::mutex> lk(mu);
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!attr_done[dev]) {
-            e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped>,
+            e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped, KPS>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
             if (e != cudaSuccess) return e;
             attr_done[dev] = true;
@@ -466,16 +479,26 @@ cudaError_t launch_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
         prm2.staged = 0;
         td = ta;
     }
-    return launch_kernel(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped>, dim3(L.plan->grid),
+    return launch_kernel(gemm_tc_kernel<BN, STAGES, kFp16In, kGrouped, KPS>, dim3(L.plan->grid),
                          dim3(kThreads), C::kSmemBytes, s, ta, tb, td, tae, tbe, prm2);
 }
 
 template <bool kFp16In>
 cudaError_t launch_in(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     switch (L.plan->block_n) {
-        case 64: return launch_cfg<64, stages_for(64), kFp16In>(L, prm, s);
-        case 96: return launch_cfg<96, stages_for(96), kFp16In>(L, prm, s);
-        case 128: return launch_cfg<128, stages_for(128), kFp16In>(L, prm, s);
+        // two K blocks per stage: block_k is twice the K block
+        case 64:
+            if (L.plan->block_k == 2 * (kFp16In ? 64 : 128))
+                return launch_cfg<64, stages_for(64, false, 2), kFp16In, false, 2>(L, prm, s);
+            return launch_cfg<64, stages_for(64), kFp16In>(L, prm, s);
+        case 96:
+            if (L.plan->block_k == 2 * (kFp16In ? 64 : 128))
+                return launch_cfg<96, stages_for(96, false, 2), kFp16In, false, 2>(L, prm, s);
+            return launch_cfg<96, stages_for(96), kFp16In>(L, prm, s);
+        case 128:
+            if (L.plan->block_k == 2 * (kFp16In ? 64 : 128))
+                return launch_cfg<128, stages_for(128, false, 2), kFp16In, false, 2>(L, prm, s);
+            return launch_cfg<128, stages_for(128), kFp16In>(L, prm, s);
         case 160: return launch_cfg<160, stages_for(160), kFp16In>(L, prm, s);
         case 192: return launch_cfg<192, stages_for(192), kFp16In>(L, prm, s);
         case 224: return launch_cfg<224, stages_for(224), kFp16In>(L, prm, s);
@@ -566,6 +589,24 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     p->tiles = static_cast<int>(tiles);
     p->grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
     p->smem_bytes = smem_for(best);
+    // One-wave plans up to 128 wide over at least 12 K blocks take two K
+    // blocks per stage: each stage then requests 256 contiguous bytes of
+    // every row of B, which streams better.  Measured on GB300 (E4M3,
+    // graph-replayed, us, one -> two): 32 x 12288 x 4096 12.87 -> 12.27,
+    // 128 x 12288 x 4096 13.28 -> 12.82, 96 x 8192 x 2048 7.84 -> 6.86,
+    // 32 x 8192 x 3072 9.73 -> 8.27, 200 x 6144 x 2048 8.12 -> 7.23,
+    // 48 x 12288 x 1536 7.28 -> 6.96; over 9 K blocks no gain and up to 4%
+    // lost on latency-bound shapes (129 x 1000 x 1040 5.33 -> 5.53).
+    // DG_TC_KPS=1|2 pins one or two for every one-wave plan up to 128 wide
+    // (sweeps).
+    const bool kps2 = kn.tc_kps == 2 || (kn.tc_kps == 0 && kblocks >= 12);
+    if (one_wave && kps2 && best <= 128) {
+        p->block_k *= 2;
+        p->stages = stages_for(best, false, 2);
+        p->smem_bytes = best == 64 ? Cfg<64, stages_for(64, false, 2), false, false, 2>::kSmemBytes
+                        : best == 96 ? Cfg<96, stages_for(96, false, 2), false, false, 2>::kSmemBytes
+                                     : Cfg<128, stages_for(128, false, 2), false, false, 2>::kSmemBytes;
+    }
 
     // CTA pairs (256 x BN tiles over sm_count / 2 clusters), for M >= 256.
     // Per-SM throughput relative to the single-CTA 128 x 256 tile: each SM

@@ -404,6 +404,9 @@ dg_status dg_release_stream(dg_stream_t stream);
  *   DG_2CTA=0|1           CTA pairs off / for every M >= 256
  *   DG_FORCE_BLOCK_N=n    tile width of the tiled kernels (64..256)
  *   DG_GROUP_M=n          raster group of M tiles (1..4096)
+ *   DG_TC_KPS=1|2         one-wave single-CTA plans up to 128 wide: one or
+ *                         two K blocks per pipeline stage (default: two
+ *                         from 12 K blocks on)
  *   DG_TC_SHORT_BOX=0|1|2 single-CTA tiled kernel: operand boxes of full
  *                         height / of the operand's rows rounded up to 8
  *                         when it has at most 32 / whenever it is shorter

@@ -426,6 +426,10 @@ def _plan_paths_and_tiles(sm):
     for m in (32, 64, 128):
         p = dg.dg_gemm_plan(m, 12288, 4096, sm_count=sm)
         assert (p["path"], p["block_m"], p["block_n"], p["tiles"], p["grid"]) == (3, 128, 96, 128, 128)
+        # two 128-byte K blocks per stage from 12 K blocks on (3 stages)
+        assert (p["block_k"], p["stages"]) == (256, 3), p
+    p = dg.dg_gemm_plan(129, 1000, 1040, sm_count=sm)   # 9 K blocks: one per stage
+    assert (p["block_n"], p["block_k"]) == (64, 128), p
     # 9..16 rows over a short K with many tiles: the one-wave tiled kernel;
     # over a long K, or with few tiles, split-K
     p = dg.dg_gemm_plan(16, 12288, 1040, sm_count=sm)

@@ -103,7 +103,8 @@ def test_grouped_widths(N):
     (32, 12288, 4096, False),   # the decode QKV projection at a batch of 32
     (17, 14336, 1040, True),    # FP16 operands
     (16, 12288, 1040, False),   # 16 rows over a short K: tiled instead of split-K
-    (12, 11008, 2048, False),
+    (12, 11008, 2048, False),   # two K blocks per stage
+    (40, 12288, 1664, False),   # 13 K blocks, two per stage: the last stage's second is past K
 ])
 def test_one_wave_96_wide(M, N, K, fp16):
     """Shapes whose every tile fits one wave only at 96 columns take the
