@@ -430,6 +430,11 @@ def _plan_paths_and_tiles(sm):
         assert (p["block_k"], p["stages"]) == (256, 3), p
     p = dg.dg_gemm_plan(129, 1000, 1040, sm_count=sm)   # 9 K blocks: one per stage
     assert (p["block_n"], p["block_k"]) == (64, 128), p
+    # the boundary: 11 K blocks one per stage, 12 two (FP16: 64-element blocks)
+    assert dg.dg_gemm_plan(32, 12288, 1408, sm_count=sm)["block_k"] == 128
+    assert dg.dg_gemm_plan(32, 12288, 1536, sm_count=sm)["block_k"] == 256
+    assert dg.dg_gemm_plan(32, 12288, 704, dg.DG_FP16, dg.DG_BF16, sm_count=sm)["block_k"] == 64
+    assert dg.dg_gemm_plan(32, 12288, 768, dg.DG_FP16, dg.DG_BF16, sm_count=sm)["block_k"] == 128
     # 9..16 rows over a short K with many tiles: the one-wave tiled kernel;
     # over a long K, or with few tiles, split-K
     p = dg.dg_gemm_plan(16, 12288, 1040, sm_count=sm)
