@@ -589,18 +589,19 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     p->tiles = static_cast<int>(tiles);
     p->grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
     p->smem_bytes = smem_for(best);
-    // One-wave plans up to 128 wide over at least 12 K blocks take two K
+    // Single-wave plans up to 128 wide over at least 12 K blocks take two K
     // blocks per stage: each stage then requests 256 contiguous bytes of
-    // every row of B, which streams better.  Measured on GB300 (E4M3,
-    // graph-replayed, us, one -> two): 32 x 12288 x 4096 12.87 -> 12.27,
-    // 128 x 12288 x 4096 13.28 -> 12.82, 96 x 8192 x 2048 7.84 -> 6.86,
-    // 32 x 8192 x 3072 9.73 -> 8.27, 200 x 6144 x 2048 8.12 -> 7.23,
-    // 48 x 12288 x 1536 7.28 -> 6.96; over 9 K blocks no gain and up to 4%
-    // lost on latency-bound shapes (129 x 1000 x 1040 5.33 -> 5.53).
-    // DG_TC_KPS=1|2 pins one or two for every one-wave plan up to 128 wide
-    // (sweeps).
+    // every row of B, which streams better, and the barrier round trips per
+    // K block halve.  Measured on GB300 (graph-replayed, us, one -> two):
+    // E4M3 32 x 12288 x 4096 12.87 -> 12.27, 128 x 12288 x 4096 13.28 ->
+    // 12.82, 96 x 8192 x 2048 7.84 -> 6.86, 32 x 8192 x 3072 9.73 -> 8.27,
+    // 48 x 12288 x 1536 7.28 -> 6.96, 256 x 4096 x 11008 26.59 -> 23.73,
+    // 2048 x 1024 x 11008 27.12 -> 22.47, 512 x 2048 x 8192 20.40 -> 16.15;
+    // FP16 1024 x 1024 x 8192 37.85 -> 32.20; over 9 K blocks no gain and up
+    // to 4% lost on latency-bound shapes (129 x 1000 x 1040 5.33 -> 5.53).
+    // DG_TC_KPS=1|2 pins one or two for every such plan (sweeps).
     const bool kps2 = kn.tc_kps == 2 || (kn.tc_kps == 0 && kblocks >= 12);
-    if (one_wave && kps2 && best <= 128) {
+    if (tiles <= sm_count && kps2 && best <= 128) {
         p->block_k *= 2;
         p->stages = stages_for(best, false, 2);
         p->smem_bytes = best == 64 ? Cfg<64, stages_for(64, false, 2), false, false, 2>::kSmemBytes
