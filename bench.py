@@ -755,7 +755,8 @@ def run_own(args):
             "bound": "tensor",
             "kernel": f"{'gemm_tc_pair_kernel' if plan['block_m'] == 256 else 'gemm_tc_kernel'} "
                       f"(tcgen05 E4M3, {plan['block_m']}x{plan['block_n']} tiles, "
-                      f"{plan['stages']} stages, grid {plan['grid']})",
+                      f"{plan['stages']} stages of {plan['block_k'] // 128} K block(s), "
+                      f"grid {plan['grid']})",
             "achieved": achieved,
             "peak": fp8_peak,
             "unit": "TFLOP/s",

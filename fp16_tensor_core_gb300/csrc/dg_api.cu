@@ -95,6 +95,7 @@ Knobs read_knobs() {
         k.splitk_tile_rows = static_cast<int>(v);
     if (env_int("DG_TC_SHORT_BOX", 0, 2, &v)) k.tc_short_box = static_cast<int>(v);
     if (env_int("DG_TC_KPS", 1, 2, &v)) k.tc_kps = static_cast<int>(v);
+    if (env_int("DG_PAIR_KPS", 1, 2, &v)) k.pair_kps = static_cast<int>(v);
     return k;
 }
 

@@ -69,6 +69,7 @@ struct Knobs {
     int splitk_tile_rows = 128;   // DG_SPLITK_TILE_ROWS=<16..128, multiple of 8> (sweeps)
     int tc_short_box = 2;         // DG_TC_SHORT_BOX (0, 1, 2): box rows of short operands
     int tc_kps = 0;               // DG_TC_KPS (1, 2; 0 planned): K blocks per stage, one-wave tiles
+    int pair_kps = 0;             // DG_PAIR_KPS (1, 2; 0 planned): K blocks per stage, CTA pairs
 };
 const Knobs& knobs();
 

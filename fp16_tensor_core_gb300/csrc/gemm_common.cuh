@@ -59,8 +59,8 @@ constexpr int kMaxGroups = 1024;
 
 // CTA-pair kernel (k_gemm_tc2.cu): shared memory and stage count of the
 // 256 x bn pair tile, and its launcher.
-int pair_smem_for(int bn);
-int pair_stages(int bn);
+int pair_smem_for(int bn, int kps);   // kps: K blocks per stage (1 or 2)
+int pair_stages(int bn, int kps);
 cudaError_t launch_gemm_tc_pair(const TcLaunch& L, const Params& prm, cudaStream_t s);
 
 namespace {

@@ -649,10 +649,19 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
             const int64_t pt = pm * ((N + pbest - 1) / pbest);
             p->block_m = 256;
             p->block_n = pbest;
-            p->stages = pair_stages(pbest);
+            // Two K blocks per stage from 12 K blocks on, as for single-CTA
+            // tiles: fewer barrier round trips per K block.  Measured on GB300
+            // (graph-replayed, us, one -> two): E4M3 4096^3 45.92 -> 43.58,
+            // HGEMM 4096^3 83.14 -> 79.59, 4096 x 4096 x 8192 85.31 ->
+            // 82.31, FP16 1024 x 4096 x 4096 25.82 -> 24.83; the 8192^3 bench
+            // step's GEMM 0.304-0.307 -> 0.298-0.301 ms.  DG_PAIR_KPS=1|2
+            // pins either (sweeps).
+            const int pkps = kn.pair_kps != 0 ? kn.pair_kps : (kblocks >= 12 ? 2 : 1);
+            p->block_k = (fp16_in ? 64 : 128) * pkps;
+            p->stages = pair_stages(pbest, pkps);
             p->tiles = static_cast<int>(pt);
             p->grid = static_cast<int>(2 * (pt < slots ? pt : slots));
-            p->smem_bytes = pair_smem_for(pbest);
+            p->smem_bytes = pair_smem_for(pbest, pkps);
         }
     }
 }

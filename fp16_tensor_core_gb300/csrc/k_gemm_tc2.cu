@@ -54,19 +54,23 @@ constexpr int kHalfBM = 128;   // rows of it per CTA
 constexpr int kStagingBytes = 4 * kBoxBytes;
 
 // Stage count: what fits in 227 KB beside the barrier block (1 KB, keeping
-// the staging boxes 1024-byte aligned) and the staging boxes, at most 8.
-constexpr int pair_stages_for(int bn) {
+// the staging boxes 1024-byte aligned) and the staging boxes, at most 8
+// (4 with two K blocks per stage).
+constexpr int pair_stages_for(int bn, int kps = 1) {
     const int st = (kSmemLimit - 1024 - 1024 - kStagingBytes) /
-                   (kHalfBM * kBKBytes + (bn / 2) * kBKBytes);
-    return st > 8 ? 8 : st;
+                   (kps * (kHalfBM * kBKBytes + (bn / 2) * kBKBytes));
+    return st > 8 / kps ? 8 / kps : st;
 }
 
-template <int BN, int STAGES, bool kFp16In>
+// KPS: K blocks per pipeline stage (1 or 2, adjacent blocks loaded together).
+template <int BN, int STAGES, bool kFp16In, int KPS = 1>
 struct PairCfg {
-    static constexpr int kBK = kFp16In ? 64 : 128;         // K elements per stage
-    static constexpr int kABytes = kHalfBM * kBKBytes;     // this CTA's 128 rows of A
+    static constexpr int kBK = kFp16In ? 64 : 128;         // K elements per K block
+    static constexpr int kABox = kHalfBM * kBKBytes;       // this CTA's 128 rows of A
     static constexpr int kBRows = BN / 2;                  // this CTA's rows of B
-    static constexpr int kBBytes = kBRows * kBKBytes;
+    static constexpr int kBBox = kBRows * kBKBytes;
+    static constexpr int kABytes = KPS * kABox;
+    static constexpr int kBBytes = KPS * kBBox;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);
     static constexpr int kStagingOff = STAGES * kStageBytes + 1024;   // after the barriers
@@ -171,12 +175,12 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     return v;
 }
 
-template <int BN, int STAGES, bool kFp16In>
+template <int BN, int STAGES, bool kFp16In, int KPS = 1>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_d, const Params p) {
-    using C = PairCfg<BN, STAGES, kFp16In>;
+    using C = PairCfg<BN, STAGES, kFp16In, KPS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -265,15 +269,24 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             if (i > 0) tile_coords(it.t, num_m, num_n, p.group_m, mt, nt);
             const int a_row = mt * kPairBM + static_cast<int>(rank) * kHalfBM;
             const int b_row = nt * BN + static_cast<int>(rank) * C::kBRows;
-            for (int kb = it.kb0; kb < it.kb1; ++kb) {
+            for (int kb = it.kb0; kb < it.kb1; kb += KPS) {
+                const int nk = min(KPS, it.kb1 - kb);   // the range's last stage may be half full
                 if (!first_lap && !wait_bounded(&empty[stage], phase ^ 1u, ctl)) { ok = false; break; }
                 if (skip) {
                     skip = false;            // leave this stage unloaded
                 } else {
-                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+                    if (leader)
+                        mbar_arrive_expect_tx(&full[stage], 2 * nk * (C::kABox + C::kBBox));
                     const uint32_t bar = leader_full + static_cast<uint32_t>(stage) * 8u;
-                    tma_load_2d_pair(sA + stage * C::kABytes, &tmap_a, bar, kb * C::kBK, a_row);
-                    tma_load_2d_pair(sB + stage * C::kBBytes, &tmap_b, bar, kb * C::kBK, b_row);
+#pragma unroll
+                    for (int j = 0; j < KPS; ++j) {
+                        if (j < nk) {
+                            tma_load_2d_pair(sA + stage * C::kABytes + j * C::kABox, &tmap_a, bar,
+                                             (kb + j) * C::kBK, a_row);
+                            tma_load_2d_pair(sB + stage * C::kBBytes + j * C::kBBox, &tmap_b, bar,
+                                             (kb + j) * C::kBK, b_row);
+                        }
+                    }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 }
@@ -301,20 +314,26 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (!wait_bounded_cluster(&acc_empty[acc], acc_phase ^ 1u, ctl)) { ok = false; break; }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                for (int kb = it.kb0; kb < it.kb1; kb += KPS) {
+                    const int nk = min(KPS, it.kb1 - kb);
                     if (!wait_bounded_cluster(&full[stage], phase, ctl)) { ok = false; break; }
                     tc_fence_after_sync();
-                    const uint32_t a0 = smem_addr(sA + stage * C::kABytes);
-                    const uint32_t b0 = smem_addr(sB + stage * C::kBBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBKBytes / 32; ++kk) {
-                        const uint64_t ad = sdesc_k_major_sw128(a0 + kk * 32);
-                        const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
-                        const uint32_t accum = (kb > it.kb0 || kk > 0) ? 1u : 0u;
-                        if constexpr (kFp16In)
-                            mma_f16_pair(d_tmem, ad, bd, C::kIdesc, accum);
-                        else
-                            mma_f8f6f4_pair(d_tmem, ad, bd, C::kIdesc, accum);
+                    for (int j = 0; j < KPS; ++j) {
+                        if (j < nk) {
+                            const uint32_t a0 = smem_addr(sA + stage * C::kABytes + j * C::kABox);
+                            const uint32_t b0 = smem_addr(sB + stage * C::kBBytes + j * C::kBBox);
+#pragma unroll
+                            for (int kk = 0; kk < kBKBytes / 32; ++kk) {
+                                const uint64_t ad = sdesc_k_major_sw128(a0 + kk * 32);
+                                const uint64_t bd = sdesc_k_major_sw128(b0 + kk * 32);
+                                const uint32_t accum = (kb > it.kb0 || j > 0 || kk > 0) ? 1u : 0u;
+                                if constexpr (kFp16In)
+                                    mma_f16_pair(d_tmem, ad, bd, C::kIdesc, accum);
+                                else
+                                    mma_f8f6f4_pair(d_tmem, ad, bd, C::kIdesc, accum);
+                            }
+                        }
                     }
                     mma_commit_pair_multicast(&empty[stage], 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -570,10 +589,10 @@ cudaError_t launch_pair(Kern kern, dim3 grid, size_t smem, cudaStream_t s,
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int BN, int STAGES, bool kFp16In>
+template <int BN, int STAGES, bool kFp16In, int KPS = 1>
 cudaError_t launch_pair_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s) {
-    using C = PairCfg<BN, STAGES, kFp16In>;
-    auto kern = gemm_tc_pair_kernel<BN, STAGES, kFp16In>;
+    using C = PairCfg<BN, STAGES, kFp16In, KPS>;
+    auto kern = gemm_tc_pair_kernel<BN, STAGES, kFp16In, KPS>;
     static std::mutex mu;
     static int max_clusters[64] = {};
     int dev = 0;
@@ -653,20 +672,38 @@ cudaError_t launch_pair_cfg(const TcLaunch& L, const Params& prm, cudaStream_t s
     return launch_pair(kern, dim3(2 * pairs), C::kSmemBytes, s, ta, tb, td, prm2);
 }
 
+// One or two K blocks per stage, as the plan says (block_k = K elements per
+// stage).
+template <int BN, bool kFp16In>
+cudaError_t launch_pair_bn(const TcLaunch& L, const Params& prm, cudaStream_t s) {
+    if (L.plan->block_k == 2 * PairCfg<BN, 1, kFp16In>::kBK)
+        return launch_pair_cfg<BN, pair_stages_for(BN, 2), kFp16In, 2>(L, prm, s);
+    return launch_pair_cfg<BN, pair_stages_for(BN), kFp16In>(L, prm, s);
+}
+
 template <bool kFp16In>
 cudaError_t launch_pair_in(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     switch (L.plan->block_n) {
-        case 128: return launch_pair_cfg<128, pair_stages_for(128), kFp16In>(L, prm, s);
-        case 160: return launch_pair_cfg<160, pair_stages_for(160), kFp16In>(L, prm, s);
-        case 192: return launch_pair_cfg<192, pair_stages_for(192), kFp16In>(L, prm, s);
-        case 224: return launch_pair_cfg<224, pair_stages_for(224), kFp16In>(L, prm, s);
-        default: return launch_pair_cfg<256, pair_stages_for(256), kFp16In>(L, prm, s);
+        case 128: return launch_pair_bn<128, kFp16In>(L, prm, s);
+        case 160: return launch_pair_bn<160, kFp16In>(L, prm, s);
+        case 192: return launch_pair_bn<192, kFp16In>(L, prm, s);
+        case 224: return launch_pair_bn<224, kFp16In>(L, prm, s);
+        default: return launch_pair_bn<256, kFp16In>(L, prm, s);
     }
 }
 
 }  // namespace
 
-int pair_smem_for(int bn) {
+int pair_smem_for(int bn, int kps) {
+    if (kps == 2) {
+        switch (bn) {
+            case 128: return PairCfg<128, pair_stages_for(128, 2), false, 2>::kSmemBytes;
+            case 160: return PairCfg<160, pair_stages_for(160, 2), false, 2>::kSmemBytes;
+            case 192: return PairCfg<192, pair_stages_for(192, 2), false, 2>::kSmemBytes;
+            case 224: return PairCfg<224, pair_stages_for(224, 2), false, 2>::kSmemBytes;
+            default: return PairCfg<256, pair_stages_for(256, 2), false, 2>::kSmemBytes;
+        }
+    }
     switch (bn) {
         case 128: return PairCfg<128, pair_stages_for(128), false>::kSmemBytes;
         case 160: return PairCfg<160, pair_stages_for(160), false>::kSmemBytes;
@@ -676,7 +713,7 @@ int pair_smem_for(int bn) {
     }
 }
 
-int pair_stages(int bn) { return pair_stages_for(bn); }
+int pair_stages(int bn, int kps) { return pair_stages_for(bn, kps); }
 
 cudaError_t launch_gemm_tc_pair(const TcLaunch& L, const Params& prm, cudaStream_t s) {
     return L.fp16_in ? launch_pair_in<true>(L, prm, s) : launch_pair_in<false>(L, prm, s);

@@ -404,6 +404,8 @@ dg_status dg_release_stream(dg_stream_t stream);
  *   DG_2CTA=0|1           CTA pairs off / for every M >= 256
  *   DG_FORCE_BLOCK_N=n    tile width of the tiled kernels (64..256)
  *   DG_GROUP_M=n          raster group of M tiles (1..4096)
+ *   DG_PAIR_KPS=1|2       CTA-pair tiles: one or two K blocks per pipeline
+ *                         stage (default: two from 12 K blocks on)
  *   DG_TC_KPS=1|2         one-wave single-CTA plans up to 128 wide: one or
  *                         two K blocks per pipeline stage (default: two
  *                         from 12 K blocks on)

@@ -443,9 +443,12 @@ def _plan_paths_and_tiles(sm):
     assert dg.dg_gemm_plan(16, 4096, 1040, sm_count=sm)["path"] == 4
     # a 96-wide one-wave plan keeps the tiled kernel over a long K too
     assert dg.dg_gemm_plan(17, 11008, 4096, sm_count=sm)["block_n"] == 96
-    # FP16 operands: 64 K elements (128 bytes) per stage
-    assert dg.dg_gemm_plan(4096, 4096, 4096, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16,
-                           sm_count=sm)["block_k"] == 64
+    # FP16 operands: 64 K elements (128 bytes) per K block; CTA pairs over
+    # 4096 K elements (64 K blocks) take two per stage
+    p = dg.dg_gemm_plan(4096, 4096, 4096, in_dtype=dg.DG_FP16, out_dtype=dg.DG_FP16, sm_count=sm)
+    assert (p["block_m"], p["block_k"]) == (256, 128), p
+    p = dg.dg_gemm_plan(4096, 4096, 4096, sm_count=sm)   # E4M3 pairs: 2 x 128 per stage
+    assert (p["block_m"], p["block_k"]) == (256, 256), p
     # edge waste: a narrow N problem gets narrower tiles than a wide one
     small = dg.dg_gemm_plan(65, 1000, 1040, sm_count=sm)
     big = dg.dg_gemm_plan(8192, 8192, 8192, sm_count=sm)
