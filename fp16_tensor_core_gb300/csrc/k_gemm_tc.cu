@@ -626,7 +626,17 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
         const int64_t pm = (M + 255) / 256;
         const int slots = sm_count / 2;
         const int pcand[5] = {256, 224, 192, 160, 128};
-        const double peff[5] = {1.06, 0.95, 0.83, 0.72, 0.58};
+        // Narrower widths with two K blocks per stage (12 K blocks on):
+        // 4096^3 E4M3, 4 / 4 / 5 / 6 / 7 rounds: 43.5 / 42.5 / 46.9 / 51.2 /
+        // 58.0 us at BN 256 / 224 / 192 / 160 / 128.  The plans this moves
+        // from single-CTA to pair tiles of the same width, measured (us,
+        // single -> pair): 3072 x 2240 x 11008 54.07 -> 50.65, 512 x 5120 x
+        // 11008 28.00 -> 26.04, 1536 x 7168 x 8192 62.14 -> 59.94, 768 x
+        // 7168 x 4096 22.51 -> 21.61, FP16 256 x 11008 x 4096 23.37 ->
+        // 23.05; 256 x 12288 x 8192 25.97 -> 26.48 and 1024 x 5120 x 2048
+        // 13.76 -> 13.92 the other way.
+        const bool pk2 = kn.pair_kps == 2 || (kn.pair_kps == 0 && kblocks >= 12);
+        const double peff[5] = {1.06, 0.95, pk2 ? 0.92 : 0.83, pk2 ? 0.84 : 0.72, pk2 ? 0.68 : 0.58};
         int pbest = 256;
         double pcost = 0.0;
         for (int i = 0; i < 5; ++i) {
