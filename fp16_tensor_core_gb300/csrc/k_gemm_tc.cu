@@ -612,11 +612,13 @@ void plan_tc(int64_t M, int64_t N, int64_t K, bool fp16_in, int sm_count, dg_pla
     // CTA pairs (256 x BN tiles over sm_count / 2 clusters), for M >= 256.
     // Per-SM throughput relative to the single-CTA 128 x 256 tile: each SM
     // stores and reads only half of the tile's B rows.  Measured on GB300:
-    // 8192^3 E4M3 3607 vs 3399 TFLOP/s (1.06).  A pair MMA costs about the
-    // same whatever its N (4096^3 E4M3, interleaved: 45.6 / 45.7 / 53.4 /
-    // 61.3 / 70.3 us at BN 256 / 224 / 192 / 160 / 128 over 4 / 4 / 5 / 6 /
-    // 7 waves), so the narrower widths' relative rates are below their
-    // share of 256.  A partial last wave whose tiles the kernel splits along
+    // 8192^3 E4M3 3607 vs 3399 TFLOP/s (1.06).  With one K block per stage
+    // a pair tile cost about the same whatever its N (4096^3 E4M3,
+    // interleaved: 45.6 / 45.7 / 53.4 / 61.3 / 70.3 us at BN 256 / 224 /
+    // 192 / 160 / 128 over 4 / 4 / 5 / 6 / 7 waves): the per-K-block
+    // barrier round trip set the pace, so the narrower widths' relative
+    // rates were below their share of 256; two K blocks per stage raise
+    // them (below).  A partial last wave whose tiles the kernel splits along
     // K (two to four K ranges per tile over idle pairs) counts as that
     // fraction of a wave.  Pairs are used when their estimate is no worse;
     // DG_2CTA=0 disables them, DG_2CTA=1 forces them for M >= 256.
