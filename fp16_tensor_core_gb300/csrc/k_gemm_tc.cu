@@ -13,7 +13,9 @@
 //    multi-stage prefetch pipeline ([FP8-guide] §2.3, §4.4; [HGEMM-L2]
 //    §3.2-§3.3) -> one TMA producer thread, one MMA-issuing thread and four
 //    epilogue warps, joined by full/empty mbarriers over a STAGES-deep
-//    shared-memory ring;
+//    shared-memory ring; single-wave plans up to 128 wide over at least 12
+//    K blocks hold two adjacent K blocks per stage (256 contiguous bytes of
+//    every operand row per request, half the barrier round trips);
 //  * bank-conflict-free shared-memory layout ([DG-FP16] §3.2) -> TMA's
 //    128-byte swizzle, which the MMA's shared-memory descriptors read
 //    natively;
@@ -21,7 +23,10 @@
 //    the output scale divided out for FP8 output ([FP8-guide] §3.2);
 //  * M/N edges by predication and K tails by zero fill, in one kernel
 //    ([FP8-guide] §3.3) -> TMA fills out-of-range box elements with zeros,
-//    and epilogue stores are predicated on m < M, n < N.
+//    and epilogue stores are predicated on m < M, n < N; an operand that
+//    ends inside a tile loads that last tile through a second tensor map
+//    whose box is the rows left rounded up to 8, since rows of a box past
+//    the tensor's end still cross into the SM.
 // The kernel is persistent (one CTA per SM, tiles strided by the grid) and
 // double-buffers the accumulator in tensor memory so that the epilogue of
 // one tile overlaps the main loop of the next; the epilogue writes each

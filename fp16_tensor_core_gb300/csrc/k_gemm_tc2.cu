@@ -12,10 +12,16 @@
 // shared memory and that the MMA reads from it, the traffic that limits the
 // single-CTA kernel with 128 x 256 tiles.
 //
+// From 12 K blocks on a stage holds two adjacent K blocks (KPS = 2): half
+// the full/empty round trips per K block, which with one per stage set a
+// floor on the time per K block above the MMA's own for tiles under 256
+// wide.
+//
 // Signalling (all waits bounded):
 //  * each CTA's producer loads its halves into its own shared memory; every
 //    box completes on the even CTA's `full` barrier of the stage, whose
-//    producer arms it for the bytes of both CTAs;
+//    producer arms it for the bytes of both CTAs (of the stage's K blocks
+//    within the item's K range);
 //  * the even CTA's MMA thread issues the pair MMAs and frees a stage in both
 //    CTAs with one multicast commit to `empty`; at the end of a tile it
 //    commits to `acc_full` in both CTAs;
