@@ -441,6 +441,17 @@ def _plan_paths_and_tiles(sm):
     assert (p["path"], p["block_n"], p["tiles"]) == (3, 96, 128), p
     assert dg.dg_gemm_plan(16, 12288, 4096, sm_count=sm)["path"] == 4
     assert dg.dg_gemm_plan(16, 4096, 1040, sm_count=sm)["path"] == 4
+    # the rule's edges: 16 K blocks tiled, 17 split-K; 76 tiles (half the
+    # SMs) tiled, 75 split-K
+    assert dg.dg_gemm_plan(16, 12288, 2048, sm_count=sm)["path"] == 3
+    assert dg.dg_gemm_plan(16, 12288, 2176, sm_count=sm)["path"] == 4
+    assert dg.dg_gemm_plan(16, 4864, 1040, sm_count=sm)["path"] == 3
+    assert dg.dg_gemm_plan(16, 4800, 1040, sm_count=sm)["path"] == 4
+    # CTA pairs: two K blocks per stage from 12 K blocks on (3 stages of 64 KB)
+    p = dg.dg_gemm_plan(8192, 8192, 1408, sm_count=sm)
+    assert (p["block_m"], p["block_k"], p["stages"]) == (256, 128, 6), p
+    p = dg.dg_gemm_plan(8192, 8192, 1536, sm_count=sm)
+    assert (p["block_m"], p["block_k"], p["stages"]) == (256, 256, 3), p
     # a 96-wide one-wave plan keeps the tiled kernel over a long K too
     assert dg.dg_gemm_plan(17, 11008, 4096, sm_count=sm)["block_n"] == 96
     # FP16 operands: 64 K elements (128 bytes) per K block; CTA pairs over
